@@ -1,0 +1,136 @@
+"""fp64 CPU oracle for Jagged Flash Attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The CUDA library never does; the two share no
+code.  The arithmetic lives in ``jfa_oracle.c`` (plain C, fp64, OpenMP) and
+follows the definition written at the top of that file: per sequence and
+head, softmax(scale * Q K^T) V with its analytic gradients, looping over the
+offsets tensor ("Why attention in GEM needed a rewrite", Meta's TLX Jagged
+Flash Attention Beats FA4 on Blackwell With 3x Less Code); broadcast-Q sums
+dQ over the batch (Meta's 3.2K-line Triton kernel outruns FlashAttention-4 on
+jagged Blackwell attention, second paragraph).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (brute force
+against padded dense attention with torch autograd in fp64, invariants,
+closed forms, a hand-derived worked example under ``tests/golden/``, central
+finite differences, and the broadcast dQ batch sum).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "jfa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libjfa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile one oracle source file into a shared library at ``out``."""
+    tmp = out + f".tmp{os.getpid()}"
+    # -ffp-contract=off keeps every multiply and add a separately rounded fp64 op.
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2 -fopenmp) if stale.  Returns the .so path."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        compile_source(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _offsets_arg(offsets):
+    offsets = offsets.detach().cpu().to(torch.int32).contiguous()
+    return offsets, ctypes.cast(offsets.data_ptr(), ctypes.POINTER(ctypes.c_int32))
+
+
+def _inputs(*ts):
+    """All-bf16 inputs pass as raw bf16 (widened exactly in C); anything else as fp64."""
+    ts = [t.detach().cpu().contiguous() for t in ts]
+    if all(t.dtype == torch.bfloat16 for t in ts):
+        return ts, 1
+    return [t.to(torch.float64).contiguous() for t in ts], 0
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        vp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)
+        ci, cd = ctypes.c_int, ctypes.c_double
+        lib.jfa_oracle_fwd.argtypes = [vp, vp, vp, ci, i32p, ci, ci, ci, ci, ci, ci, cd, vp, vp]
+        lib.jfa_oracle_fwd.restype = None
+        lib.jfa_oracle_bwd.argtypes = [vp, vp, vp, vp, ci, i32p, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp]
+        lib.jfa_oracle_bwd.restype = None
+        lib.jfa_oracle_max_threads.argtypes = []
+        lib.jfa_oracle_max_threads.restype = ci
+        self.lib = lib
+        self.path = path
+
+    def max_threads(self) -> int:
+        return int(self.lib.jfa_oracle_max_threads())
+
+    def fwd(self, q, k, v, offsets, Lq: int, broadcast_q: bool, causal: bool, scale: float,
+            want_o: bool = True, want_lse: bool = True):
+        """O (fp64, [B,Lq,H,D] or [N,H,D]) and LSE (fp64, [B,H,Lq] or [H,N])."""
+        offsets, off_p = _offsets_arg(offsets)
+        B = offsets.numel() - 1
+        N = int(offsets[-1]) if B > 0 else 0
+        H, D = k.shape[1], k.shape[2]
+        (qq, kk, vv), bf = _inputs(q, k, v)
+        o = torch.zeros((B, Lq, H, D) if broadcast_q else (N, H, D), dtype=torch.float64) if want_o else None
+        lse = torch.zeros((B, H, Lq) if broadcast_q else (H, N), dtype=torch.float64) if want_lse else None
+        self.lib.jfa_oracle_fwd(_ptr(qq), _ptr(kk), _ptr(vv), bf, off_p, B, Lq, H, D,
+                                int(broadcast_q), int(causal), float(scale), _ptr(o), _ptr(lse))
+        return o, lse
+
+    def bwd(self, q, k, v, do, offsets, Lq: int, broadcast_q: bool, causal: bool, scale: float,
+            want_dq: bool = True, want_dkv: bool = True):
+        """dQ (fp64, shaped like Q), dK and dV (fp64, [N,H,D]) for upstream gradient dO."""
+        offsets, off_p = _offsets_arg(offsets)
+        B = offsets.numel() - 1
+        N = int(offsets[-1]) if B > 0 else 0
+        H, D = k.shape[1], k.shape[2]
+        (qq, kk, vv, dd), bf = _inputs(q, k, v, do)
+        dq = torch.zeros(tuple(q.shape), dtype=torch.float64) if want_dq else None
+        dk = torch.zeros((N, H, D), dtype=torch.float64) if want_dkv else None
+        dv = torch.zeros((N, H, D), dtype=torch.float64) if want_dkv else None
+        self.lib.jfa_oracle_bwd(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(dd), bf, off_p, B, Lq, H, D,
+                                int(broadcast_q), int(causal), float(scale),
+                                _ptr(dq), _ptr(dk), _ptr(dv))
+        return dq, dk, dv
+
+
+def _default() -> Oracle:
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = Oracle(build())
+    return _lib
+
+
+def max_threads() -> int:
+    return _default().max_threads()
+
+
+def fwd(*args, **kwargs):
+    return _default().fwd(*args, **kwargs)
+
+
+def bwd(*args, **kwargs):
+    return _default().bwd(*args, **kwargs)
