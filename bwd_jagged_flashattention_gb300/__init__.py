@@ -1,0 +1,203 @@
+"""Jagged Flash Attention for GB300 (sm_103a): thin Python binding over libjfa.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only marshals torch tensors (device memory and the current stream) into the
+C ABI declared in ``include/jfa.h``.  There is no CPU fallback: if the
+library is missing or a call fails, an exception is raised.
+
+The operation is FlashAttention applied directly to packed, unpadded Q/K/V
+with an int32 offsets tensor ("Why attention in GEM needed a rewrite", Meta's
+TLX Jagged Flash Attention Beats FA4 on Blackwell With 3x Less Code), with an
+optional broadcast Q whose gradient is summed over the batch (Meta's 3.2K-line
+Triton kernel outruns FlashAttention-4 on jagged Blackwell attention, second
+paragraph).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libjfa.so")
+
+JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUDA, JFA_ERR_DEVICE_TIMEOUT = range(6)
+
+# Every symbol include/jfa.h and include/jfa_selftest.h declare.
+EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
+            "jfa_num_ctas", "jfa_selftest_mma")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class JFAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                  "(python bwd_jagged_flashattention_gb300/buildlib.py)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32p, ci, cf, sz = (ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.c_int,
+                                    ctypes.c_float, ctypes.c_size_t)
+            L.jfa_workspace_bytes.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+            L.jfa_workspace_bytes.restype = sz
+            L.jfa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp, sz, vp]
+            L.jfa_fwd.restype = ci
+            L.jfa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp, vp, sz, vp]
+            L.jfa_bwd.restype = ci
+            L.jfa_device_status.argtypes = [vp, vp]
+            L.jfa_device_status.restype = ci
+            L.jfa_status_string.argtypes = [ci]
+            L.jfa_status_string.restype = ctypes.c_char_p
+            L.jfa_num_ctas.argtypes = []
+            L.jfa_num_ctas.restype = ci
+            L.jfa_selftest_mma.argtypes = [ci, vp, vp, vp, vp, vp]
+            L.jfa_selftest_mma.restype = ci
+            L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
+            L.jfa_host_build_schedule.restype = ctypes.c_longlong
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().jfa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != JFA_OK:
+        raise JFAError(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_bytes(B: int, total_len: int, Lq: int, H: int, D: int, broadcast_q: bool, causal: bool) -> int:
+    n = lib().jfa_workspace_bytes(B, total_len, Lq, H, D, int(broadcast_q), int(causal))
+    if n == 0:
+        raise JFAError(JFA_ERR_UNSUPPORTED, "jfa_workspace_bytes")
+    return int(n)
+
+
+def new_workspace(B: int, total_len: int, Lq: int, H: int, D: int, broadcast_q: bool, causal: bool,
+                  device) -> torch.Tensor:
+    """A workspace for these sizes; the status word at its start is zeroed."""
+    ws = torch.empty(workspace_bytes(B, total_len, Lq, H, D, broadcast_q, causal), dtype=torch.uint8,
+                     device=device)
+    ws[:256].zero_()
+    return ws
+
+
+def _host_offsets(offsets, offsets_host):
+    if offsets_host is None:
+        offsets_host = offsets.detach().to("cpu", torch.int32)
+    offsets_host = offsets_host.to(torch.int32).contiguous()
+    assert offsets_host.device.type == "cpu"
+    return offsets_host
+
+
+def fwd(q, k, v, offsets, Lq: int | None = None, broadcast_q: bool = True, causal: bool = False,
+        scale: float | None = None, offsets_host=None, workspace=None, out=None, lse=None):
+    """O (bf16) and LSE (fp32).  q [Lq,H,D] (broadcast) or [N,H,D]; k, v [N,H,D]."""
+    assert q.is_cuda and q.dtype == torch.bfloat16 and k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16
+    H, D = k.shape[1], k.shape[2]
+    offsets_host = _host_offsets(offsets, offsets_host)
+    B = offsets_host.numel() - 1
+    N = int(offsets_host[-1]) if B > 0 else 0
+    Lq = q.shape[0] if broadcast_q else 0
+    o_shape = (B, Lq, H, D) if broadcast_q else (N, H, D)
+    lse_shape = (B, H, Lq) if broadcast_q else (H, N)
+    out = torch.empty(o_shape, dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = new_workspace(B, N, Lq, H, D, broadcast_q, causal, q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    offsets_dev = offsets if (offsets is not None and offsets.is_cuda) else None
+    st = lib().jfa_fwd(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()),
+                       _ptr(offsets_dev), ctypes.c_void_p(offsets_host.data_ptr()),
+                       B, Lq, H, D, int(broadcast_q), int(causal), sc, _ptr(out), _ptr(lse),
+                       _ptr(workspace), workspace.numel(), _stream(q.device))
+    _check(st, "jfa_fwd")
+    return out, lse
+
+
+def bwd(q, k, v, o, lse, do, offsets, broadcast_q: bool = True, causal: bool = False,
+        scale: float | None = None, offsets_host=None, workspace=None, dq=None, dk=None, dv=None):
+    """dQ (fp32, shaped like q), dK and dV (bf16, [N,H,D])."""
+    H, D = k.shape[1], k.shape[2]
+    offsets_host = _host_offsets(offsets, offsets_host)
+    B = offsets_host.numel() - 1
+    N = int(offsets_host[-1]) if B > 0 else 0
+    Lq = q.shape[0] if broadcast_q else 0
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
+    if workspace is None:
+        workspace = new_workspace(B, N, Lq, H, D, broadcast_q, causal, q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    offsets_dev = offsets if (offsets is not None and offsets.is_cuda) else None
+    st = lib().jfa_bwd(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()), _ptr(o.contiguous()),
+                       _ptr(lse.contiguous()), _ptr(do.contiguous()), _ptr(offsets_dev),
+                       ctypes.c_void_p(offsets_host.data_ptr()), B, Lq, H, D, int(broadcast_q), int(causal), sc,
+                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(q.device))
+    _check(st, "jfa_bwd")
+    return dq, dk, dv
+
+
+def device_status(workspace, device=None) -> int:
+    """Synchronises the current stream and returns (and clears) the kernels' status word."""
+    device = workspace.device if device is None else device
+    return int(lib().jfa_device_status(_ptr(workspace), _stream(device)))
+
+
+def num_ctas() -> int:
+    return int(lib().jfa_num_ctas())
+
+
+def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool, is_bwd: bool, P: int,
+                  policy: int = 0):
+    """The host scheduler alone (no GPU): returns (items int32 [n,4], cta_start int32 [P+1])."""
+    off = offsets_host.to(torch.int32).contiguous()
+    B = off.numel() - 1
+    N = int(off[-1]) if B > 0 else 0
+    cap = H * (N // 128 + B) + H * B * ((max(Lq, 0) + 255) // 256) + 1
+    items = torch.zeros((cap, 4), dtype=torch.int32)
+    starts = torch.zeros(P + 1, dtype=torch.int32)
+    n = lib().jfa_host_build_schedule(ctypes.c_void_p(off.data_ptr()), B, Lq, H, int(broadcast_q), int(causal),
+                                      int(is_bwd), P, policy, ctypes.c_void_p(items.data_ptr()),
+                                      ctypes.c_void_p(starts.data_ptr()), cap)
+    if n < 0:
+        raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
+    return items[:n].clone(), starts
+
+
+def selftest_mma(mode: int, a, b):
+    """One 128x128x128 tcgen05 product (see include/jfa_selftest.h); returns (C fp32, status word)."""
+    c = torch.empty((128, 128), dtype=torch.float32, device=a.device)
+    status = torch.zeros(1, dtype=torch.int32, device=a.device)
+    st = lib().jfa_selftest_mma(mode, _ptr(a.contiguous()), _ptr(b.contiguous()), _ptr(c), _ptr(status),
+                                _stream(a.device))
+    if st != 0:
+        raise JFAError(st, "jfa_selftest_mma")
+    return c, status

@@ -1,0 +1,626 @@
+// bwd.cu -- Jagged Flash Attention backward for sm_103a.
+//
+// Two kernels:
+//   jfa_bwd_pre    Delta = rowsum(dO * O) in fp32 (LSE layout).  The pages do
+//                  not name it; FlashAttention's backward needs it.
+//   jfa_bwd_kernel persistent, warp-specialised main pass.
+//
+// The main pass walks items (sequence b, head h, key/value tile n of 128
+// rows) and loops over the query tiles that see that key tile.  For query
+// tile i (128 rows), with K, V the item's tiles:
+//   S^T  = K Q_i^T                       (TMEM, fp32)
+//   dP^T = V dO_i^T                      (TMEM, fp32)
+//   P^T  = exp(scale S^T - LSE_i)        (bf16, written over S^T in TMEM)
+//   dV  += P^T dO_i                      (A operand straight from TMEM)
+//   dS^T = P^T * (dP^T - Delta_i)        (bf16, shared memory)
+//   dK  += dS^T Q_i                      (TMEM accumulator for the item)
+//   dQ_i = dS_i K                        (TMEM, over the dP^T columns)
+// dQ_i is read out by a dedicated warpgroup, which frees its TMEM columns at
+// once and then streams it through two 16-column fp32 shared-memory stages (64-byte swizzle)
+// into TMA bulk reduce-adds on the global fp32 dQ.  In broadcast-Q mode every
+// sequence adds into the same dQ [Lq,H,D]: the pages call this contended
+// reduction the first backward bottleneck and hide it with a double-buffered
+// shared-memory pipeline and an early release of the dQ tensor memory
+// (Meta's TLX Jagged Flash Attention Beats FA4 on Blackwell With 3x Less
+// Code, section "Optimizations layered on top"; Meta's 3.2K-line Triton
+// kernel outruns FlashAttention-4 on jagged Blackwell attention, second
+// paragraph).  dK/dV stay in TMEM for the whole item and are written once.
+//
+// Roles (320 threads):
+//   warps 0-3  compute: P^T and dS^T (thread r = key row r = TMEM lane r)
+//   warps 4-7  dQ readout + reduce-add; dK/dV epilogue
+//   warp  8    loads: K, V per item; Q_i (+ LSE_i, Delta_i) and dO_i per tile
+//   warp  9    tcgen05 MMA issue and TMEM allocation
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace jfa {
+namespace {
+
+constexpr int kBwdThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int kSlabBytes = 16384;
+    static constexpr int kSlabs = D / 64;
+    static constexpr int kTileBytes = kSlabs * kSlabBytes;
+    static constexpr int kK = 0;
+    static constexpr int kV = kTileBytes;
+    static constexpr int kQ = 2 * kTileBytes;   // two stages
+    static constexpr int kDO = 4 * kTileBytes;  // one stage
+    static constexpr int kDS = 5 * kTileBytes;  // 128 x 128 bf16 = 32 KB
+    static constexpr int kDQ = kDS + 32768;     // two stages of 128 x 16 fp32
+    static constexpr int kDQStage = 128 * 16 * 4;
+    static constexpr int kStats = kDQ + 2 * kDQStage;  // two stages of {lse2[128], delta[128]}
+    static constexpr int kBytes = kStats + 2 * 1024;
+    static constexpr int kDynSmem = kBytes + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
+};
+
+struct BwdBars {
+    uint64_t k_full, k_empty, v_full, v_empty;
+    uint64_t q_full[2], q_empty[2];
+    uint64_t do_full, do_empty;
+    uint64_t s_full, dp_full, p_full, ds_full, ds_empty;
+    uint64_t dq_full, dq_empty;
+    uint64_t dkv_full, dkv_empty;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+struct BwdItem {
+    int b, h, kv_start, Lk, n, q_row0, o_row0, q_rows, i0, i1;
+};
+
+__device__ __forceinline__ BwdItem decode_bwd(const WorkItem& w, const BwdParams& p) {
+    BwdItem it;
+    it.b = w.b;
+    it.kv_start = w.kv_start;
+    it.Lk = w.kv_len;
+    it.h = static_cast<int>(w.packed & 0xFFu);
+    it.n = static_cast<int>((w.packed >> 8) & 0x7FFFFFu);
+    it.q_row0 = p.broadcast_q ? 0 : w.kv_start;
+    it.o_row0 = p.broadcast_q ? w.b * p.Lq : w.kv_start;
+    it.q_rows = p.broadcast_q ? p.Lq : w.kv_len;
+    it.i0 = p.causal ? it.n : 0;
+    it.i1 = (it.q_rows + 127) / 128;
+    return it;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Uniform decision across the 128 threads of named barrier `id`.
+__device__ __forceinline__ bool group_all(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// C(tmem) = A B^T with both operands K-major [rows][D] (S^T = K Q^T, dP^T = V dO^T).
+template <int D>
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(d_tmem, smem_desc(a_addr + off, 16, 1024), smem_desc(b_addr + off, 16, 1024), idesc, kk > 0);
+    }
+}
+
+// dV (+)= P^T dO: A = P^T from TMEM (bf16 pairs), B = dO_i [q][D] MN-major.
+template <int D>
+__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint32_t do_addr, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(do_addr + kk * 2048, 16384, 1024), idesc, (acc | kk) != 0);
+}
+
+// dK (+)= dS^T Q: A = dS^T [key][q] K-major (smem), B = Q_i [q][D] MN-major.
+template <int D>
+__device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint32_t ds_addr, uint32_t q_addr, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk / 4) * 16384 + (kk % 4) * 32;
+        mma_ss(d_tmem, smem_desc(ds_addr + aoff, 16, 1024), smem_desc(q_addr + kk * 2048, 16384, 1024), idesc,
+               (acc | kk) != 0);
+    }
+}
+
+// dQ = dS K: A = dS [q][key] read MN-major from the dS^T buffer, B = K [key][D] MN-major.
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_addr, uint32_t k_addr) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 1, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ss(d_tmem, smem_desc(ds_addr + kk * 2048, 16384, 1024), smem_desc(k_addr + kk * 2048, 16384, 1024),
+               idesc, kk > 0);
+}
+
+// ---------------------------------------------------------------------------
+// Load warp (all 32 lanes: lane 0 issues TMA, every lane stages statistics).
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* smem, BwdBars& bars, int ib, int ie,
+                              const AbortState& ab) {
+    using L = BwdLayout<D>;
+    const int lane = threadIdx.x % 32;
+    if (lane == 0) {
+        prefetch_tensormap(&m->q);
+        prefetch_tensormap(&m->k);
+        prefetch_tensormap(&m->v);
+        prefetch_tensormap(&m->dout);
+    }
+    uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, do_cnt = 0;
+    for (int idx = ib; idx < ie; ++idx) {
+        const BwdItem it = decode_bwd(p.items[idx], p);
+        const int kv_row = it.kv_start + 128 * it.n;
+        if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.k_full, L::kTileBytes);
+#pragma unroll
+            for (int s = 0; s < L::kSlabs; ++s)
+                tma_load_2d(smem + L::kK + s * L::kSlabBytes, &m->k, &bars.k_full, it.h * D + 64 * s, kv_row);
+        }
+        ++k_cnt;
+        if (!mbar_wait_warp(&bars.v_empty, (v_cnt & 1) ^ 1, ab)) goto done;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars.v_full, L::kTileBytes);
+#pragma unroll
+            for (int s = 0; s < L::kSlabs; ++s)
+                tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.v_full, it.h * D + 64 * s, kv_row);
+        }
+        ++v_cnt;
+        for (int i = it.i0; i < it.i1; ++i) {
+            const int st = q_cnt % 2;
+            if (!mbar_wait_warp(&bars.q_empty[st], ((q_cnt / 2) & 1) ^ 1, ab)) goto done;
+            // LSE_i (as log2) and Delta_i for the 128 queries of the tile.
+            float* lse2 = reinterpret_cast<float*>(smem + L::kStats + st * 1024);
+            float* delta = lse2 + 128;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int qi = 128 * i + lane * 4 + e;
+                float l2 = INFINITY, dl = 0.0f;
+                if (qi < it.q_rows) {
+                    const int64_t si = p.broadcast_q ? (static_cast<int64_t>(it.b) * p.H + it.h) * p.Lq + qi
+                                                     : static_cast<int64_t>(it.h) * p.N + it.q_row0 + qi;
+                    const float lv = p.lse[si];
+                    l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
+                    dl = p.delta[si];
+                }
+                lse2[lane * 4 + e] = l2;
+                delta[lane * 4 + e] = dl;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars.q_full[st], L::kTileBytes);
+#pragma unroll
+                for (int s = 0; s < L::kSlabs; ++s)
+                    tma_load_2d(smem + L::kQ + st * L::kTileBytes + s * L::kSlabBytes, &m->q, &bars.q_full[st],
+                                it.h * D + 64 * s, it.q_row0 + 128 * i);
+            }
+            ++q_cnt;
+            if (!mbar_wait_warp(&bars.do_empty, (do_cnt & 1) ^ 1, ab)) goto done;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars.do_full, L::kTileBytes);
+#pragma unroll
+                for (int s = 0; s < L::kSlabs; ++s)
+                    tma_load_2d(smem + L::kDO + s * L::kSlabBytes, &m->dout, &bars.do_full, it.h * D + 64 * s,
+                                it.o_row0 + 128 * i);
+            }
+            ++do_cnt;
+        }
+    }
+done:
+    // Let every issued copy land before the CTA can exit.
+    if (lane == 0) {
+        if (k_cnt) mbar_wait_drain(&bars.k_full, (k_cnt - 1) & 1);
+        if (v_cnt) mbar_wait_drain(&bars.v_full, (v_cnt - 1) & 1);
+        for (uint32_t c = q_cnt > 2 ? q_cnt - 2 : 0; c < q_cnt; ++c) mbar_wait_drain(&bars.q_full[c % 2], (c / 2) & 1);
+        if (do_cnt) mbar_wait_drain(&bars.do_full, (do_cnt - 1) & 1);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread).
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
+                             const AbortState& ab) {
+    using L = BwdLayout<D>;
+    const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
+    const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO), sDS = smem_u32(smem + L::kDS);
+    uint32_t it_cnt = 0, q_cnt = 0, tile_cnt = 0;
+    for (int idx = ib; idx < ie; ++idx) {
+        const BwdItem it = decode_bwd(p.items[idx], p);
+        if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
+        if (!mbar_wait(&bars.v_full, it_cnt & 1, ab)) goto done;
+        for (int i = it.i0; i < it.i1; ++i) {
+            const int st = q_cnt % 2;
+            if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
+            tc_fence_after();
+            issue_kmajor<D>(tmem + L::kColS, sK, sQ + st * L::kTileBytes);  // S^T = K Q^T
+            mma_commit(&bars.s_full);
+            if (!mbar_wait(&bars.do_full, tile_cnt & 1, ab)) goto done;
+            if (!mbar_wait(&bars.dq_empty, (tile_cnt & 1) ^ 1, ab)) goto done;  // previous dQ read out
+            tc_fence_after();
+            issue_kmajor<D>(tmem + L::kColDP, sV, sDO);  // dP^T = V dO^T
+            mma_commit(&bars.dp_full);
+            if (i == it.i1 - 1) mma_commit(&bars.v_empty);
+            if (i == it.i0) {
+                if (!mbar_wait(&bars.dkv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+            }
+            if (!mbar_wait(&bars.p_full, tile_cnt & 1, ab)) goto done;
+            tc_fence_after();
+            issue_dv<D>(tmem + L::kColDV, tmem + L::kColS, sDO, i > it.i0);
+            mma_commit(&bars.do_empty);
+            if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
+            tc_fence_after();
+            issue_dk<D>(tmem + L::kColDK, sDS, sQ + st * L::kTileBytes, i > it.i0);
+            mma_commit(&bars.q_empty[st]);
+            issue_dq<D>(tmem + L::kColDP, sDS, sK);
+            mma_commit(&bars.dq_full);
+            mma_commit(&bars.ds_empty);
+            ++q_cnt;
+            ++tile_cnt;
+        }
+        mma_commit(&bars.dkv_full);
+        mma_commit(&bars.k_empty);
+        ++it_cnt;
+    }
+done:
+    mma_commit(&bars.mma_done);
+    mbar_wait_drain(&bars.mma_done, 0);
+}
+
+// ---------------------------------------------------------------------------
+// Compute warpgroup: P^T into TMEM, dS^T into shared memory.
+// ---------------------------------------------------------------------------
+template <int D, bool kMask>
+__device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* lse2, uint32_t s_addr, int key,
+                                              int qbase, int q_rows, bool row_valid) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(s_addr + c * 32, sr);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int q0 = c * 32 + 2 * e;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, -lse2[q0]));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, -lse2[q0 + 1]));
+            if (kMask) {
+                const int qa = qbase + q0, qb = qa + 1;
+                if (!(row_valid && qa < q_rows && (!p.causal || key <= qa))) p0 = 0.0f;
+                if (!(row_valid && qb < q_rows && (!p.causal || key <= qb))) p1 = 0.0f;
+            }
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c * 16, pk);
+    }
+    tmem_st_wait();
+}
+
+template <int D>
+__device__ __forceinline__ void bwd_compute_ds(const float* delta, uint32_t s_addr, uint32_t dp_addr, uint8_t* ds_tile,
+                                               int row) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32], pp[16];
+        tmem_ld32(dp_addr + c * 32, dp);
+        tmem_ld16(s_addr + c * 16, pp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int q0 = c * 32 + 2 * e;
+            const float d0 = bf16lo_to_f32(pp[e]) * (__uint_as_float(dp[2 * e]) - delta[q0]);
+            const float d1 = bf16hi_to_f32(pp[e]) * (__uint_as_float(dp[2 * e + 1]) - delta[q0 + 1]);
+            pk[e] = pack_bf16x2(d0, d1);
+        }
+        // Row `row`, queries c*32 .. c*32+31: slab c/2, 16-byte chunks (c%2)*4 .. +3,
+        // stored at chunk ^ (row % 8) (128-byte swizzle, as TMA would place them).
+        uint8_t* slab = ds_tile + (c / 2) * 16384 + row * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int chunk = ((c % 2) * 4 + v) ^ (row % 8);
+            *reinterpret_cast<uint4*>(slab + chunk * 16) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+    }
+}
+
+template <int D>
+__device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
+                                 const AbortState& ab) {
+    using L = BwdLayout<D>;
+    const int row = threadIdx.x;  // 0..127
+    const uint32_t lane_off = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + L::kColS;
+    const uint32_t dp_addr = tmem + lane_off + L::kColDP;
+    uint8_t* ds_tile = smem + L::kDS;
+    uint32_t q_cnt = 0, tile_cnt = 0;
+    for (int idx = ib; idx < ie; ++idx) {
+        const BwdItem it = decode_bwd(p.items[idx], p);
+        const int key = 128 * it.n + row;
+        const bool row_valid = key < it.Lk;
+        const bool kv_full_tile = 128 * (it.n + 1) <= it.Lk;
+        for (int i = it.i0; i < it.i1; ++i) {
+            const int st = q_cnt % 2;
+            const float* lse2 = reinterpret_cast<const float*>(smem + L::kStats + st * 1024);
+            const float* delta = lse2 + 128;
+            if (!mbar_wait_warp(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
+            if (!mbar_wait_warp(&bars.s_full, tile_cnt & 1, ab)) goto done;
+            tc_fence_after();
+            const bool unmasked = kv_full_tile && 128 * (i + 1) <= it.q_rows && !(p.causal && i == it.n);
+            if (unmasked)
+                bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
+            else
+                bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
+            tc_fence_before();
+            mbar_arrive(&bars.p_full);
+            if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
+            if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
+            tc_fence_after();
+            bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.ds_full);
+            ++q_cnt;
+            ++tile_cnt;
+        }
+    }
+done:;
+}
+
+// ---------------------------------------------------------------------------
+// dQ warpgroup: TMEM dQ -> registers (release TMEM) -> two 128x16 fp32 smem
+// stages -> TMA bulk reduce-add into global dQ.  Then the item's dK/dV.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8_t* smem, BwdBars& bars,
+                            uint32_t tmem, int ib, int ie, const AbortState& ab) {
+    using L = BwdLayout<D>;
+    const int r = threadIdx.x - 128;  // query row of the tile (TMEM lane)
+    const bool issuer = r == 0;
+    const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x / 32) % 4) * 32) << 16;
+    const uint32_t dq_addr = tmem + lane_off + L::kColDP;
+    uint8_t* stage_base = smem + L::kDQ;
+    uint32_t tile_cnt = 0, it_cnt = 0, stage_uses = 0;
+    if (issuer) prefetch_tensormap(map_dq);
+    for (int idx = ib; idx < ie; ++idx) {
+        const BwdItem it = decode_bwd(p.items[idx], p);
+        for (int i = it.i0; i < it.i1; ++i) {
+            bool ok = mbar_wait_warp(&bars.dq_full, tile_cnt & 1, ab);
+            if (!group_all(1, ok)) goto done;
+            tc_fence_after();
+            uint32_t v[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(dq_addr + c * 32, v[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
+#pragma unroll
+            for (int sl = 0; sl < D / 16; ++sl) {
+                const int st = stage_uses % 2;
+                uint8_t* stage = stage_base + st * L::kDQStage;
+                if (issuer) bulk_wait_group_read<1>();  // the reduce that last used this stage has read it
+                group_sync(1);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    // 64-byte swizzle (what the tensor map declares): chunk k of row r
+                    // sits at chunk k ^ ((r >> 1) & 3), which also spreads the banks.
+                    const uint32_t* src = &v[sl / 2][(sl % 2) * 16 + k * 4];
+                    *reinterpret_cast<float4*>(stage + r * 64 + ((k ^ ((r >> 1) & 3)) * 16)) =
+                        make_float4(__uint_as_float(src[0]) * p.scale, __uint_as_float(src[1]) * p.scale,
+                                    __uint_as_float(src[2]) * p.scale, __uint_as_float(src[3]) * p.scale);
+                }
+                fence_proxy_async_smem();
+                group_sync(1);
+                if (issuer) {
+                    tma_reduce_add_2d(map_dq, stage, it.h * D + sl * 16, it.q_row0 + 128 * i);
+                    bulk_commit_group();
+                }
+                ++stage_uses;
+            }
+            ++tile_cnt;
+        }
+        // dK / dV epilogue for key rows of this tile.
+        {
+            bool ok = mbar_wait_warp(&bars.dkv_full, it_cnt & 1, ab);
+            if (!group_all(1, ok)) goto done;
+            tc_fence_after();
+            const int key = 128 * it.n + r;
+            const bool valid = key < it.Lk;
+            const int64_t grow = (static_cast<int64_t>(it.kv_start) + key) * p.H + it.h;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled)
+                uint32_t v[D / 32][32];
+                const uint32_t col = which ? L::kColDK : L::kColDV;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + col + c * 32, v[c]);
+                tmem_ld_wait();
+                if (which == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&bars.dkv_empty);
+                }
+                if (valid) {
+                    const float sc = which ? p.scale : 1.0f;
+                    uint16_t* dst = (which ? p.dk : p.dv) + grow * D;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 u;
+                            u.x = pack_bf16x2(__uint_as_float(v[c][8 * q + 0]) * sc, __uint_as_float(v[c][8 * q + 1]) * sc);
+                            u.y = pack_bf16x2(__uint_as_float(v[c][8 * q + 2]) * sc, __uint_as_float(v[c][8 * q + 3]) * sc);
+                            u.z = pack_bf16x2(__uint_as_float(v[c][8 * q + 4]) * sc, __uint_as_float(v[c][8 * q + 5]) * sc);
+                            u.w = pack_bf16x2(__uint_as_float(v[c][8 * q + 6]) * sc, __uint_as_float(v[c][8 * q + 7]) * sc);
+                            reinterpret_cast<uint4*>(dst + c * 32)[q] = u;
+                        }
+                }
+            }
+            ++it_cnt;
+        }
+    }
+done:
+    if (issuer) bulk_wait_group<0>();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    jfa_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
+    using L = BwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ BwdBars bars;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
+    const AbortState ab{&bars.abort_flag, p.status};
+
+    if (threadIdx.x == 0) {
+        bars.abort_flag = 0;
+        mbar_init(&bars.k_full, 1);
+        mbar_init(&bars.k_empty, 1);
+        mbar_init(&bars.v_full, 1);
+        mbar_init(&bars.v_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.q_full[s], 1);
+            mbar_init(&bars.q_empty[s], 1);
+        }
+        mbar_init(&bars.do_full, 1);
+        mbar_init(&bars.do_empty, 1);
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.dp_full, 1);
+        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.ds_full, 128);
+        mbar_init(&bars.ds_empty, 1);
+        mbar_init(&bars.dq_full, 1);
+        mbar_init(&bars.dq_empty, 128);
+        mbar_init(&bars.dkv_full, 1);
+        mbar_init(&bars.dkv_empty, 128);
+        mbar_init(&bars.mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars.tmem_base, L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp < 4) {
+        bwd_compute_role<D>(p, smem, bars, tmem, ib, ie, ab);
+    } else if (warp < 8) {
+        bwd_dq_role<D>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);
+    } else if (warp == kWarpLoad) {
+        bwd_load_role<D>(p, &maps, smem, bars, ib, ie, ab);
+    } else {
+        if (lane == 0) bwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
+}
+
+// Delta[row] = sum_d dO[row, d] * O[row, d] (fp32), one 16-byte chunk per
+// lane; D/8 consecutive lanes own one (row, head) pair.
+template <int D>
+__global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
+    constexpr int kLanes = D / 8;
+    const int64_t total = p.rows;
+    const int sub = threadIdx.x % kLanes;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x / kLanes);
+    int64_t pair = static_cast<int64_t>(blockIdx.x) * (blockDim.x / kLanes) + threadIdx.x / kLanes;
+    // All lanes of a group iterate together so the shuffles below stay converged.
+    const int64_t iters = (total + stride - 1) / stride;
+    for (int64_t k = 0; k < iters; ++k, pair += stride) {
+        float acc = 0.0f;
+        const bool in = pair < total;
+        if (in) {
+            const uint4 a = reinterpret_cast<const uint4*>(p.o + pair * D)[sub];
+            const uint4 b = reinterpret_cast<const uint4*>(p.dout + pair * D)[sub];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                acc = fmaf(bf16lo_to_f32(aw[w]), bf16lo_to_f32(bw[w]), acc);
+                acc = fmaf(bf16hi_to_f32(aw[w]), bf16hi_to_f32(bw[w]), acc);
+            }
+        }
+#pragma unroll
+        for (int off = kLanes / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (in && sub == 0) {
+            const int64_t orow = pair / p.H;
+            const int h = static_cast<int>(pair % p.H);
+            int64_t di;
+            if (p.broadcast_q) {
+                const int64_t b = orow / p.Lq, i = orow % p.Lq;
+                di = (b * p.H + h) * p.Lq + i;
+            } else {
+                di = static_cast<int64_t>(h) * p.N + orow;
+            }
+            p.delta[di] = acc;
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
+    using L = BwdLayout<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    jfa_bwd_kernel<D><<<grid, kBwdThreads, L::kDynSmem, s>>>(p, m);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s) {
+    if (p.rows <= 0) return cudaSuccess;
+    const int lanes = p.D / 8;
+    const int pairs_per_block = 256 / lanes;
+    int64_t blocks = (p.rows + pairs_per_block - 1) / pairs_per_block;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (p.D == 128)
+        jfa_bwd_pre_kernel<128><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+    else
+        jfa_bwd_pre_kernel<64><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
+    if (grid <= 0) return cudaSuccess;
+    return D == 128 ? launch_bwd_d<128>(p, m, grid, s) : launch_bwd_d<64>(p, m, grid, s);
+}
+
+}  // namespace jfa

@@ -1,0 +1,362 @@
+// jfa_api.cu -- the C ABI declared in include/jfa.h: argument checks, the
+// host schedule (staged through a small pinned ring), TMA tensor maps and
+// the kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/jfa.h"
+#include "host_util.h"
+#include "kernels.h"
+#include "sched.h"
+
+namespace jfa {
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t fwd_off, bwd_off, region_bytes, delta_off, delta_bytes, total;
+    int64_t max_items;
+};
+
+bool ws_layout(int B, int64_t N, int Lq, int H, int broadcast_q, WsLayout* w) {
+    if (B < 0 || N < 0 || H <= 0) return false;
+    w->max_items = max_work_items(B, N, Lq, H, broadcast_q);
+    w->region_bytes = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
+    w->fwd_off = kStatusBytes;
+    w->bwd_off = w->fwd_off + w->region_bytes;
+    w->delta_off = w->bwd_off + w->region_bytes;
+    const int64_t stat_elems = broadcast_q ? static_cast<int64_t>(B) * H * Lq : static_cast<int64_t>(H) * N;
+    w->delta_bytes = align_up(static_cast<size_t>(stat_elems) * sizeof(float), 256);
+    w->total = w->delta_off + w->delta_bytes;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Pinned staging ring for schedules: a slot is reused only after the copy
+// that last read it has executed (its event has completed).
+// ---------------------------------------------------------------------------
+struct StageSlot {
+    void* buf = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool used = false;
+};
+
+struct DeviceStage {
+    std::mutex mu;
+    StageSlot slots[4];
+    unsigned next = 0;
+};
+
+DeviceStage& device_stage(int dev) {
+    static DeviceStage stages[64];
+    return stages[dev & 63];
+}
+
+// Builds the schedule into a pinned slot and enqueues its copy into
+// workspace + off.  Returns the item count (>= 0) or -1 on error.
+int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
+                       int64_t max_items, void* ws_region, cudaStream_t stream, jfa_status* st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        *st = JFA_ERR_CUDA;
+        return -1;
+    }
+    DeviceStage& ds = device_stage(dev);
+    std::lock_guard<std::mutex> lock(ds.mu);
+    StageSlot& slot = ds.slots[ds.next++ % 4];
+    if (slot.used && cudaEventSynchronize(slot.ev) != cudaSuccess) {
+        *st = JFA_ERR_CUDA;
+        return -1;
+    }
+    const size_t need = kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
+    if (slot.cap < need) {
+        if (slot.buf) cudaFreeHost(slot.buf);
+        slot.buf = nullptr;
+        slot.cap = 0;
+        if (cudaHostAlloc(&slot.buf, need, cudaHostAllocDefault) != cudaSuccess) {
+            *st = JFA_ERR_CUDA;
+            return -1;
+        }
+        slot.cap = need;
+    }
+    if (!slot.ev && cudaEventCreateWithFlags(&slot.ev, cudaEventDisableTiming) != cudaSuccess) {
+        *st = JFA_ERR_CUDA;
+        return -1;
+    }
+    int32_t* cta_start = static_cast<int32_t*>(slot.buf);
+    WorkItem* items = reinterpret_cast<WorkItem*>(static_cast<char*>(slot.buf) + kCtaStartBytes);
+    const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, kSchedLptZigzag, items,
+                                     cta_start, max_items);
+    if (n < 0) {
+        *st = JFA_ERR_WORKSPACE;
+        return -1;
+    }
+    const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
+    if (cudaMemcpyAsync(ws_region, slot.buf, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaEventRecord(slot.ev, stream) != cudaSuccess) {
+        *st = JFA_ERR_CUDA;
+        return -1;
+    }
+    slot.used = true;
+    return n;
+}
+
+// ---------------------------------------------------------------------------
+// Argument checks shared by both passes.
+// ---------------------------------------------------------------------------
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Problem {
+    int B, Lq, H, D, broadcast_q, causal;
+    int64_t N;
+    float scale;
+    std::vector<int32_t> off_copy;
+    const int32_t* off;
+};
+
+jfa_status check_common(int B, int Lq, int H, int D, int broadcast_q, int causal, float scale,
+                        const int32_t* offsets_dev, const int32_t* offsets_host, cudaStream_t stream, Problem* pr) {
+    if (B < 0 || H <= 0 || Lq < 0) return JFA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return JFA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return JFA_ERR_UNSUPPORTED;
+    if (H > 255) return JFA_ERR_UNSUPPORTED;
+    if (broadcast_q && causal) return JFA_ERR_UNSUPPORTED;
+    if (broadcast_q && Lq > kMaxSeqLen) return JFA_ERR_UNSUPPORTED;
+    if (!offsets_host && !offsets_dev) return JFA_ERR_INVALID_ARG;
+    pr->B = B;
+    pr->Lq = broadcast_q ? Lq : 0;
+    pr->H = H;
+    pr->D = D;
+    pr->broadcast_q = broadcast_q ? 1 : 0;
+    pr->causal = causal ? 1 : 0;
+    pr->scale = scale > 0.0f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+    if (offsets_host) {
+        pr->off = offsets_host;
+    } else {
+        pr->off_copy.resize(static_cast<size_t>(B) + 1);
+        if (cudaMemcpyAsync(pr->off_copy.data(), offsets_dev, sizeof(int32_t) * (static_cast<size_t>(B) + 1),
+                            cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return JFA_ERR_CUDA;
+        pr->off = pr->off_copy.data();
+    }
+    if (pr->off[0] != 0) return JFA_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b) {
+        const int64_t len = static_cast<int64_t>(pr->off[b + 1]) - pr->off[b];
+        if (len < 0) return JFA_ERR_INVALID_ARG;
+        if (len > kMaxSeqLen) return JFA_ERR_UNSUPPORTED;
+    }
+    pr->N = pr->off[B];
+    return JFA_OK;
+}
+
+jfa_status check_workspace(const Problem& pr, void* workspace, size_t ws_bytes, WsLayout* w) {
+    if (!ws_layout(pr.B, pr.N, pr.Lq, pr.H, pr.broadcast_q, w)) return JFA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < w->total) return JFA_ERR_WORKSPACE;
+    return JFA_OK;
+}
+
+// A 2D [rows, H*D] view with 64x128 bf16 boxes and 128-byte swizzle.
+bool map_rows_bf16(CUtensorMap* m, const void* base, int64_t rows, int H, int D, const void* fallback) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(H) * D, static_cast<uint64_t>(rows > 0 ? rows : 1)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(H) * D * 2};
+    const uint32_t box[2] = {64, 128};
+    return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows > 0 ? base : fallback, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// A 2D [rows, H*D] fp32 view with 16x128 boxes and 64-byte swizzle (dQ reduce-add).
+bool map_rows_f32(CUtensorMap* m, const void* base, int64_t rows, int H, int D, const void* fallback) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(H) * D, static_cast<uint64_t>(rows > 0 ? rows : 1)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(H) * D * 4};
+    const uint32_t box[2] = {16, 128};
+    return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, rows > 0 ? base : fallback, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+int ctas_for(int64_t items) {
+    const int sms = device_sm_count();
+    int p = sms > 0 ? sms : 1;
+    if (p > kMaxCtas) p = kMaxCtas;
+    if (items < p) p = static_cast<int>(items > 0 ? items : 1);
+    return p;
+}
+
+int64_t count_items(const Problem& pr, int is_bwd) {
+    int64_t n = 0;
+    for (int b = 0; b < pr.B; ++b) {
+        const int64_t Lk = static_cast<int64_t>(pr.off[b + 1]) - pr.off[b];
+        const int64_t nkv = (Lk + 127) / 128;
+        if (is_bwd)
+            n += nkv;
+        else
+            n += ((pr.broadcast_q ? (pr.Lq + 127) / 128 : nkv) + 1) / 2;
+    }
+    return n * pr.H;
+}
+
+}  // namespace
+}  // namespace jfa
+
+using namespace jfa;
+
+extern "C" size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D, int broadcast_q, int causal) {
+    (void)causal;
+    if (D != 64 && D != 128) return 0;
+    WsLayout w;
+    if (!ws_layout(B, total_len, broadcast_q ? Lq : 0, H, broadcast_q, &w)) return 0;
+    return w.total;
+}
+
+extern "C" int jfa_num_ctas(void) { return ctas_for(1 << 30); }
+
+extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
+                              const int32_t* offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
+                              float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem pr;
+    jfa_status st = check_common(B, Lq, H, D, broadcast_q, causal, scale, offsets_dev, offsets_host, s, &pr);
+    if (st != JFA_OK) return st;
+    WsLayout w;
+    if ((st = check_workspace(pr, workspace, workspace_bytes, &w)) != JFA_OK) return st;
+    const int64_t q_rows = pr.broadcast_q ? pr.Lq : pr.N;
+    const int64_t o_rows = pr.broadcast_q ? static_cast<int64_t>(pr.B) * pr.Lq : pr.N;
+    if ((q_rows > 0 && !q) || (pr.N > 0 && (!k || !v)) || (o_rows > 0 && (!o || !lse))) return JFA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return JFA_ERR_UNSUPPORTED;
+    if (o_rows == 0) return JFA_OK;  // nothing to compute
+
+    char* ws = static_cast<char*>(workspace);
+    const int64_t n_items = count_items(pr, 0);
+    const int P = ctas_for(n_items);
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w.max_items,
+                                     ws + w.fwd_off, s, &st);
+    if (n < 0) return st;
+    if (n == 0) return JFA_OK;
+
+    FwdMaps maps;
+    if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
+        !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace))
+        return JFA_ERR_CUDA;
+    FwdParams p;
+    p.cta_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off);
+    p.items = reinterpret_cast<const WorkItem*>(ws + w.fwd_off + kCtaStartBytes);
+    p.o = static_cast<uint16_t*>(o);
+    p.lse = lse;
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.Lq = pr.Lq;
+    p.H = H;
+    p.N = static_cast<int>(pr.N);
+    p.broadcast_q = pr.broadcast_q;
+    p.causal = pr.causal;
+    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    return launch_fwd(D, p, maps, P, s) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, const int32_t* offsets_dev, const int32_t* offsets_host, int B,
+                              int Lq, int H, int D, int broadcast_q, int causal, float scale, float* dq, void* dk,
+                              void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem pr;
+    jfa_status st = check_common(B, Lq, H, D, broadcast_q, causal, scale, offsets_dev, offsets_host, s, &pr);
+    if (st != JFA_OK) return st;
+    WsLayout w;
+    if ((st = check_workspace(pr, workspace, workspace_bytes, &w)) != JFA_OK) return st;
+    const int64_t q_rows = pr.broadcast_q ? pr.Lq : pr.N;
+    const int64_t o_rows = pr.broadcast_q ? static_cast<int64_t>(pr.B) * pr.Lq : pr.N;
+    if ((q_rows > 0 && (!q || !dq)) || (pr.N > 0 && (!k || !v || !dk || !dv)) ||
+        (o_rows > 0 && (!o || !lse || !dout)))
+        return JFA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dout, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+        return JFA_ERR_UNSUPPORTED;
+
+    const size_t elems_kv = static_cast<size_t>(pr.N) * H * D;
+    if (q_rows > 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(q_rows) * H * D * sizeof(float), s) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    if (o_rows == 0) {  // no query rows: every key gets a zero gradient
+        if (elems_kv && (cudaMemsetAsync(dk, 0, elems_kv * 2, s) != cudaSuccess ||
+                         cudaMemsetAsync(dv, 0, elems_kv * 2, s) != cudaSuccess))
+            return JFA_ERR_CUDA;
+        return JFA_OK;
+    }
+    if (pr.N == 0) return JFA_OK;
+
+    char* ws = static_cast<char*>(workspace);
+    float* delta = reinterpret_cast<float*>(ws + w.delta_off);
+    PreParams pp;
+    pp.o = static_cast<const uint16_t*>(o);
+    pp.dout = static_cast<const uint16_t*>(dout);
+    pp.delta = delta;
+    pp.rows = o_rows * H;
+    pp.B = pr.B;
+    pp.Lq = pr.Lq;
+    pp.H = H;
+    pp.N = static_cast<int>(pr.N);
+    pp.D = D;
+    pp.broadcast_q = pr.broadcast_q;
+    if (launch_bwd_pre(pp, s) != cudaSuccess) return JFA_ERR_CUDA;
+
+    const int64_t n_items = count_items(pr, 1);
+    const int P = ctas_for(n_items);
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w.max_items,
+                                     ws + w.bwd_off, s, &st);
+    if (n < 0) return st;
+    if (n == 0) return JFA_OK;
+
+    BwdMaps maps;
+    if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
+        !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dout, dout, o_rows, H, D, workspace) ||
+        !map_rows_f32(&maps.dq, dq, q_rows, H, D, workspace))
+        return JFA_ERR_CUDA;
+    BwdParams p;
+    p.cta_start = reinterpret_cast<const int32_t*>(ws + w.bwd_off);
+    p.items = reinterpret_cast<const WorkItem*>(ws + w.bwd_off + kCtaStartBytes);
+    p.lse = lse;
+    p.delta = delta;
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.Lq = pr.Lq;
+    p.H = H;
+    p.N = static_cast<int>(pr.N);
+    p.broadcast_q = pr.broadcast_q;
+    p.causal = pr.causal;
+    p.scale = pr.scale;
+    p.scale_log2 = pr.scale * 1.4426950408889634f;
+    return launch_bwd(D, p, maps, P, s) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+extern "C" jfa_status jfa_device_status(void* workspace, void* stream) {
+    if (!workspace) return JFA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return JFA_ERR_CUDA;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+    if (word != 0 && cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return JFA_ERR_CUDA;
+    return word ? JFA_ERR_DEVICE_TIMEOUT : JFA_OK;
+}
+
+extern "C" const char* jfa_status_string(jfa_status s) {
+    switch (s) {
+        case JFA_OK: return "JFA_OK";
+        case JFA_ERR_INVALID_ARG: return "JFA_ERR_INVALID_ARG";
+        case JFA_ERR_UNSUPPORTED: return "JFA_ERR_UNSUPPORTED";
+        case JFA_ERR_WORKSPACE: return "JFA_ERR_WORKSPACE";
+        case JFA_ERR_CUDA: return "JFA_ERR_CUDA";
+        case JFA_ERR_DEVICE_TIMEOUT: return "JFA_ERR_DEVICE_TIMEOUT";
+    }
+    return "JFA_ERR_UNKNOWN";
+}

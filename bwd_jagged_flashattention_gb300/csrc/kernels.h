@@ -1,0 +1,59 @@
+// kernels.h -- launch parameters of the attention kernels and the host-side
+// launch functions (implemented in fwd.cu / bwd.cu, called by jfa_api.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "sched.h"
+
+namespace jfa {
+
+struct FwdParams {
+    const WorkItem* items;     // device, CSR-ordered by CTA
+    const int32_t* cta_start;  // device, [grid + 1]
+    uint16_t* o;               // bf16 output
+    float* lse;                // fp32 output
+    uint32_t* status;          // device status word
+    int Lq, H, N;
+    int broadcast_q, causal;
+    float scale_log2;          // softmax scale * log2(e)
+};
+
+struct BwdParams {
+    const WorkItem* items;
+    const int32_t* cta_start;
+    const float* lse;          // [B,H,Lq] or [H,N]
+    const float* delta;        // same layout as lse
+    uint16_t* dk;              // bf16 [N,H,D]
+    uint16_t* dv;              // bf16 [N,H,D]
+    uint32_t* status;
+    int Lq, H, N;
+    int broadcast_q, causal;
+    float scale, scale_log2;
+};
+
+struct PreParams {
+    const uint16_t* o;         // bf16, O layout
+    const uint16_t* dout;      // bf16, O layout
+    float* delta;              // fp32, LSE layout
+    int64_t rows;              // number of (row, head) pairs = O rows * H
+    int B, Lq, H, N, D;
+    int broadcast_q;
+};
+
+// Tensor maps for one call.  Q/K/V/dO are viewed as 2D [rows, H*D] bf16
+// with 64x128 boxes (128-byte swizzle); dQ as 2D [rows, H*D] fp32.
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
+struct BwdMaps {
+    CUtensorMap q, k, v, dout, dq;
+};
+
+cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s);
+cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
+cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
+
+}  // namespace jfa

@@ -1,0 +1,105 @@
+// sched.cpp -- see sched.h.
+#include "sched.h"
+
+#include <algorithm>
+#include <vector>
+
+namespace jfa {
+
+namespace {
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+}  // namespace
+
+int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q) {
+    if (B <= 0 || H <= 0) return 0;
+    // backward: sum_b ceil(L_b/128) <= N/128 + B; forward pairs of q tiles
+    // are never more.  Broadcast forward: B * ceil(ceil(Lq/128)/2).
+    int64_t bwd = static_cast<int64_t>(H) * (total_len / kTileRows + B);
+    int64_t fwd = broadcast_q ? static_cast<int64_t>(B) * H * ceil_div(ceil_div(std::max(Lq, 0), kTileRows), 2)
+                              : static_cast<int64_t>(H) * (total_len / (2 * kTileRows) + B);
+    return std::max<int64_t>(std::max(bwd, fwd), 1);
+}
+
+int64_t item_cost(const WorkItem& w, int Lq, int broadcast_q, int causal, int is_bwd) {
+    const int64_t Lk = w.kv_len;
+    const int tile = static_cast<int>((w.packed >> 8) & 0x7FFFFFu);
+    const int two = static_cast<int>(w.packed >> 31);
+    const int64_t nkv = ceil_div(Lk, kTileRows);
+    if (!is_bwd) {
+        int64_t blocks = 0;
+        for (int t = 0; t <= two; ++t) {
+            const int64_t m = tile + t;
+            blocks += causal ? std::min<int64_t>(m + 1, nkv) : nkv;
+        }
+        return blocks + 1;
+    }
+    const int64_t nq = broadcast_q ? ceil_div(Lq, kTileRows) : nkv;
+    const int64_t visited = causal ? (nq - tile) : nq;
+    return visited + 1;
+}
+
+int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
+                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items) {
+    if (P <= 0 || P > kMaxCtas) return -1;
+    // 1. Generate items in (b, h, tile) order.
+    std::vector<WorkItem> gen;
+    gen.reserve(static_cast<size_t>(std::min<int64_t>(max_items, 1 << 22)));
+    for (int b = 0; b < B; ++b) {
+        const int32_t Lk = offsets[b + 1] - offsets[b];
+        const int64_t nkv = ceil_div(Lk, kTileRows);
+        if (!is_bwd) {
+            const int64_t nq = broadcast_q ? ceil_div(Lq, kTileRows) : nkv;
+            // broadcast rows exist even for an empty sequence (their O is 0, LSE -inf)
+            for (int h = 0; h < H; ++h)
+                for (int64_t m = 0; m < nq; m += 2)
+                    gen.push_back({b, offsets[b], Lk, pack_item(h, static_cast<int>(m), m + 1 < nq ? 1 : 0)});
+        } else {
+            for (int h = 0; h < H; ++h)
+                for (int64_t n = 0; n < nkv; ++n) gen.push_back({b, offsets[b], Lk, pack_item(h, static_cast<int>(n), 0)});
+        }
+        if (static_cast<int64_t>(gen.size()) > max_items) return -1;
+    }
+    const int64_t n = static_cast<int64_t>(gen.size());
+
+    // 2. Order: cost-descending, stable (counting sort on the integer cost).
+    std::vector<int64_t> order(static_cast<size_t>(n));
+    if (policy == kSchedLptZigzag && n > 0) {
+        std::vector<int64_t> cost(static_cast<size_t>(n));
+        int64_t cmax = 0;
+        for (int64_t i = 0; i < n; ++i) {
+            cost[i] = item_cost(gen[i], Lq, broadcast_q, causal, is_bwd);
+            cmax = std::max(cmax, cost[i]);
+        }
+        std::vector<int64_t> start(static_cast<size_t>(cmax + 2), 0);
+        for (int64_t i = 0; i < n; ++i) ++start[cmax - cost[i] + 1];  // bucket 0 = largest cost
+        for (int64_t c = 1; c <= cmax + 1; ++c) start[c] += start[c - 1];
+        for (int64_t i = 0; i < n; ++i) order[start[cmax - cost[i]]++] = i;
+    } else {
+        for (int64_t i = 0; i < n; ++i) order[i] = i;
+    }
+
+    // 3. Deal.  Zigzag: sorted position i, round r = i / P, lane p = i % P;
+    //    CTA p on even rounds, CTA P-1-p on odd rounds.  Naive: round-robin.
+    std::vector<int32_t> owner(static_cast<size_t>(n));
+    std::fill(cta_start, cta_start + P + 1, 0);
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = i / P, p = i % P;
+        const int32_t cta = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
+        owner[i] = cta;
+        ++cta_start[cta + 1];
+    }
+    for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
+    std::vector<int32_t> fill(cta_start, cta_start + P);
+    for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
+    return n;
+}
+
+}  // namespace jfa
+
+// Host-only C entry used by the scheduler's unit tests (no GPU needed).
+extern "C" long long jfa_host_build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q,
+                                             int causal, int is_bwd, int P, int policy, void* items,
+                                             int32_t* cta_start, long long max_items) {
+    return jfa::build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, policy,
+                               static_cast<jfa::WorkItem*>(items), cta_start, max_items);
+}

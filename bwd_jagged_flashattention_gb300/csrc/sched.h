@@ -1,0 +1,53 @@
+// sched.h -- host tile scheduler: work items, cost model, LPT sort and
+// zigzag deal to persistent CTAs.
+//
+// The pages describe this step for the forward pass: tiles are sorted on the
+// host by their KV workload in descending order and handed to the SMs in a
+// zigzag pattern, which recovered about 20% of forward time at negligible CPU
+// cost (Meta's TLX Jagged Flash Attention Beats FA4 on Blackwell With 3x Less
+// Code, section "Optimizations layered on top", the paragraph after the
+// list; "Scheduling jagged tiles across SMs" in the same list).  The backward
+// uses the same sort and deal over its own items.
+#pragma once
+#include <cstdint>
+
+namespace jfa {
+
+// One unit of persistent-kernel work (16 bytes, read once per item).
+//   forward : query tiles [tile, tile + 1 + two) of sequence b, head h
+//   backward: key/value tile `tile` of sequence b, head h
+struct WorkItem {
+    int32_t b;         // sequence index
+    int32_t kv_start;  // first packed row of the sequence (offsets[b])
+    int32_t kv_len;    // sequence length (offsets[b+1] - offsets[b])
+    uint32_t packed;   // h | tile << 8 | two << 31
+};
+static_assert(sizeof(WorkItem) == 16, "WorkItem must stay 16 bytes");
+
+constexpr int kTileRows = 128;          // rows per Q or K/V tile
+constexpr int kMaxCtas = 1023;          // schedule bound on persistent CTAs
+constexpr int kMaxSeqLen = 1 << 23;     // tile index must fit 23 bits
+
+inline uint32_t pack_item(int h, int tile, int two) {
+    return static_cast<uint32_t>(h) | (static_cast<uint32_t>(tile) << 8) | (static_cast<uint32_t>(two) << 31);
+}
+
+enum SchedPolicy {
+    kSchedLptZigzag = 0,  // cost-descending stable sort, then zigzag deal
+    kSchedNaive = 1,      // generation order, round-robin deal (ablation)
+};
+
+// Upper bound on the number of items either pass produces.
+int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q);
+
+// Build a schedule.  Writes `n` items into `items` (capacity max_items) and
+// the CSR bounds cta_start[0..P] (CTA p owns items [cta_start[p],
+// cta_start[p+1])).  Returns n, or -1 if the capacity is too small.
+// is_bwd selects the backward item decomposition and cost.
+int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
+                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items);
+
+// Cost of one item in 128x128 block-products (+1 fixed per-item overhead).
+int64_t item_cost(const WorkItem& w, int Lq, int broadcast_q, int causal, int is_bwd);
+
+}  // namespace jfa

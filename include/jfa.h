@@ -1,0 +1,131 @@
+/*
+ * jfa.h -- C ABI of libjfa.so: Jagged Flash Attention forward and backward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  Sequences of different lengths are packed back to back
+ * with no padding, and an int32 offsets tensor records where each one
+ * starts; FlashAttention runs directly on the packed Q/K/V ("Why attention
+ * in GEM needed a rewrite", Meta's TLX Jagged Flash Attention Beats FA4 on
+ * Blackwell With 3x Less Code; Meta's 3.2K-line Triton kernel outruns
+ * FlashAttention-4 on jagged Blackwell attention, third paragraph).  For
+ * sequence b (keys offsets[b] .. offsets[b+1]-1) and head h:
+ *
+ *     S = scale * Q K^T,  P = softmax(S) row-wise,  O = P V,
+ *     LSE = natural log of the row sums of exp(S).
+ *
+ * Two query modes:
+ *   broadcast_q = 1: one dense Q [Lq,H,D] is shared by every sequence, and
+ *     dQ is the sum over the whole batch of each sequence's gradient (Meta's
+ *     3.2K-line Triton kernel ..., second paragraph; Meta's TLX Jagged Flash
+ *     Attention ..., section "Optimizations layered on top").
+ *   broadcast_q = 0: jagged self-attention; Q is packed like K/V and
+ *     sequence b's queries are rows offsets[b] .. offsets[b+1]-1.  `causal`
+ *     (query i sees keys j <= i, counted from the sequence start) is only
+ *     defined in this mode.
+ *
+ * Layouts (all row-major, contiguous, device memory):
+ *   q    bf16  [Lq, H, D] (broadcast) or [N, H, D] (jagged), N = offsets[B]
+ *   k, v bf16  [N, H, D]
+ *   o    bf16  [B, Lq, H, D] (broadcast) or [N, H, D]
+ *   lse  fp32  [B, H, Lq]    (broadcast) or [H, N]
+ *   dout bf16  shaped like o
+ *   dq   fp32  shaped like q (the library zeroes it before accumulating)
+ *   dk, dv bf16 [N, H, D]
+ * Empty sequences are allowed: their O rows are 0, their LSE is -inf and
+ * they add nothing to dQ.
+ *
+ * Supported: D in {64, 128}; 1 <= H <= 255; every sequence no longer than
+ * 2^23 rows; N < 2^31; broadcast Lq <= 2^23.  Arithmetic: bf16 operands on
+ * the tensor cores with fp32 accumulation; softmax statistics in fp32.
+ *
+ * Ownership and concurrency.  The caller owns every device buffer and the
+ * stream.  The library allocates no device memory; it keeps a small pinned
+ * host staging ring per device for the tile schedule.  Scratch memory (the
+ * tile schedule, the backward row statistics and a status word) lives in the
+ * caller's `workspace`, which must hold jfa_workspace_bytes(...) bytes and
+ * must not be shared by calls that may run concurrently.  Calls are
+ * asynchronous on `stream`; the one exception is that, when offsets_host is
+ * NULL, the library first copies the offsets from the device synchronously.
+ *
+ * Errors are returned, never thrown.  A call that returns anything but
+ * JFA_OK has enqueued no work, except JFA_ERR_CUDA, which reports a failed
+ * launch.  Kernels never trap: a bounded wait that times out records
+ * JFA_ERR_DEVICE_TIMEOUT in the workspace, which jfa_device_status() reads.
+ */
+#ifndef JFA_H
+#define JFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    JFA_OK = 0,
+    JFA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad offsets, non-finite scale */
+    JFA_ERR_UNSUPPORTED = 2,   /* D not in {64,128}, causal with broadcast_q, misaligned pointer, size limits */
+    JFA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or smaller than jfa_workspace_bytes() */
+    JFA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    JFA_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait expired (reported by jfa_device_status) */
+} jfa_status;
+
+/*
+ * Bytes of workspace one call needs (forward or backward) for a batch of B
+ * sequences holding total_len = offsets[B] rows in all, Lq broadcast query
+ * rows (ignored when broadcast_q == 0), H heads and head dimension D.  The
+ * same workspace serves jfa_fwd and jfa_bwd.  Returns 0 for unsupported or
+ * invalid sizes.  The workspace must be 256-byte aligned.
+ */
+size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D, int broadcast_q, int causal);
+
+/*
+ * jfa_fwd -- O and LSE (the forward pass).
+ *   q, k, v      device bf16 inputs (layouts above), 16-byte aligned.
+ *   offsets_dev  device int32 [B+1]; may be NULL when offsets_host is given.
+ *   offsets_host host int32 [B+1]; may be NULL (then copied from offsets_dev,
+ *                synchronously).  offsets[0] must be 0 and offsets must not
+ *                decrease.
+ *   scale        softmax scale; <= 0 selects 1/sqrt(D).
+ *   o, lse       device outputs (layouts above).
+ *   workspace    device scratch of at least jfa_workspace_bytes() bytes.
+ *   stream       cudaStream_t (NULL = legacy default stream).
+ */
+jfa_status jfa_fwd(const void *q, const void *k, const void *v, const int32_t *offsets_dev,
+                   const int32_t *offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
+                   float scale, void *o, float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * jfa_bwd -- dQ, dK, dV (the backward pass) given the forward's O and LSE
+ * and the upstream gradient dout.  Computes Delta = rowsum(dout * o) in the
+ * workspace first.  dq is fp32 and is overwritten (zeroed, then summed over
+ * every sequence in broadcast mode); dk and dv are bf16.  Other arguments as
+ * for jfa_fwd.  dQ is accumulated with fp32 atomics, so its low-order bits
+ * may differ from run to run; dK and dV are deterministic.
+ */
+jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, const int32_t *offsets_dev, const int32_t *offsets_host, int B, int Lq, int H,
+                   int D, int broadcast_q, int causal, float scale, float *dq, void *dk, void *dv, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * jfa_device_status -- synchronises `stream`, then reads and clears the
+ * status word kernels write into `workspace`.  Returns JFA_OK,
+ * JFA_ERR_DEVICE_TIMEOUT, or JFA_ERR_CUDA if the synchronisation failed.
+ */
+jfa_status jfa_device_status(void *workspace, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *jfa_status_string(jfa_status s);
+
+/*
+ * jfa_num_ctas -- number of persistent CTAs the kernels launch on the current
+ * device (one per SM); the schedule deals work to exactly this many.
+ */
+int jfa_num_ctas(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JFA_H */

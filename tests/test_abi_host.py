@@ -1,0 +1,121 @@
+"""The C-ABI library builds, loads and exports every symbol include/*.h
+declares, and rejects invalid arguments on the host before any GPU work.
+No call here launches a kernel or needs a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def jfa():
+    import bwd_jagged_flashattention_gb300 as jfa
+    jfa.build()
+    return jfa
+
+
+def _declared_functions():
+    names = set()
+    for h in ("jfa.h", "jfa_selftest.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(jfa_[a-z_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(jfa):
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    lib = jfa.lib()
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert declared <= set(jfa.EXPORTED) | {"jfa_host_build_schedule"}
+
+
+def test_status_strings(jfa):
+    for code, name in enumerate(["JFA_OK", "JFA_ERR_INVALID_ARG", "JFA_ERR_UNSUPPORTED", "JFA_ERR_WORKSPACE",
+                                 "JFA_ERR_CUDA", "JFA_ERR_DEVICE_TIMEOUT"]):
+        assert jfa.status_string(code) == name
+
+
+def test_workspace_bytes(jfa):
+    lib = jfa.lib()
+    a = lib.jfa_workspace_bytes(512, 190000, 256, 4, 128, 1, 0)
+    assert a > 0 and a % 256 == 0
+    # Delta [B,H,Lq] fp32 is part of it
+    assert a >= 512 * 4 * 256 * 4
+    assert lib.jfa_workspace_bytes(4, 100, 32, 2, 96, 1, 0) == 0          # unsupported D
+    assert lib.jfa_workspace_bytes(-1, 100, 32, 2, 64, 1, 0) == 0
+    j = lib.jfa_workspace_bytes(32, 139000, 0, 16, 128, 0, 1)
+    assert j >= 16 * 139000 * 4
+
+
+# Fake, never-dereferenced device addresses: validation must reject these
+# calls before touching them.
+P16 = 1 << 20
+WS = 1 << 24
+
+
+def _fwd(lib, offsets, B=2, Lq=32, H=2, D=64, bq=1, causal=0, scale=0.125, q=P16, o=P16, lse=P16, ws=WS,
+         ws_bytes=1 << 30):
+    off = torch.tensor(offsets, dtype=torch.int32)
+    return lib.jfa_fwd(ctypes.c_void_p(q), ctypes.c_void_p(P16), ctypes.c_void_p(P16), None,
+                       ctypes.c_void_p(off.data_ptr()), B, Lq, H, D, bq, causal, scale, ctypes.c_void_p(o),
+                       ctypes.c_void_p(lse), ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_fwd_argument_errors(jfa):
+    lib = jfa.lib()
+    ok_off = [0, 3, 7]
+    assert _fwd(lib, ok_off, D=96) == jfa.JFA_ERR_UNSUPPORTED
+    assert _fwd(lib, ok_off, H=256) == jfa.JFA_ERR_UNSUPPORTED
+    assert _fwd(lib, ok_off, causal=1) == jfa.JFA_ERR_UNSUPPORTED      # causal with broadcast Q
+    assert _fwd(lib, [1, 3, 7]) == jfa.JFA_ERR_INVALID_ARG            # offsets[0] != 0
+    assert _fwd(lib, [0, 5, 4]) == jfa.JFA_ERR_INVALID_ARG            # decreasing offsets
+    assert _fwd(lib, ok_off, B=-1) == jfa.JFA_ERR_INVALID_ARG
+    assert _fwd(lib, ok_off, scale=float("nan")) == jfa.JFA_ERR_INVALID_ARG
+    assert _fwd(lib, ok_off, ws_bytes=16) == jfa.JFA_ERR_WORKSPACE
+    assert _fwd(lib, ok_off, ws=WS + 8) == jfa.JFA_ERR_WORKSPACE        # misaligned workspace
+    assert _fwd(lib, ok_off, q=P16 + 2) == jfa.JFA_ERR_UNSUPPORTED      # TMA needs 16-byte alignment
+    assert _fwd(lib, ok_off, q=0) == jfa.JFA_ERR_INVALID_ARG            # null input
+    assert _fwd(lib, [0, 1 << 24, 1 << 24]) == jfa.JFA_ERR_UNSUPPORTED  # sequence longer than 2^23
+    # neither offsets copy given
+    assert lib.jfa_fwd(None, None, None, None, None, 2, 32, 2, 64, 1, 0, 0.1, None, None, None, 0,
+                       None) == jfa.JFA_ERR_INVALID_ARG
+
+
+def test_bwd_argument_errors(jfa):
+    lib = jfa.lib()
+    off = torch.tensor([0, 3, 7], dtype=torch.int32)
+    p = ctypes.c_void_p(P16)
+
+    def call(D=64, bq=1, causal=0, dq=P16, ws_bytes=1 << 30):
+        return lib.jfa_bwd(p, p, p, p, p, p, None, ctypes.c_void_p(off.data_ptr()), 2, 32, 2, D, bq, causal, 0.1,
+                           ctypes.c_void_p(dq), p, p, ctypes.c_void_p(WS), ws_bytes, None)
+    assert call(D=32) == jfa.JFA_ERR_UNSUPPORTED
+    assert call(causal=1) == jfa.JFA_ERR_UNSUPPORTED
+    assert call(dq=P16 + 4) == jfa.JFA_ERR_UNSUPPORTED
+    assert call(ws_bytes=100) == jfa.JFA_ERR_WORKSPACE
+    assert call(dq=0) == jfa.JFA_ERR_INVALID_ARG
+
+
+def test_device_status_rejects_null(jfa):
+    assert jfa.lib().jfa_device_status(None, None) == jfa.JFA_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle and raises when its library is missing."""
+    pkg = os.path.join(ROOT, "bwd_jagged_flashattention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "jfa_oracle" not in text, f
+    src = open(os.path.join(pkg, "__init__.py")).read()
+    assert "raise ImportError" in src

@@ -1,0 +1,119 @@
+"""Host tile scheduler: cost-descending (LPT) order dealt zigzag to CTAs.
+
+The pages: tiles are sorted on the host by KV workload, descending, and
+handed to the SMs in a zigzag pattern (Meta's TLX Jagged Flash Attention
+Beats FA4 on Blackwell With 3x Less Code, section "Optimizations layered on
+top").  These tests need no GPU.
+"""
+import pytest
+import torch
+
+import jfa_inputs
+
+
+@pytest.fixture(scope="module")
+def jfa():
+    import bwd_jagged_flashattention_gb300 as jfa
+    jfa.build()
+    return jfa
+
+
+def _decode(items):
+    b, start, length, packed = items.unbind(1)
+    packed = packed.to(torch.int64) & 0xFFFFFFFF
+    h = packed & 0xFF
+    tile = (packed >> 8) & 0x7FFFFF
+    two = packed >> 31
+    return b, start, length, h, tile, two
+
+
+def _cost(length, tile, two, Lq, broadcast_q, causal, is_bwd):
+    """The documented cost model, restated: 128x128 block products + 1."""
+    nkv = (length + 127) // 128
+    if not is_bwd:
+        c = 0
+        for t in range(int(two) + 1):
+            m = int(tile) + t
+            c += min(m + 1, int(nkv)) if causal else int(nkv)
+        return c + 1
+    nq = (Lq + 127) // 128 if broadcast_q else int(nkv)
+    return (nq - int(tile) if causal else nq) + 1
+
+
+@pytest.mark.parametrize("name,is_bwd", [("tiny", 0), ("tiny", 1), ("ads_fwd", 0), ("ads_bwd", 1),
+                                         ("extreme", 0), ("extreme", 1)])
+def test_every_item_exactly_once(jfa, name, is_bwd):
+    w = jfa_inputs.WORKLOADS[name]
+    g = torch.Generator().manual_seed(5)
+    L = jfa_inputs.draw_lengths(w.lengths, w.B, g)
+    off = jfa_inputs.offsets_from_lengths(L)
+    P = 152
+    items, starts = jfa.host_schedule(off, w.Lq, w.H, w.broadcast_q, w.causal, bool(is_bwd), P)
+    b, start, length, h, tile, two = _decode(items)
+    seen = set()
+    for i in range(items.shape[0]):
+        key = (int(b[i]), int(h[i]), int(tile[i]))
+        assert key not in seen
+        seen.add(key)
+        assert int(start[i]) == int(off[b[i]]) and int(length[i]) == int(off[b[i] + 1] - off[b[i]])
+    expect = set()
+    for bb in range(w.B):
+        Lk = int(off[bb + 1] - off[bb])
+        nkv = (Lk + 127) // 128
+        for hh in range(w.H):
+            if is_bwd:
+                expect |= {(bb, hh, n) for n in range(nkv)}
+            else:
+                nq = (w.Lq + 127) // 128 if w.broadcast_q else nkv
+                expect |= {(bb, hh, m) for m in range(0, nq, 2)}
+    assert seen == expect
+    assert int(starts[0]) == 0 and int(starts[-1]) == items.shape[0]
+    assert torch.all(starts[1:] >= starts[:-1])
+
+
+def test_lpt_zigzag_bound(jfa):
+    """Sorted zigzag dealing stays within the LPT-style bound on the makespan."""
+    w = jfa_inputs.WORKLOADS["extreme"]
+    g = torch.Generator().manual_seed(6)
+    off = jfa_inputs.offsets_from_lengths(jfa_inputs.draw_lengths(w.lengths, w.B, g))
+    P = 152
+    items, starts = jfa.host_schedule(off, w.Lq, w.H, True, False, False, P)
+    b, start, length, h, tile, two = _decode(items)
+    cost = [_cost(int(length[i]), int(tile[i]), int(two[i]), w.Lq, True, False, False) for i in range(len(b))]
+    loads = [sum(cost[int(starts[p]):int(starts[p + 1])]) for p in range(P)]
+    total, biggest = sum(cost), max(cost)
+    lower = max(total / P, biggest)
+    assert max(loads) <= 4 / 3 * lower + biggest
+    # and it clearly beats the round-robin deal in generation order
+    items_n, starts_n = jfa.host_schedule(off, w.Lq, w.H, True, False, False, P, policy=1)
+    bn, sn, ln, hn, tn, twon = _decode(items_n)
+    cost_n = [_cost(int(ln[i]), int(tn[i]), int(twon[i]), w.Lq, True, False, False) for i in range(len(bn))]
+    loads_n = [sum(cost_n[int(starts_n[p]):int(starts_n[p + 1])]) for p in range(P)]
+    assert max(loads) <= max(loads_n)
+
+
+def test_zigzag_hand_example(jfa):
+    """Six sequences, one head, P = 3 CTAs, broadcast Lq = 128 (one q tile).
+
+    KV lengths 128*[1,5,3,6,2,4] give costs [2,6,4,7,3,5] (blocks + 1).
+    Sorted descending: b = 3(7), 1(6), 5(5), 2(4), 4(3), 0(2).
+    Zigzag: round 0 -> CTAs 0,1,2; round 1 -> CTAs 2,1,0.
+    CTA 0: b3, b0; CTA 1: b1, b4; CTA 2: b5, b2.
+    """
+    L = torch.tensor([1, 5, 3, 6, 2, 4]) * 128
+    off = jfa_inputs.offsets_from_lengths(L)
+    items, starts = jfa.host_schedule(off, 128, 1, True, False, False, 3)
+    b = items[:, 0].tolist()
+    assert starts.tolist() == [0, 2, 4, 6]
+    assert b == [3, 0, 1, 4, 5, 2]
+
+
+def test_causal_costs_and_pairs(jfa):
+    """Jagged causal forward pairs q tiles; the later tile of a pair sees one more KV block."""
+    off = torch.tensor([0, 1000], dtype=torch.int32)      # 8 q tiles -> 4 items per head
+    items, starts = jfa.host_schedule(off, 0, 2, False, True, False, 4)
+    b, start, length, h, tile, two = _decode(items)
+    assert sorted(int(t) for t in tile[h == 0]) == [0, 2, 4, 6]
+    assert torch.all(two == 1)
+    costs = [_cost(1000, int(tile[i]), 1, 0, False, True, False) for i in range(len(tile))]
+    assert costs == sorted(costs, reverse=True) or len(set(starts.tolist())) > 1
