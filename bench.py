@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark: Jagged Flash Attention forward + backward on one GB300.
+
+One step = one pass of the whole hot path over one batch: the host tile
+schedule, the forward kernel (O, LSE), the backward pre-pass (Delta) and the
+backward kernel (dQ summed over the batch, dK, dV), all through the C ABI.
+
+Workload (BASELINE metric's configuration): jagged broadcast-Q attention in
+the ads shape, B=512 sequences with lognormal KV lengths (median 256,
+sigma 1, clipped to [8, 4096]), one dense Q [256, 4, 128] shared by every
+sequence, bf16 N(0,1) inputs and upstream gradient, non-causal.  Inputs are
+synthetic and seeded (jfa_inputs).  K+V alone (~390 MB) exceed the 129 MB
+L2, so no explicit L2 flush is done between steps.
+
+Metric: useful TFLOPS of forward + backward (4*D*H*pairs for the forward,
+2.5x that for the backward; no padding is counted).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import jfa_inputs  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD = "ads_bwd"
+WORKLOAD_DESC = ("jagged broadcast-Q attention fwd+bwd, ads shape: B=512, KV lengths lognormal(median 256, "
+                 "sigma 1) clipped to [8,4096], Q [256,4,128] shared, packed K/V [N,4,128], bf16, non-causal")
+
+
+# ----------------------------------------------------------------------------
+# FLOP / byte accounting (useful work only)
+# ----------------------------------------------------------------------------
+def pair_count(offsets, Lq, broadcast_q, causal, first=None):
+    L = (offsets[1:] - offsets[:-1]).to(torch.int64)
+    if first is not None:
+        L = L[:first]
+    if broadcast_q:
+        return int(Lq * L.sum())
+    if causal:
+        return int((L * (L + 1) // 2).sum())
+    return int((L * L).sum())
+
+
+def accounting(x):
+    B, Lq, H, D, N = x["B"], x["Lq"], x["H"], x["D"], x["N"]
+    pairs = pair_count(x["offsets"], Lq, x["broadcast_q"], x["causal"])
+    f_fwd = 4.0 * D * H * pairs
+    f_bwd = 2.5 * f_fwd
+    q_rows = Lq if x["broadcast_q"] else N
+    o_rows = B * Lq if x["broadcast_q"] else N
+    e = H * D
+    q_b, kv_b, o_b = 2 * q_rows * e, 2 * N * e, 2 * o_rows * e
+    stat_b = 4 * o_rows * H
+    bytes_fwd = q_b + 2 * kv_b + o_b + stat_b                       # Q, K, V in; O, LSE out
+    bytes_pre = 2 * o_b + stat_b                                     # O, dO in; Delta out
+    bytes_bwd = q_b + 2 * kv_b + o_b + 2 * stat_b + 2 * kv_b + 2 * q_b  # Q,K,V,dO,LSE,Delta in; dK,dV,dQ(fp32) out
+    return dict(pairs=pairs, flops_fwd=f_fwd, flops_bwd=f_bwd, bytes_fwd=bytes_fwd, bytes_pre=bytes_pre,
+                bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("fwd.cu", "bwd.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "bwd_jagged_flashattention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_sha") != kernel_source_hash():
+        return {}
+    return d.get("kernels", {})
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.05 <= t <= (self.t1 or t) + 0.15]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[6:10]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_smi_id(dev) -> str:
+    """nvidia-smi's identifier for this CUDA device (its UUID when torch exposes it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    return str(dev.index or 0)
+
+
+# ----------------------------------------------------------------------------
+# Distributed plumbing (independent replicas; no data-path collective)
+# ----------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ----------------------------------------------------------------------------
+def oracle_sample(x, nseq):
+    import oracle
+    off = x["offsets"][: nseq + 1].clone()
+    N = int(off[-1])
+    sub = dict(x, B=nseq, offsets=off, N=N, k=x["k"][:N], v=x["v"][:N])
+    sub["do"] = x["do"][:nseq] if x["broadcast_q"] else x["do"][:N]
+    sub["q"] = x["q"] if x["broadcast_q"] else x["q"][:N]
+    flops = 3.5 * 4.0 * x["D"] * x["H"] * pair_count(off, x["Lq"], x["broadcast_q"], x["causal"])
+    t0 = time.perf_counter()
+    oracle.fwd(sub["q"], sub["k"], sub["v"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"])
+    oracle.bwd(sub["q"], sub["k"], sub["v"], sub["do"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"])
+    return flops, time.perf_counter() - t0
+
+
+def size_oracle_sample(x, budget_s):
+    """Number of leading sequences whose oracle fwd+bwd takes about budget_s."""
+    f1, t1 = oracle_sample(x, 2)
+    rate = f1 / max(t1, 1e-6)
+    per_seq = 3.5 * 4.0 * x["D"] * x["H"] * pair_count(x["offsets"], x["Lq"], x["broadcast_q"], x["causal"]) / x["B"]
+    return max(1, min(x["B"], int(budget_s * rate / per_seq)))
+
+
+def cpu_baseline(x, budget_s=12.0):
+    import oracle
+    n = size_oracle_sample(x, budget_s)
+    flops, secs = oracle_sample(x, n)
+    return {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on the first {n} of {x['B']} sequences of the same inputs "
+                      f"({flops / 1e9:.1f} GFLOP useful, {secs:.1f} s)"}
+
+
+def first_sequences(x, n):
+    """The same workload restricted to its first n sequences (for small profiling runs)."""
+    off = x["offsets"][: n + 1].clone()
+    N = int(off[-1])
+    y = dict(x, B=n, offsets=off, N=N, k=x["k"][:N].contiguous(), v=x["v"][:N].contiguous())
+    y["do"] = (x["do"][:n] if x["broadcast_q"] else x["do"][:N]).contiguous()
+    if not x["broadcast_q"]:
+        y["q"] = x["q"][:N].contiguous()
+    return y
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    x = jfa_inputs.make(WORKLOAD)
+    budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = size_oracle_sample(x, budget)
+    for _ in range(args.warmup):
+        oracle_sample(x, n)
+    tot_f, tot_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t = oracle_sample(x, n)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": "fwd+bwd TFLOPS (bf16, 1 GB300) on jagged broadcast-Q",
+            "value": value, "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "sample": f"first {n} of 512 sequences per step"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"fp64 oracle fwd+bwd on the first {n} of 512 sequences, per step"},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# The GPU arm
+# ----------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first BATCH sequences (small profiling case; not a bench line)")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import bwd_jagged_flashattention_gb300 as jfa
+    jfa.lib()  # raises if the CUDA library is missing: no fallback
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = jfa_inputs.make(WORKLOAD)
+    if args.batch:
+        x = first_sequences(x, args.batch)
+    acc = accounting(x)
+    B, Lq, H, D, N = x["B"], x["Lq"], x["H"], x["D"], x["N"]
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    off_h = x["offsets"]
+    off_d = off_h.to(dev)
+    o = torch.empty((B, Lq, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=dev)
+    dq = torch.empty((Lq, H, D), dtype=torch.float32, device=dev)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws = jfa.new_workspace(B, N, Lq, H, D, True, False, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        jfa.fwd(q, k, v, off_d, broadcast_q=True, causal=False, scale=x["scale"], offsets_host=off_h,
+                workspace=ws, out=o, lse=lse)
+        jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=True, causal=False, scale=x["scale"],
+                offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert jfa.device_status(ws) == 0, "kernel status word reports a timeout"
+
+    sampler = ClockSampler(gpu_smi_id(dev))
+    sampler.start()
+    for _ in range(3):
+        step()
+    jfa.profile_enable(True)
+    jfa.profile_read()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark(0)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(1)
+    barrier(world)
+    prof = jfa.profile_read()
+    jfa.profile_enable(False)
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(world, ev0.elapsed_time(ev1), dev)
+    ms_per_step = elapsed_ms / args.steps
+    step_flops = acc["flops_fwd"] + acc["flops_bwd"]
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    assert jfa.device_status(ws) == 0, "kernel status word reports a timeout"
+
+    # Per-kernel live timing -> rooflines.
+    peaks = load_peaks()
+    traffic = load_traffic()
+    kernels = {}
+    for name, flops, nbytes in (("fwd", acc["flops_fwd"], acc["bytes_fwd"]),
+                                ("bwd_pre", acc["flops_pre"], acc["bytes_pre"]),
+                                ("bwd", acc["flops_bwd"], acc["bytes_bwd"])):
+        ms, n = prof[name]
+        avg = ms / max(n, 1)
+        tflops = flops / (avg * 1e-3) / 1e12 if avg > 0 else 0.0
+        gbs = nbytes / (avg * 1e-3) / 1e9 if avg > 0 else 0.0
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if (t_tensor >= t_hbm and name != "bwd_pre") else "hbm"
+        kernels[name] = {"launches": n, "avg_ms": avg, "share": None, "tflops": tflops, "gbs": gbs,
+                         "tensor_frac": tflops / peaks["bf16_tflops"], "hbm_frac": gbs / peaks["hbm_gbs"],
+                         "model_bound": bound, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                         "traffic": traffic.get(name)}
+    total_k = sum(k_["avg_ms"] * k_["launches"] for k_ in kernels.values())
+    for k_ in kernels.values():
+        k_["share"] = k_["avg_ms"] * k_["launches"] / total_k if total_k else None
+    dom_name = max(kernels, key=lambda n_: kernels[n_]["avg_ms"] * kernels[n_]["launches"])
+    dom = kernels[dom_name]
+    if dom["model_bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dom["tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": dom["tflops"] / peaks["bf16_tflops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dom["gbs"] / peaks["hbm_gbs"]}
+    roof.update(kernel=f"jfa_{dom_name}_kernel", traffic=dom["traffic"], peak_source=peaks["source"],
+                algorithmic_per_launch=dom["algorithmic_bytes"] if roof["bound"] == "hbm" else dom["algorithmic_flops"])
+
+    # End to end: pinned host inputs -> device, both passes, outputs -> host, per step.
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
+    ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
+    hdk, hdv = torch.empty(dk.shape, dtype=dk.dtype).pin_memory(), torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, off_h))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        off_d.copy_(off_h, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev) / args.e2e_steps
+    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(x)
+    line = {
+        "metric": "fwd+bwd TFLOPS (bf16, 1 GB300) on jagged broadcast-Q",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC if not args.batch else f"first {B} sequences of: " + WORKLOAD_DESC,
+                   "B": B, "Lq": Lq, "H": H, "D": D, "N": N, "pairs": acc["pairs"],
+                   "l2": "no flush: K+V inputs (~390 MB) exceed the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "fwd_tflops": kernels["fwd"]["tflops"], "bwd_tflops": acc["flops_bwd"] / (
+            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"]) * 1e-3) / 1e12,
+        "tensor_peak_frac": {"fwd": kernels["fwd"]["tensor_frac"], "bwd_kernel": kernels["bwd"]["tensor_frac"],
+                             "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
+        "roofline": roof,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": int(sum(k_["launches"] for k_ in kernels.values())),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

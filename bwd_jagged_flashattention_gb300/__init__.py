@@ -28,7 +28,7 @@ JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUD
 
 # Every symbol include/jfa.h and include/jfa_selftest.h declare.
 EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
-            "jfa_num_ctas", "jfa_selftest_mma")
+            "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +68,11 @@ def lib() -> ctypes.CDLL:
             L.jfa_status_string.restype = ctypes.c_char_p
             L.jfa_num_ctas.argtypes = []
             L.jfa_num_ctas.restype = ci
+            L.jfa_profile_enable.argtypes = [ci]
+            L.jfa_profile_enable.restype = ci
+            dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
+            L.jfa_profile_read.argtypes = [dp, ip, dp, ip, dp, ip]
+            L.jfa_profile_read.restype = ci
             L.jfa_selftest_mma.argtypes = [ci, vp, vp, vp, vp, vp]
             L.jfa_selftest_mma.restype = ci
             L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
@@ -169,6 +174,17 @@ def device_status(workspace, device=None) -> int:
     """Synchronises the current stream and returns (and clears) the kernels' status word."""
     device = workspace.device if device is None else device
     return int(lib().jfa_device_status(_ptr(workspace), _stream(device)))
+
+
+def profile_enable(on: bool = True) -> None:
+    _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
+
+
+def profile_read() -> dict:
+    """Per-kernel event-timed totals since the previous read: {kernel: (ms, launches)}."""
+    v = [ctypes.c_double(), ctypes.c_int(), ctypes.c_double(), ctypes.c_int(), ctypes.c_double(), ctypes.c_int()]
+    _check(lib().jfa_profile_read(*[ctypes.byref(x) for x in v]), "jfa_profile_read")
+    return {"fwd": (v[0].value, v[1].value), "bwd_pre": (v[2].value, v[3].value), "bwd": (v[4].value, v[5].value)}
 
 
 def num_ctas() -> int:

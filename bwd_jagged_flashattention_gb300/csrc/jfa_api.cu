@@ -205,6 +205,56 @@ int64_t count_items(const Problem& pr, int is_bwd) {
     return n * pr.H;
 }
 
+// ---------------------------------------------------------------------------
+// Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
+// ---------------------------------------------------------------------------
+enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2 };
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> pool;
+    std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
+};
+
+Profiler& profiler() {
+    static Profiler p;
+    return p;
+}
+
+cudaEvent_t prof_event(Profiler& p) {
+    if (!p.pool.empty()) {
+        cudaEvent_t e = p.pool.back();
+        p.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Runs `launch` between two recorded events when profiling is on.
+template <typename F>
+cudaError_t timed_launch(int kind, cudaStream_t s, F&& launch) {
+    Profiler& p = profiler();
+    cudaEvent_t a = nullptr, b = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(p.mu);
+        if (p.on) {
+            a = prof_event(p);
+            b = prof_event(p);
+        }
+    }
+    if (a) cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    if (b) {
+        cudaEventRecord(b, s);
+        std::lock_guard<std::mutex> lock(p.mu);
+        p.pending.push_back({kind, {a, b}});
+    }
+    return e;
+}
+
 }  // namespace
 }  // namespace jfa
 
@@ -261,7 +311,8 @@ extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
-    return launch_fwd(D, p, maps, P, s) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+    return timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) == cudaSuccess ? JFA_OK
+                                                                                                : JFA_ERR_CUDA;
 }
 
 extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -307,7 +358,7 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     pp.N = static_cast<int>(pr.N);
     pp.D = D;
     pp.broadcast_q = pr.broadcast_q;
-    if (launch_bwd_pre(pp, s) != cudaSuccess) return JFA_ERR_CUDA;
+    if (timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess) return JFA_ERR_CUDA;
 
     const int64_t n_items = count_items(pr, 1);
     const int P = ctas_for(n_items);
@@ -336,7 +387,8 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     p.causal = pr.causal;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
-    return launch_bwd(D, p, maps, P, s) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+    return timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, P, s); }) == cudaSuccess ? JFA_OK
+                                                                                                : JFA_ERR_CUDA;
 }
 
 extern "C" jfa_status jfa_device_status(void* workspace, void* stream) {
@@ -359,4 +411,38 @@ extern "C" const char* jfa_status_string(jfa_status s) {
         case JFA_ERR_DEVICE_TIMEOUT: return "JFA_ERR_DEVICE_TIMEOUT";
     }
     return "JFA_ERR_UNKNOWN";
+}
+
+extern "C" jfa_status jfa_profile_enable(int on) {
+    Profiler& p = profiler();
+    std::lock_guard<std::mutex> lock(p.mu);
+    p.on = on != 0;
+    return JFA_OK;
+}
+
+extern "C" jfa_status jfa_profile_read(double* fwd_ms, int* fwd_launches, double* pre_ms, int* pre_launches,
+                                       double* bwd_ms, int* bwd_launches) {
+    Profiler& p = profiler();
+    std::lock_guard<std::mutex> lock(p.mu);
+    double ms[3] = {0, 0, 0};
+    int n[3] = {0, 0, 0};
+    jfa_status st = JFA_OK;
+    for (auto& e : p.pending) {
+        float t = 0.0f;
+        if (cudaEventSynchronize(e.second.second) != cudaSuccess ||
+            cudaEventElapsedTime(&t, e.second.first, e.second.second) != cudaSuccess)
+            st = JFA_ERR_CUDA;
+        ms[e.first] += t;
+        n[e.first] += 1;
+        p.pool.push_back(e.second.first);
+        p.pool.push_back(e.second.second);
+    }
+    p.pending.clear();
+    if (fwd_ms) *fwd_ms = ms[kProfFwd];
+    if (fwd_launches) *fwd_launches = n[kProfFwd];
+    if (pre_ms) *pre_ms = ms[kProfPre];
+    if (pre_launches) *pre_launches = n[kProfPre];
+    if (bwd_ms) *bwd_ms = ms[kProfBwd];
+    if (bwd_launches) *bwd_launches = n[kProfBwd];
+    return st;
 }

@@ -120,6 +120,19 @@ jfa_status jfa_device_status(void *workspace, void *stream);
 const char *jfa_status_string(jfa_status s);
 
 /*
+ * Measurement aid (computes nothing).  While enabled, every jfa_fwd and
+ * jfa_bwd call also records a pair of CUDA events on its stream around each
+ * of the library's kernels (the forward kernel; the backward's Delta
+ * pre-pass and its main kernel).  jfa_profile_read() waits for the recorded
+ * events, writes the summed kernel milliseconds and launch counts since the
+ * previous read into the non-NULL pointers, and clears the totals.  The
+ * events are host-owned CUDA events; no device memory is allocated.
+ */
+jfa_status jfa_profile_enable(int on);
+jfa_status jfa_profile_read(double *fwd_ms, int *fwd_launches, double *pre_ms, int *pre_launches, double *bwd_ms,
+                            int *bwd_launches);
+
+/*
  * jfa_num_ctas -- number of persistent CTAs the kernels launch on the current
  * device (one per SM); the schedule deals work to exactly this many.
  */
