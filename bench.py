@@ -233,12 +233,18 @@ def size_oracle_sample(x, budget_s):
 
 
 def cpu_baseline(x, budget_s=12.0):
+    """The oracle as it stands on the host cores: repeated passes over the first n sequences
+    until about budget_s seconds of CPU work have been timed."""
     import oracle
     n = size_oracle_sample(x, budget_s)
-    flops, secs = oracle_sample(x, n)
+    flops = secs = 0.0
+    reps = 0
+    while secs < budget_s * 0.8 and reps < 8:
+        f, t = oracle_sample(x, n)
+        flops, secs, reps = flops + f, secs + t, reps + 1
     return {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on the first {n} of {x['B']} sequences of the same inputs "
-                      f"({flops / 1e9:.1f} GFLOP useful, {secs:.1f} s)"}
+            "sample": f"fp64 oracle fwd+bwd, {reps} pass(es) over the first {n} of {x['B']} sequences of the "
+                      f"same inputs ({flops / 1e9:.1f} GFLOP useful, {secs:.1f} s)"}
 
 
 def first_sequences(x, n):
