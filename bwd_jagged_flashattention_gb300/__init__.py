@@ -28,7 +28,7 @@ JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUD
 
 # Every symbol include/jfa.h and include/jfa_selftest.h declare.
 EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
-            "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma")
+            "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma", "jfa_fwd_static_scratch")
 
 _lock = threading.Lock()
 _lib = None

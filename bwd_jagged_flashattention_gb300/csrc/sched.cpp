@@ -94,6 +94,47 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     return n;
 }
 
+int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
+                               int P, WorkItem* items, int32_t* cta_start, int64_t max_items, WorkItem* gen,
+                               int64_t* order, int32_t* owner, int32_t* fill, int64_t* buckets) {
+    if (P <= 0 || P > kMaxCtas) return -1;
+    int64_t n = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t Lk = offsets[b + 1] - offsets[b];
+        const int64_t nkv = ceil_div(Lk, kTileRows);
+        const int64_t ntiles = is_bwd ? nkv : (broadcast_q ? ceil_div(Lq, kTileRows) : nkv);
+        const int64_t step = is_bwd ? 1 : 2;
+        for (int h = 0; h < H; ++h)
+            for (int64_t m = 0; m < ntiles; m += step) {
+                if (n >= max_items) return -1;
+                const int two = (!is_bwd && m + 1 < ntiles) ? 1 : 0;
+                gen[n++] = {b, offsets[b], Lk, pack_item(h, static_cast<int>(m), two)};
+            }
+    }
+    // Stable counting sort, largest cost first (bucket 0).
+    for (int64_t c = 0; c < kCostBuckets + 2; ++c) buckets[c] = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t cost = std::min<int64_t>(item_cost(gen[i], Lq, broadcast_q, causal, is_bwd), kCostBuckets - 1);
+        ++buckets[(kCostBuckets - 1 - cost) + 1];
+    }
+    for (int64_t c = 1; c < kCostBuckets + 2; ++c) buckets[c] += buckets[c - 1];
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t cost = std::min<int64_t>(item_cost(gen[i], Lq, broadcast_q, causal, is_bwd), kCostBuckets - 1);
+        order[buckets[kCostBuckets - 1 - cost]++] = i;
+    }
+    // Zigzag deal over P CTAs, then CSR placement in deal order.
+    for (int p = 0; p <= P; ++p) cta_start[p] = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = i / P, p = i % P;
+        owner[i] = static_cast<int32_t>((r & 1) ? (P - 1 - p) : p);
+        ++cta_start[owner[i] + 1];
+    }
+    for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
+    for (int p = 0; p < P; ++p) fill[p] = cta_start[p];
+    for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
+    return n;
+}
+
 }  // namespace jfa
 
 // Host-only C entry used by the scheduler's unit tests (no GPU needed).

@@ -47,6 +47,16 @@ int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q)
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
                        int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items);
 
+// Allocation-free twin of build_schedule (same items, order and deal) for
+// callers that cannot allocate: every array comes from the caller.
+//   gen, order, owner: capacity max_items each; fill: P entries;
+//   buckets: kCostBuckets + 2 entries.  Costs of kCostBuckets - 1 or more
+//   share the last bucket (their relative order stays the generation order).
+constexpr int64_t kCostBuckets = 65536;
+int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
+                               int P, WorkItem* items, int32_t* cta_start, int64_t max_items, WorkItem* gen,
+                               int64_t* order, int32_t* owner, int32_t* fill, int64_t* buckets);
+
 // Cost of one item in 128x128 block-products (+1 fixed per-item overhead).
 int64_t item_cost(const WorkItem& w, int Lq, int broadcast_q, int causal, int is_bwd);
 

@@ -120,6 +120,32 @@ jfa_status jfa_device_status(void *workspace, void *stream);
 const char *jfa_status_string(jfa_status s);
 
 /*
+ * jfa_fwd_static_scratch -- jfa_fwd for callers that cannot allocate memory.
+ * The pages describe no such entry point; it exists for code that cannot
+ * provide a workspace, such as a plugin inside an engine that owns all device
+ * memory and forbids allocation while it runs, or a program restricted to a
+ * fixed memory pool.  It computes exactly what jfa_fwd computes, with the
+ * same arguments minus the workspace; offsets_host is required.
+ *
+ * Scratch (tile schedule and status word) lives in a 1 MiB array the library
+ * declares in device global memory; every GPU that loads the library holds
+ * it until the process exits.  The call makes no allocation of any kind (no
+ * cudaMalloc/cudaFree, no pinned or heap memory).  Limit: at most 65,264
+ * forward work items (H x the number of 256-row query-tile pairs summed over
+ * the sequences); larger batches return JFA_ERR_WORKSPACE before any work is
+ * enqueued.  Every call shares the array and overwrites what the previous
+ * call left there; calls whose work overlaps on the GPU (other streams or
+ * threads) race on it and must be serialised by the caller.  The first call
+ * on each device looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  A kernel wait that times
+ * out is recorded in the array's status word, which this entry point clears
+ * at the start of each call and does not report.
+ */
+jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, const int32_t *offsets_host, int B,
+                                  int Lq, int H, int D, int broadcast_q, int causal, float scale, void *o, float *lse,
+                                  void *stream);
+
+/*
  * Measurement aid (computes nothing).  While enabled, every jfa_fwd and
  * jfa_bwd call also records a pair of CUDA events on its stream around each
  * of the library's kernels (the forward kernel; the backward's Delta
