@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "libjfa.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["jfa_api.cu", "fwd.cu", "bwd.cu", "host_util.cu", "selftest.cu", "sched.cpp", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "sched.h", "host_util.h"]
+SOURCES = ["jfa_api.cu", "fwd.cu", "bwd.cu", "host_util.cu", "selftest.cu", "scheduler.cpp", "noalloc.cu"]
+HEADERS = ["ptx.cuh", "kernels.h", "scheduler.h", "host_util.h", "trace.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,19 +44,29 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    """Compile (if stale) and link libjfa.so.  Returns its path."""
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None, trace: bool = False,
+          defines: list[str] | None = None, tag: str = "") -> str:
+    """Compile (if stale) and link libjfa.so.  Returns its path.
+
+    trace=True builds the separate event-trace variant libjfa_trace.so
+    (-DJFA_TRACE), used only to study the kernels' pipelines.  `defines`
+    with a `tag` builds a separately named variant (tuning experiments)."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    if trace:
+        tag = "trace" + tag
+    defines = list(defines or []) + (["JFA_TRACE"] if trace else [])
+    build_dir = BUILD_DIR + (f"_{tag}" if tag else "")
+    lib_path = LIB_PATH.replace("libjfa.so", f"libjfa_{tag}.so") if tag else LIB_PATH
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "jfa.h"),
                                                         os.path.join(ROOT, "include", "jfa_selftest.h")]
     objs, cmds = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD_DIR, src.replace(".", "_") + ".o")
+        obj = os.path.join(build_dir, src.replace(".", "_") + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + hdrs):
-            cmds.append([nvcc] + _flags(verbose_ptxas) + ["-c", path, "-o", obj])
+            cmds.append([nvcc] + _flags(verbose_ptxas) + [f"-D{d}" for d in defines] + ["-c", path, "-o", obj])
     if cmds:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(cmds), os.cpu_count() or 4)) as ex:
             results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), cmds))
@@ -65,16 +75,15 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(c)}")
-    if force or cmds or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
+    if force or cmds or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link of libjfa.so failed")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv)
-    print(LIB_PATH)
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

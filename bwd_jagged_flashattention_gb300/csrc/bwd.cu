@@ -28,18 +28,41 @@
 //
 // Roles (320 threads):
 //   warps 0-3  compute: P^T and dS^T (thread r = key row r = TMEM lane r)
-//   warps 4-7  dQ readout + reduce-add; dK/dV epilogue
+//   warps 4-7  dQ readout + reduce-add; dK/dV epilogue (staged, coalesced)
 //   warp  8    loads: K, V per item; Q_i (+ LSE_i, Delta_i) and dO_i per tile
 //   warp  9    tcgen05 MMA issue and TMEM allocation
+//   warps 10-11 idle (they give their registers to the compute warps)
 #include <cuda_runtime.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kBwdThreads = 320;
+// Tuning knob (compile-time): L2 prefetch of the next item's tiles (measured
+// slower on the ads workload, so off by default).
+#ifndef JFA_BWD_PREFETCH
+#define JFA_BWD_PREFETCH 0
+#endif
+// dK/dV epilogue: 1 = staged through the dS buffer (free at the end of an
+// item) with coalesced copies, 0 = each thread stores its own row (measured
+// faster on the ads workload: it never holds up the compute warps' dS).
+#ifndef JFA_BWD_EPI_STAGED
+#define JFA_BWD_EPI_STAGED 0
+#endif
+
+// 384 threads = three warpgroups (compute, dQ, and load + MMA + two idle
+// warps).  Registers move from the load/MMA warpgroup (which needs ~144 to
+// keep its descriptors without spilling) to the compute warpgroup: launch
+// 384 x 168 = 64,512 = 128 x (kComputeRegs + kDqRegs + kAuxRegs).
+constexpr int kBwdThreads = 384;
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kComputeRegs = 192;
+constexpr uint32_t kDqRegs = 168;
+constexpr uint32_t kAuxRegs = 144;
+static_assert(128 * (kComputeRegs + kDqRegs + kAuxRegs) <= kBwdThreads * kLaunchRegs, "register split exceeds launch");
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,7 +92,7 @@ struct BwdBars {
     uint64_t do_full, do_empty;
     uint64_t s_full, dp_full, p_full, ds_full, ds_empty;
     uint64_t dq_full, dq_empty;
-    uint64_t dkv_full, dkv_empty;
+    uint64_t dkv_full, dv_empty, dk_empty, ds_free;
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -114,46 +137,47 @@ __device__ __forceinline__ bool group_all(int id, bool pred) {
 
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
+// Operand descriptors are built once per buffer; each MMA adds a
+// compile-time offset (16-byte units) so the issuing thread stays lean.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) { return smem_desc(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t saddr) { return smem_desc(saddr, 16384, 1024); }
+
 // C(tmem) = A B^T with both operands K-major [rows][D] (S^T = K Q^T, dP^T = V dO^T).
 template <int D>
-__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+__device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-        mma_ss(d_tmem, smem_desc(a_addr + off, 16, 1024), smem_desc(b_addr + off, 16, 1024), idesc, kk > 0);
+        const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) / 16;
+        mma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
     }
 }
 
 // dV (+)= P^T dO: A = P^T from TMEM (bf16 pairs), B = dO_i [q][D] MN-major.
 template <int D>
-__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint32_t do_addr, uint32_t acc) {
+__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint64_t do_desc, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(do_addr + kk * 2048, 16384, 1024), idesc, (acc | kk) != 0);
+    for (int kk = 0; kk < 8; ++kk) mma_ts(d_tmem, p_tmem + kk * 8, do_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
 }
 
 // dK (+)= dS^T Q: A = dS^T [key][q] K-major (smem), B = Q_i [q][D] MN-major.
 template <int D>
-__device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint32_t ds_addr, uint32_t q_addr, uint32_t acc) {
+__device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint64_t ds_desc_k, uint64_t q_desc_mn, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk / 4) * 16384 + (kk % 4) * 32;
-        mma_ss(d_tmem, smem_desc(ds_addr + aoff, 16, 1024), smem_desc(q_addr + kk * 2048, 16384, 1024), idesc,
-               (acc | kk) != 0);
+        const uint64_t aoff = ((kk / 4) * 16384 + (kk % 4) * 32) / 16;
+        mma_ss(d_tmem, ds_desc_k + aoff, q_desc_mn + kk * (2048 / 16), idesc, (acc | kk) != 0);
     }
 }
 
 // dQ = dS K: A = dS [q][key] read MN-major from the dS^T buffer, B = K [key][D] MN-major.
 template <int D>
-__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint64_t ds_desc_mn, uint64_t k_desc_mn) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 1, 1);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_ss(d_tmem, smem_desc(ds_addr + kk * 2048, 16384, 1024), smem_desc(k_addr + kk * 2048, 16384, 1024),
-               idesc, kk > 0);
+    for (int kk = 0; kk < 8; ++kk) mma_ss(d_tmem, ds_desc_mn + kk * (2048 / 16), k_desc_mn + kk * (2048 / 16), idesc, kk > 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -174,7 +198,21 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
     for (int idx = ib; idx < ie; ++idx) {
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int kv_row = it.kv_start + 128 * it.n;
+        if (lane == 0) JFA_TRACE_EVENT(1, 8, idx, 0);
+        if (JFA_BWD_PREFETCH && lane == 0 && idx + 1 < ie) {  // pull the next item's K, V, Q, dO tiles into L2
+            const BwdItem nx = decode_bwd(p.items[idx + 1], p);
+#pragma unroll
+            for (int s = 0; s < L::kSlabs; ++s) {
+                tma_prefetch_2d(&m->k, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
+                tma_prefetch_2d(&m->v, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
+                for (int i = nx.i0; i < nx.i1; ++i) {
+                    tma_prefetch_2d(&m->dout, nx.h * D + 64 * s, nx.o_row0 + 128 * i);
+                    if (!p.broadcast_q) tma_prefetch_2d(&m->q, nx.h * D + 64 * s, nx.q_row0 + 128 * i);
+                }
+            }
+        }
         if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
+        if (lane == 0) JFA_TRACE_EVENT(2, 8, idx, 0);
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars.k_full, L::kTileBytes);
 #pragma unroll
@@ -190,6 +228,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                 tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.v_full, it.h * D + 64 * s, kv_row);
         }
         ++v_cnt;
+        if (lane == 0) JFA_TRACE_EVENT(3, 8, idx, 0);
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             if (!mbar_wait_warp(&bars.q_empty[st], ((q_cnt / 2) & 1) ^ 1, ab)) goto done;
@@ -219,6 +258,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                                 it.h * D + 64 * s, it.q_row0 + 128 * i);
             }
             ++q_cnt;
+            if (lane == 0) JFA_TRACE_EVENT(4, 8, i, 0);
             if (!mbar_wait_warp(&bars.do_empty, (do_cnt & 1) ^ 1, ab)) goto done;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars.do_full, L::kTileBytes);
@@ -228,6 +268,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                                 it.o_row0 + 128 * i);
             }
             ++do_cnt;
+            if (lane == 0) JFA_TRACE_EVENT(5, 8, i, 0);
         }
     }
 done:
@@ -248,37 +289,67 @@ template <int D>
 __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = BwdLayout<D>;
-    const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-    const uint32_t sQ = smem_u32(smem + L::kQ), sDO = smem_u32(smem + L::kDO), sDS = smem_u32(smem + L::kDS);
+    const uint64_t dK_k = kmajor_desc(smem_u32(smem + L::kK)), dK_mn = mnmajor_desc(smem_u32(smem + L::kK));
+    const uint64_t dV_k = kmajor_desc(smem_u32(smem + L::kV));
+    const uint64_t dQ_k = kmajor_desc(smem_u32(smem + L::kQ)), dQ_mn = mnmajor_desc(smem_u32(smem + L::kQ));
+    const uint64_t dDO_k = kmajor_desc(smem_u32(smem + L::kDO)), dDO_mn = mnmajor_desc(smem_u32(smem + L::kDO));
+    const uint64_t dDS_k = kmajor_desc(smem_u32(smem + L::kDS)), dDS_mn = mnmajor_desc(smem_u32(smem + L::kDS));
+    constexpr uint64_t kTileUnits = L::kTileBytes / 16;
     uint32_t it_cnt = 0, q_cnt = 0, tile_cnt = 0;
     for (int idx = ib; idx < ie; ++idx) {
         const BwdItem it = decode_bwd(p.items[idx], p);
+        JFA_TRACE_EVENT(10, 9, idx, 0);
         if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
+        JFA_TRACE_EVENT(11, 9, idx, 0);
         if (!mbar_wait(&bars.v_full, it_cnt & 1, ab)) goto done;
-        for (int i = it.i0; i < it.i1; ++i) {
+        JFA_TRACE_EVENT(12, 9, idx, 0);
+        // S^T of the first query tile; later tiles' S^T are issued as soon as
+        // the previous tile's dS^T is written (before its dK and dQ), so the
+        // compute warps can start the next P while the tensor core finishes
+        // dK and dQ of this tile.
+        {
             const int st = q_cnt % 2;
             if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
+            JFA_TRACE_EVENT(13, 9, it.i0, 0);
             tc_fence_after();
-            issue_kmajor<D>(tmem + L::kColS, sK, sQ + st * L::kTileBytes);  // S^T = K Q^T
+            issue_kmajor<D>(tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
             mma_commit(&bars.s_full);
+        }
+        for (int i = it.i0; i < it.i1; ++i) {
+            const int st = q_cnt % 2;
             if (!mbar_wait(&bars.do_full, tile_cnt & 1, ab)) goto done;
+            JFA_TRACE_EVENT(15, 9, i, 0);
             if (!mbar_wait(&bars.dq_empty, (tile_cnt & 1) ^ 1, ab)) goto done;  // previous dQ read out
+            JFA_TRACE_EVENT(16, 9, i, 0);
             tc_fence_after();
-            issue_kmajor<D>(tmem + L::kColDP, sV, sDO);  // dP^T = V dO^T
+            issue_kmajor<D>(tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
             mma_commit(&bars.dp_full);
             if (i == it.i1 - 1) mma_commit(&bars.v_empty);
-            if (i == it.i0) {
-                if (!mbar_wait(&bars.dkv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+            if (i == it.i0) {  // the previous item's dV has been read out of TMEM
+                if (!mbar_wait(&bars.dv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+                JFA_TRACE_EVENT(18, 9, i, 0);
             }
             if (!mbar_wait(&bars.p_full, tile_cnt & 1, ab)) goto done;
+            JFA_TRACE_EVENT(19, 9, i, 0);
             tc_fence_after();
-            issue_dv<D>(tmem + L::kColDV, tmem + L::kColS, sDO, i > it.i0);
+            issue_dv<D>(tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
             mma_commit(&bars.do_empty);
             if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
+            JFA_TRACE_EVENT(20, 9, i, 0);
+            if (i + 1 < it.i1) {  // next tile's S^T: T_S is free (P^T read by dV and by the dS pass)
+                const int st2 = (q_cnt + 1) % 2;
+                if (!mbar_wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1, ab)) goto done;
+                tc_fence_after();
+                issue_kmajor<D>(tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
+                mma_commit(&bars.s_full);
+            }
+            if (i == it.i0) {  // ... and its dK
+                if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+            }
             tc_fence_after();
-            issue_dk<D>(tmem + L::kColDK, sDS, sQ + st * L::kTileBytes, i > it.i0);
+            issue_dk<D>(tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
             mma_commit(&bars.q_empty[st]);
-            issue_dq<D>(tmem + L::kColDP, sDS, sK);
+            issue_dq<D>(tmem + L::kColDP, dDS_mn, dK_mn);
             mma_commit(&bars.dq_full);
             mma_commit(&bars.ds_empty);
             ++q_cnt;
@@ -299,21 +370,39 @@ done:
 template <int D, bool kMask>
 __device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* lse2, uint32_t s_addr, int key,
                                               int qbase, int q_rows, bool row_valid) {
+    // All 128 scores of this key row in one batch of TMEM loads, one wait.
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+    tmem_ld_wait();
+    // Queries qbase .. qbase + nvis - 1 see this key (sequence end, causal bound).
+    int nvis = 128;
+    if (kMask) {
+        nvis = row_valid ? min(128, q_rows - qbase) : 0;
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(s_addr + c * 32, sr);
-        tmem_ld_wait();
         uint32_t pk[16];
+        float l2[32];  // the 32 queries' log2-LSE, read 4 at a time (same address for every thread)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float4 f = reinterpret_cast<const float4*>(lse2)[c * 8 + v];
+            l2[4 * v] = f.x;
+            l2[4 * v + 1] = f.y;
+            l2[4 * v + 2] = f.z;
+            l2[4 * v + 3] = f.w;
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int q0 = c * 32 + 2 * e;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, -lse2[q0]));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, -lse2[q0 + 1]));
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1]), p.scale_log2,
+                  p.scale_log2, -l2[2 * e], -l2[2 * e + 1]);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
             if (kMask) {
-                const int qa = qbase + q0, qb = qa + 1;
-                if (!(row_valid && qa < q_rows && (!p.causal || key <= qa))) p0 = 0.0f;
-                if (!(row_valid && qb < q_rows && (!p.causal || key <= qb))) p1 = 0.0f;
+                if (q0 >= nvis || (p.causal && key > qbase + q0)) p0 = 0.0f;
+                if (q0 + 1 >= nvis || (p.causal && key > qbase + q0 + 1)) p1 = 0.0f;
             }
             pk[e] = pack_bf16x2(p0, p1);
         }
@@ -326,26 +415,42 @@ template <int D>
 __device__ __forceinline__ void bwd_compute_ds(const float* delta, uint32_t s_addr, uint32_t dp_addr, uint8_t* ds_tile,
                                                int row) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t dp[32], pp[16];
-        tmem_ld32(dp_addr + c * 32, dp);
-        tmem_ld16(s_addr + c * 16, pp);
-        tmem_ld_wait();
-        uint32_t pk[16];
+    for (int h = 0; h < 2; ++h) {  // two halves of 64 queries: one TMEM wait each
+        uint32_t dp[2][32], pp[2][16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int q0 = c * 32 + 2 * e;
-            const float d0 = bf16lo_to_f32(pp[e]) * (__uint_as_float(dp[2 * e]) - delta[q0]);
-            const float d1 = bf16hi_to_f32(pp[e]) * (__uint_as_float(dp[2 * e + 1]) - delta[q0 + 1]);
-            pk[e] = pack_bf16x2(d0, d1);
+        for (int u = 0; u < 2; ++u) {
+            tmem_ld32(dp_addr + (2 * h + u) * 32, dp[u]);
+            tmem_ld16(s_addr + (2 * h + u) * 16, pp[u]);
         }
-        // Row `row`, queries c*32 .. c*32+31: slab c/2, 16-byte chunks (c%2)*4 .. +3,
-        // stored at chunk ^ (row % 8) (128-byte swizzle, as TMA would place them).
-        uint8_t* slab = ds_tile + (c / 2) * 16384 + row * 128;
+        tmem_ld_wait();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int chunk = ((c % 2) * 4 + v) ^ (row % 8);
-            *reinterpret_cast<uint4*>(slab + chunk * 16) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int u = 0; u < 2; ++u) {
+            const int c = 2 * h + u;
+            uint32_t pk[16];
+            float dl[32];  // Delta of the 32 queries, read 4 at a time
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 f = reinterpret_cast<const float4*>(delta)[c * 8 + v];
+                dl[4 * v] = f.x;
+                dl[4 * v + 1] = f.y;
+                dl[4 * v + 2] = f.z;
+                dl[4 * v + 3] = f.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float d0 = bf16lo_to_f32(pp[u][e]) * (__uint_as_float(dp[u][2 * e]) - dl[2 * e]);
+                const float d1 = bf16hi_to_f32(pp[u][e]) * (__uint_as_float(dp[u][2 * e + 1]) - dl[2 * e + 1]);
+                pk[e] = pack_bf16x2(d0, d1);
+            }
+            // Row `row`, queries c*32 .. c*32+31: slab c/2, 16-byte chunks (c%2)*4 .. +3,
+            // stored at chunk ^ (row % 8) (128-byte swizzle, as TMA would place them).
+            uint8_t* slab = ds_tile + (c / 2) * 16384 + row * 128;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int chunk = ((c % 2) * 4 + v) ^ (row % 8);
+                *reinterpret_cast<uint4*>(slab + chunk * 16) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
         }
     }
 }
@@ -359,31 +464,40 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
     const uint32_t s_addr = tmem + lane_off + L::kColS;
     const uint32_t dp_addr = tmem + lane_off + L::kColDP;
     uint8_t* ds_tile = smem + L::kDS;
-    uint32_t q_cnt = 0, tile_cnt = 0;
-    for (int idx = ib; idx < ie; ++idx) {
+    uint32_t q_cnt = 0, tile_cnt = 0, item_cnt = 0;
+    for (int idx = ib; idx < ie; ++idx, ++item_cnt) {
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int key = 128 * it.n + row;
         const bool row_valid = key < it.Lk;
         const bool kv_full_tile = 128 * (it.n + 1) <= it.Lk;
+        if (row == 0) JFA_TRACE_EVENT(30, 0, idx, 0);
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             const float* lse2 = reinterpret_cast<const float*>(smem + L::kStats + st * 1024);
             const float* delta = lse2 + 128;
             if (!mbar_wait_warp(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
             if (!mbar_wait_warp(&bars.s_full, tile_cnt & 1, ab)) goto done;
+            if (row == 0) JFA_TRACE_EVENT(31, 0, i, 0);
             tc_fence_after();
             const bool unmasked = kv_full_tile && 128 * (i + 1) <= it.q_rows && !(p.causal && i == it.n);
             if (unmasked)
                 bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
             else
                 bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
+            if (row == 0) JFA_TRACE_EVENT(32, 0, i, 0);
             tc_fence_before();
             mbar_arrive(&bars.p_full);
             if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
+            if (row == 0) JFA_TRACE_EVENT(33, 0, i, 0);
             if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
+            if (JFA_BWD_EPI_STAGED && i == it.i0) {  // the previous item's dK/dV staging has left the buffer
+                if (!mbar_wait_warp(&bars.ds_free, (item_cnt & 1) ^ 1, ab)) goto done;
+            }
+            if (row == 0) JFA_TRACE_EVENT(34, 0, i, 0);
             tc_fence_after();
             bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
             fence_proxy_async_smem();
+            if (row == 0) JFA_TRACE_EVENT(35, 0, i, 0);
             tc_fence_before();
             mbar_arrive(&bars.ds_full);
             ++q_cnt;
@@ -413,6 +527,7 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
         for (int i = it.i0; i < it.i1; ++i) {
             bool ok = mbar_wait_warp(&bars.dq_full, tile_cnt & 1, ab);
             if (!group_all(1, ok)) goto done;
+            if (issuer) JFA_TRACE_EVENT(41, 4, i, 0);
             tc_fence_after();
             uint32_t v[D / 32][32];
 #pragma unroll
@@ -420,6 +535,7 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
+            if (issuer) JFA_TRACE_EVENT(42, 4, i, 0);
 #pragma unroll
             for (int sl = 0; sl < D / 16; ++sl) {
                 const int st = stage_uses % 2;
@@ -443,43 +559,77 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
                 }
                 ++stage_uses;
             }
+            if (issuer) JFA_TRACE_EVENT(43, 4, i, 0);
             ++tile_cnt;
         }
-        // dK / dV epilogue for key rows of this tile.
+        // dK / dV epilogue in 64-column halves: TMEM -> registers -> the dS
+        // tile's smem (free once the item's last dK/dQ products are done;
+        // 128-byte swizzle) -> coalesced row copies (each warp store covers
+        // four whole 128-byte segments; rows past the sequence end are
+        // skipped).  dV's TMEM is released after its last half is read, then
+        // dK's, so the next item's products can start; ds_free tells the
+        // compute warps when they may write dS again.
         {
             bool ok = mbar_wait_warp(&bars.dkv_full, it_cnt & 1, ab);
             if (!group_all(1, ok)) goto done;
+            if (issuer) JFA_TRACE_EVENT(44, 4, idx, 0);
             tc_fence_after();
-            const int key = 128 * it.n + r;
-            const bool valid = key < it.Lk;
-            const int64_t grow = (static_cast<int64_t>(it.kv_start) + key) * p.H + it.h;
+            uint8_t* ep_stage = smem + L::kDS;  // dK/dV staging: the dS tile is free until ds_free
+            const int rows_valid = min(128, it.Lk - 128 * it.n);
+            const int64_t row0 = static_cast<int64_t>(it.kv_start) + 128 * it.n;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled)
-                uint32_t v[D / 32][32];
                 const uint32_t col = which ? L::kColDK : L::kColDV;
+                const float sc = which ? p.scale : 1.0f;
+                uint16_t* out = which ? p.dk : p.dv;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + col + c * 32, v[c]);
-                tmem_ld_wait();
-                if (which == 1) {
-                    tc_fence_before();
-                    mbar_arrive(&bars.dkv_empty);
-                }
-                if (valid) {
-                    const float sc = which ? p.scale : 1.0f;
-                    uint16_t* dst = (which ? p.dk : p.dv) + grow * D;
+                for (int half = 0; half < D / 64; ++half) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tmem + lane_off + col + half * 64, v[0]);
+                    tmem_ld32(tmem + lane_off + col + half * 64 + 32, v[1]);
+                    tmem_ld_wait();
+                    if (half == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(which ? &bars.dk_empty : &bars.dv_empty);
+                    }
+                    if (!JFA_BWD_EPI_STAGED) {
+                        if (r < rows_valid) {
+                            uint4* dst = reinterpret_cast<uint4*>(out + ((row0 + r) * p.H + it.h) * D + half * 64);
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 u;
-                            u.x = pack_bf16x2(__uint_as_float(v[c][8 * q + 0]) * sc, __uint_as_float(v[c][8 * q + 1]) * sc);
-                            u.y = pack_bf16x2(__uint_as_float(v[c][8 * q + 2]) * sc, __uint_as_float(v[c][8 * q + 3]) * sc);
-                            u.z = pack_bf16x2(__uint_as_float(v[c][8 * q + 4]) * sc, __uint_as_float(v[c][8 * q + 5]) * sc);
-                            u.w = pack_bf16x2(__uint_as_float(v[c][8 * q + 6]) * sc, __uint_as_float(v[c][8 * q + 7]) * sc);
-                            reinterpret_cast<uint4*>(dst + c * 32)[q] = u;
+                            for (int ch = 0; ch < 8; ++ch) {
+                                const uint32_t* f = &v[ch / 4][(ch % 4) * 8];
+                                dst[ch] = make_uint4(pack_bf16x2(__uint_as_float(f[0]) * sc, __uint_as_float(f[1]) * sc),
+                                                     pack_bf16x2(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
+                                                     pack_bf16x2(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
+                                                     pack_bf16x2(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
+                            }
                         }
+                        continue;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t* f = &v[ch / 4][(ch % 4) * 8];
+                        *reinterpret_cast<uint4*>(ep_stage + half * 16384 + r * 128 + ((ch ^ (r & 7)) * 16)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(f[0]) * sc, __uint_as_float(f[1]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
+                    }
+                    group_sync(1);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int q = r + 128 * k;
+                        const int rr = q >> 3, ch = q & 7;
+                        if (rr < rows_valid)
+                            *reinterpret_cast<uint4*>(out + ((row0 + rr) * p.H + it.h) * D + half * 64 + ch * 8) =
+                                *reinterpret_cast<const uint4*>(ep_stage + half * 16384 + rr * 128 +
+                                                                ((ch ^ (rr & 7)) * 16));
+                    }
+                    group_sync(1);
                 }
             }
+            if (JFA_BWD_EPI_STAGED) mbar_arrive(&bars.ds_free);  // the compute warps may write dS again
+            if (issuer) JFA_TRACE_EVENT(45, 4, idx, 0);
             ++it_cnt;
         }
     }
@@ -498,6 +648,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
     const AbortState ab{&bars.abort_flag, p.status};
 
+    JFA_TRACE_INIT();
     if (threadIdx.x == 0) {
         bars.abort_flag = 0;
         mbar_init(&bars.k_full, 1);
@@ -518,7 +669,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars.dq_full, 1);
         mbar_init(&bars.dq_empty, 128);
         mbar_init(&bars.dkv_full, 1);
-        mbar_init(&bars.dkv_empty, 128);
+        mbar_init(&bars.dv_empty, 128);
+        mbar_init(&bars.dk_empty, 128);
+        mbar_init(&bars.ds_free, 128);
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
     }
@@ -532,14 +685,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tmem = bars.tmem_base;
 
     if (warp < 4) {
+        regs_inc<kComputeRegs>();
         bwd_compute_role<D>(p, smem, bars, tmem, ib, ie, ab);
     } else if (warp < 8) {
+        if constexpr (kDqRegs > kLaunchRegs) regs_inc<kDqRegs>();
         bwd_dq_role<D>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);
-    } else if (warp == kWarpLoad) {
-        bwd_load_role<D>(p, &maps, smem, bars, ib, ie, ab);
     } else {
-        if (lane == 0) bwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
-        __syncwarp();
+        regs_dec<kAuxRegs>();
+        if (warp == kWarpLoad) {
+            bwd_load_role<D>(p, &maps, smem, bars, ib, ie, ab);
+        } else if (warp == kWarpMma) {
+            if (lane == 0) bwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
@@ -594,8 +752,12 @@ cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStr
     using L = BwdLayout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+        // The register split is only safe at exactly kLaunchRegs per thread.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_bwd_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
+        e = cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -624,3 +786,5 @@ cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cu
 }
 
 }  // namespace jfa
+
+JFA_TRACE_DEFINE_READER(jfa_trace_read_bwd)

@@ -9,6 +9,7 @@
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA loads: Q tiles once per item, K/V tiles through a ring
 //   warp  9    tcgen05 MMA issue (one thread) and TMEM allocation
+//   warps 10-11 idle (they only give their registers to the softmax warps)
 // Tensor memory (512 columns): S0 | S1 | O0 | O1.  P (bf16) is written back
 // over the first half of its S columns and fed to the PV product straight
 // from TMEM (S and P have non-overlapping lifetimes, as the pages' TMEM
@@ -23,11 +24,30 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace jfa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+// Tuning knobs (compile-time): K/V ring depth in 128-row tiles at D=128, and
+// how many KV blocks ahead of the ring the L2 prefetch runs (0 = off).
+#ifndef JFA_FWD_SLOTS
+#define JFA_FWD_SLOTS 4
+#endif
+#ifndef JFA_FWD_PREFETCH
+#define JFA_FWD_PREFETCH 0
+#endif
+
+// 384 threads = three warpgroups: two softmax warpgroups and one holding the
+// TMA warp, the MMA warp and two idle warps.  Registers are moved from the
+// third warpgroup to the softmax ones: launch 384 x 168 = 64,512; after the
+// split 256 x kSoftmaxRegs + 128 x kAuxRegs = 64,512 (never more than launch;
+// below 88 the TMA/MMA roles spill, from 200 up the softmax does not).
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 208;
+constexpr uint32_t kAuxRegs = 88;
+static_assert(256 * kSoftmaxRegs + 128 * kAuxRegs <= kFwdThreads * kLaunchRegs, "register split exceeds launch");
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr float kRescaleLog2 = 8.0f;
@@ -38,10 +58,13 @@ struct FwdLayout {
     static constexpr int kSlabBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzle span)
     static constexpr int kSlabs = D / 64;
     static constexpr int kTileBytes = kSlabs * kSlabBytes;
-    static constexpr int kSlots = D == 128 ? 4 : 8;  // K/V ring tiles
+    static constexpr int kSlots = D == 128 ? JFA_FWD_SLOTS : 2 * JFA_FWD_SLOTS;  // K/V ring tiles
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
-    static constexpr int kBytes = (2 + kSlots) * kTileBytes;
+    // Epilogue staging: 128 rows x 64 columns of bf16 (16 KB) per softmax warpgroup.
+    static constexpr int kStageOff = (2 + kSlots) * kTileBytes;
+    static constexpr int kStageBytes = 16384;
+    static constexpr int kBytes = kStageOff + 2 * kStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kOCol = 256;
@@ -49,7 +72,7 @@ struct FwdLayout {
 
 struct FwdBars {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[8], kv_empty[8];
+    uint64_t kv_full[2 * JFA_FWD_SLOTS], kv_empty[2 * JFA_FWD_SLOTS];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -89,30 +112,68 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
     return it;
 }
 
+// Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+// Operand descriptors are built once per buffer; one MMA then only adds a
+// compile-time offset (in 16-byte units) to the start-address field, which
+// keeps the single issuing thread's instruction count per MMA minimal.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) { return smem_desc(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t saddr) { return smem_desc(saddr, 16384, 1024); }
+
 // S(tmem) = Q K^T: both operands K-major in 128-byte-swizzled slabs of 64
 // columns; one K=16 step advances 32 bytes inside a slab.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-        mma_ss(d_tmem, smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024), idesc, kk > 0);
+        constexpr uint64_t unit = 16;
+        const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) / unit;
+        mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0);
     }
 }
 
 // O(tmem) (+)= P(tmem, bf16) V: V is MN-major (D contiguous); one K=16 step
 // covers 16 key rows = 2048 bytes; the 64-column slabs are 16 KB apart.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, uint32_t acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(v_addr + kk * 2048, 16384, 1024), idesc, (acc | kk) != 0);
+    for (int kk = 0; kk < 8; ++kk) mma_ts(d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
+}
+
+// L2 prefetch runs this many KV blocks ahead of the smem ring, so the ring's
+// TMA loads hit L2 instead of waiting for HBM.
+constexpr int kPrefetchBlocks = JFA_FWD_PREFETCH;
+
+// Walks the same (item, KV block) sequence as the loads, kPrefetchBlocks ahead.
+struct PrefetchCursor {
+    int i, j, nb, h, kv_start;
+};
+
+template <int D>
+__device__ __forceinline__ void prefetch_next_block(PrefetchCursor& c, const FwdParams& p, int ie,
+                                                    const CUtensorMap* mk, const CUtensorMap* mv) {
+    while (c.i < ie && c.j >= c.nb) {
+        if (++c.i >= ie) return;
+        const FwdItem it = decode_fwd(p.items[c.i], p);
+        c.j = 0;
+        c.nb = it.nb;
+        c.h = it.h;
+        c.kv_start = it.kv_start;
+    }
+    if (kPrefetchBlocks == 0 || c.i >= ie) return;
+#pragma unroll
+    for (int s = 0; s < D / 64; ++s) {
+        tma_prefetch_2d(mk, c.h * D + 64 * s, c.kv_start + 128 * c.j);
+        tma_prefetch_2d(mv, c.h * D + 64 * s, c.kv_start + 128 * c.j);
+    }
+    ++c.j;
 }
 
 // ---------------------------------------------------------------------------
@@ -127,8 +188,11 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     prefetch_tensormap(mk);
     prefetch_tensormap(mv);
     uint32_t ring = 0, q_loads = 0;
+    PrefetchCursor pf{ib - 1, 0, 0, 0, 0};
+    for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D>(pf, p, ie, mk, mv);
     for (int i = ib; i < ie; ++i) {
         const FwdItem it = decode_fwd(p.items[i], p);
+        JFA_TRACE_EVENT(1, 8, i, it.nb);
         if (it.nb == 0) continue;
         if (!mbar_wait(&bars.q_empty, (q_loads & 1) ^ 1, ab)) goto done;
         mbar_arrive_expect_tx(&bars.q_full, it.nq * L::kTileBytes);
@@ -138,6 +202,7 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                 tma_load_2d(smem + L::kQOff + t * L::kTileBytes + s * L::kSlabBytes, mq, &bars.q_full,
                             it.h * D + 64 * s, it.q_row0 + 128 * (it.m0 + t));
         ++q_loads;
+        JFA_TRACE_EVENT(2, 8, i, 0);
         for (int j = 0; j < it.nb; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = ring % L::kSlots;
@@ -147,8 +212,10 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                 for (int s = 0; s < L::kSlabs; ++s)
                     tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
                                 &bars.kv_full[slot], it.h * D + 64 * s, it.kv_start + 128 * j);
+                JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
                 ++ring;
             }
+            prefetch_next_block<D>(pf, p, ie, mk, mv);
         }
     }
 done:
@@ -168,23 +235,28 @@ template <int D>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
-    const uint32_t q_base = smem_u32(smem + L::kQOff);
-    const uint32_t ring_base = smem_u32(smem + L::kRingOff);
+    const uint64_t q_desc = kmajor_desc(smem_u32(smem + L::kQOff));
+    const uint64_t k_desc = kmajor_desc(smem_u32(smem + L::kRingOff));
+    const uint64_t v_desc = mnmajor_desc(smem_u32(smem + L::kRingOff));
+    constexpr uint64_t kTileUnits = L::kTileBytes / 16;  // descriptor step between tiles
     uint32_t ring = 0, q_ph = 0;
     uint32_t p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
     for (int i = ib; i < ie; ++i) {
         const FwdItem it = decode_fwd(p.items[i], p);
+        JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
         if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
         q_ph ^= 1;
+        JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
         if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
         ++ring;
+        JFA_TRACE_EVENT(12, 9, 0, 0);
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t)
             if (it.nblk[t] > 0) {
-                issue_qk<D>(tmem + t * 128, q_base + t * L::kTileBytes, ring_base + kslot * L::kTileBytes);
+                issue_qk<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
                 mma_commit(&bars.s_full[t]);
             }
         mma_commit(&bars.kv_empty[kslot]);
@@ -193,11 +265,13 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             const uint32_t vslot = ring % L::kSlots;
             if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
             ++ring;
+            JFA_TRACE_EVENT(13, 9, j, 0);
             const bool has_next = j + 1 < it.nb;
             if (has_next) {
                 kslot = ring % L::kSlots;
                 if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
                 ++ring;
+                JFA_TRACE_EVENT(12, 9, j + 1, 0);
             }
             tc_fence_after();
 #pragma unroll
@@ -206,14 +280,18 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 if (j == 0) {
                     if (!mbar_wait(&bars.o_empty[t], oe_ph[t], ab)) goto done;
                     oe_ph[t] ^= 1;
+                    JFA_TRACE_EVENT(17, 9, t, j);
                 }
                 if (!mbar_wait(&bars.p_full[t], p_ph[t], ab)) goto done;
                 p_ph[t] ^= 1;
+                JFA_TRACE_EVENT(15, 9, t, j);
                 tc_fence_after();
-                issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, ring_base + vslot * L::kTileBytes, j > 0);
+                issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                JFA_TRACE_EVENT(16, 9, t, j);
                 if (j == it.nblk[t] - 1) mma_commit(&bars.o_full[t]);
                 if (j + 1 < it.nblk[t]) {
-                    issue_qk<D>(tmem + t * 128, q_base + t * L::kTileBytes, ring_base + kslot * L::kTileBytes);
+                    issue_qk<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                    JFA_TRACE_EVENT(18, 9, t, j + 1);
                     mma_commit(&bars.s_full[t]);
                 }
             }
@@ -242,21 +320,30 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
     for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
     tmem_ld_wait();
     if (kMask) {
+        // Keys kbase .. kbase + nvis - 1 are visible to this row: the
+        // sequence end and (causal) the diagonal bound one count.
         const int kbase = 128 * j;
+        int nvis = it.Lk - kbase;
+        if (p.causal) nvis = min(nvis, qpos - kbase + 1);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int key = kbase + c * 32 + i;
-                const bool vis = key < it.Lk && (!p.causal || key <= qpos);
-                if (!vis) sr[c][i] = __float_as_uint(-INFINITY);
-            }
+            for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= nvis) sr[c][i] = __float_as_uint(-INFINITY);
     }
-    float mx = -INFINITY;
+    // Row max: 8 independent running maxima (short dependency chains), then
+    // a 3-level tree; three-input max halves the instruction count.
+    float mxs[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int a = 0; a < 8; ++a) mxs[a] = fmaxf(__uint_as_float(sr[a / 2][(a % 2) * 16]),
+                                               __uint_as_float(sr[a / 2][(a % 2) * 16 + 1]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
+    for (int a = 0; a < 8; ++a) {
+        const uint32_t* src = &sr[a / 2][(a % 2) * 16];
+#pragma unroll
+        for (int i = 2; i < 16; i += 2) mxs[a] = fmax3(mxs[a], __uint_as_float(src[i]), __uint_as_float(src[i + 1]));
+    }
+    const float mx = fmaxf(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(fmax3(mxs[3], mxs[4], mxs[5]), mxs[6], mxs[7]));
     const float m_new = fmaxf(m_use, mx * p.scale_log2);
     float corr = 1.0f;
     bool resc = false;
@@ -268,19 +355,27 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
         resc = true;
     }
     const float base = m_use == -INFINITY ? 0.0f : m_use;
-    float rs = 0.0f;
+    // P = 2^(s * scale_log2 - base): paired FMAs, then the hardware exp2;
+    // the row sum uses 8 partial sums.
+    float rss[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) rss[a] = 0.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i]), p.scale_log2, -base));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][2 * i + 1]), p.scale_log2, -base));
-            rs += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+        for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1]), p.scale_log2, p.scale_log2,
+                  -base, -base);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            rss[(c * 2 + e / 8)] += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
     }
+    const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
     l = l * corr + rs;
     if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
@@ -302,7 +397,7 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
 }
 
 template <int D>
-__device__ void fwd_softmax_role(const FwdParams& p, FwdBars& bars, uint32_t tmem, int ib, int ie,
+__device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                                  const AbortState& ab) {
     using L = FwdLayout<D>;
     const int t = threadIdx.x / 128;
@@ -317,11 +412,12 @@ __device__ void fwd_softmax_role(const FwdParams& p, FwdBars& bars, uint32_t tme
         if (t >= it.nq) continue;
         const int nblk = t == 0 ? it.nblk[0] : it.nblk[1];   // scalar copies: no
         const int nfull = t == 0 ? it.nfull[0] : it.nfull[1];  // dynamic array indexing
+        if (row == 0) JFA_TRACE_EVENT(20, t, i, nblk);
         const int qpos = 128 * (it.m0 + t) + row;
         const bool valid = qpos < it.q_rows;
         const int64_t orow = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + qpos
                                            : static_cast<int64_t>(it.q_row0) + qpos;
-        uint16_t* optr = p.o + (orow * p.H + it.h) * D;
+        uint16_t* optr = p.o + (orow * p.H + it.h) * D;  // this row of O (empty-sequence path)
         const int64_t lse_idx = p.broadcast_q ? (static_cast<int64_t>(it.b) * p.H + it.h) * p.Lq + qpos
                                               : static_cast<int64_t>(it.h) * p.N + it.q_row0 + qpos;
         if (nblk == 0) {  // empty sequence: O = 0, LSE = -inf
@@ -337,22 +433,30 @@ __device__ void fwd_softmax_role(const FwdParams& p, FwdBars& bars, uint32_t tme
         for (; j < nfull; ++j) {  // bulk: every key visible, no mask
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
+            if (row == 0) JFA_TRACE_EVENT(21, t, j, 0);
             tc_fence_after();
             softmax_block<D, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            if (row == 0) JFA_TRACE_EVENT(22, t, j, 0);
             tc_fence_before();
             mbar_arrive(&bars.p_full[t]);
         }
         for (; j < nblk; ++j) {  // tail: ragged end and/or causal diagonal
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
+            if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
             softmax_block<D, true>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
             tc_fence_before();
             mbar_arrive(&bars.p_full[t]);
         }
         // Epilogue: O / l to bf16, LSE = ln(sum exp) of the scaled scores.
+        // O leaves TMEM first (freeing it for the next item's PV), then goes
+        // out through a 128-byte-swizzled smem stage in 64-column halves, so
+        // each warp store covers four whole 128-byte segments.
         if (!mbar_wait_warp(&bars.o_full[t], o_ph, ab)) goto done;
         o_ph ^= 1;
+        if (row == 0) JFA_TRACE_EVENT(23, t, i, 0);
         tc_fence_after();
         {
             uint32_t orr[D / 32][32];
@@ -361,26 +465,38 @@ __device__ void fwd_softmax_role(const FwdParams& p, FwdBars& bars, uint32_t tme
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars.o_empty[t]);  // TMEM O is free: the next item's PV may start
-            if (valid) {
-                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            if (valid) p.lse[lse_idx] = l > 0.0f ? (m_use + lg2_approx(l)) * kLn2 : -INFINITY;
+            uint8_t* stage = smem + L::kStageOff + t * L::kStageBytes;
+            const int64_t row0 = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + 128 * (it.m0 + t)
+                                               : static_cast<int64_t>(it.q_row0) + 128 * (it.m0 + t);
+            const int rows_valid = min(128, it.q_rows - 128 * (it.m0 + t));
 #pragma unroll
-                for (int oc = 0; oc < D / 32; ++oc)
+            for (int half = 0; half < D / 64; ++half) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(orr[oc][8 * v + 0]) * inv,
-                                          __uint_as_float(orr[oc][8 * v + 1]) * inv);
-                        u.y = pack_bf16x2(__uint_as_float(orr[oc][8 * v + 2]) * inv,
-                                          __uint_as_float(orr[oc][8 * v + 3]) * inv);
-                        u.z = pack_bf16x2(__uint_as_float(orr[oc][8 * v + 4]) * inv,
-                                          __uint_as_float(orr[oc][8 * v + 5]) * inv);
-                        u.w = pack_bf16x2(__uint_as_float(orr[oc][8 * v + 6]) * inv,
-                                          __uint_as_float(orr[oc][8 * v + 7]) * inv);
-                        reinterpret_cast<uint4*>(optr + oc * 32)[v] = u;
+                for (int ch = 0; ch < 8; ++ch) {  // 8 bf16 per 16-byte chunk
+                    const uint32_t* f = &orr[half * 2 + ch / 4][(ch % 4) * 8];
+                    const uint4 u = make_uint4(pack_bf16x2(__uint_as_float(f[0]) * inv, __uint_as_float(f[1]) * inv),
+                                               pack_bf16x2(__uint_as_float(f[2]) * inv, __uint_as_float(f[3]) * inv),
+                                               pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv),
+                                               pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv));
+                    *reinterpret_cast<uint4*>(stage + row * 128 + ((ch ^ (row & 7)) * 16)) = u;
+                }
+                group_sync(1 + t);
+                // 128 rows x 8 chunks: thread k of the warpgroup copies chunks k, k+128, ...
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int q = row + 128 * k;
+                    const int r = q >> 3, ch = q & 7;
+                    if (r < rows_valid) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(stage + r * 128 + ((ch ^ (r & 7)) * 16));
+                        *reinterpret_cast<uint4*>(p.o + ((row0 + r) * p.H + it.h) * D + half * 64 + ch * 8) = u;
                     }
-                p.lse[lse_idx] = l > 0.0f ? (m_use + lg2_approx(l)) * kLn2 : -INFINITY;
+                }
+                group_sync(1 + t);
             }
         }
+        if (row == 0) JFA_TRACE_EVENT(24, t, i, 0);
     }
 done:;
 }
@@ -397,6 +513,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
     const AbortState ab{&bars.abort_flag, p.status};
 
+    JFA_TRACE_INIT();
     if (threadIdx.x == 0) {
         bars.abort_flag = 0;
         mbar_init(&bars.q_full, 1);
@@ -423,16 +540,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    if (threadIdx.x == 0 || threadIdx.x == 128 || threadIdx.x == 256 || threadIdx.x == 288)
+        JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     if (warp < 8) {
-        fwd_softmax_role<D>(p, bars, tmem, ib, ie, ab);
-    } else if (warp == kWarpTma) {
-        if (lane == 0) fwd_tma_role<D>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
-        __syncwarp();
+        regs_inc<kSoftmaxRegs>();
+        fwd_softmax_role<D>(p, smem, bars, tmem, ib, ie, ab);
     } else {
-        if (lane == 0) fwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
-        __syncwarp();
+        regs_dec<kAuxRegs>();
+        if (warp == kWarpTma) {
+            if (lane == 0) fwd_tma_role<D>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
+            __syncwarp();
+        } else if (warp == kWarpMma) {
+            if (lane == 0) fwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
+            __syncwarp();
+        }
     }
 
+    if (threadIdx.x == 0 || threadIdx.x == 128 || threadIdx.x == 256 || threadIdx.x == 288)
+        JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -444,8 +569,13 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
     using L = FwdLayout<D>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(jfa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+        // The register split above is only safe if the kernel launches with
+        // exactly kLaunchRegs registers per thread; refuse to launch otherwise.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_fwd_kernel<D>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
+        e = cudaFuncSetAttribute(jfa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -461,3 +591,5 @@ cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cu
 }
 
 }  // namespace jfa
+
+JFA_TRACE_DEFINE_READER(jfa_trace_read_fwd)

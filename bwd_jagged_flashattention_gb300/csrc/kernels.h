@@ -6,7 +6,7 @@
 
 #include <cstdint>
 
-#include "sched.h"
+#include "scheduler.h"
 
 namespace jfa {
 

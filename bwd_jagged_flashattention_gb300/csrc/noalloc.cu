@@ -29,7 +29,7 @@
 #include "../../include/jfa.h"
 #include "host_util.h"
 #include "kernels.h"
-#include "sched.h"
+#include "scheduler.h"
 
 namespace jfa {
 namespace {

@@ -65,8 +65,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Suspend-time hint of a barrier wait, in nanoseconds: the waiting thread
+// sleeps in hardware until the phase completes (or the hint elapses) instead
+// of spinning and taking issue slots from the warps that do the work.
+#ifndef JFA_WAIT_HINT_NS
+#define JFA_WAIT_HINT_NS 1000000
+#endif
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
     uint32_t ok;
+#if JFA_WAIT_HINT_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(static_cast<uint32_t>(JFA_WAIT_HINT_NS))
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
@@ -74,6 +90,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         : "=r"(ok)
         : "r"(bar_addr), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -92,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (JFA_WAIT_HINT_NS > 0 || (it & 63u) == 0) {
             if (*ab.smem_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 *ab.smem_flag = 1u;
@@ -111,7 +128,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs / 4) return false;
+        if ((JFA_WAIT_HINT_NS > 0 || (it & 63u) == 0) && global_timer_ns() - t0 > kWaitLimitNs / 4) return false;
     }
 }
 
@@ -151,6 +168,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
         "%5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// Pull a tile of global memory into L2 ahead of its TMA load (no smem, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
 }
 
 // Element-wise fp32 add of a shared-memory tile into global memory (bulk
@@ -316,6 +347,20 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
+// Per-warpgroup register reallocation (all four warps of a warpgroup execute
+// the same instruction).  The host checks the kernel's launch register count
+// so that what the .inc warpgroups take never exceeds what .dec released.
+// ---------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
 // Small arithmetic helpers (hardware instructions, not library math).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -328,6 +373,25 @@ __device__ __forceinline__ float lg2_approx(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// d = a * b + c on two fp32 lanes at once (Blackwell paired-fp32 FMA).
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}\n"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// max of three fp32 values in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // Two fp32 values to a packed bf16x2 (round to nearest even); `lo` goes to

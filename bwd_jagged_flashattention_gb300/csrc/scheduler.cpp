@@ -1,5 +1,5 @@
-// sched.cpp -- see sched.h.
-#include "sched.h"
+// scheduler.cpp -- see scheduler.h.
+#include "scheduler.h"
 
 #include <algorithm>
 #include <vector>

@@ -1,4 +1,4 @@
-// sched.h -- host tile scheduler: work items, cost model, LPT sort and
+// scheduler.h -- host tile scheduler: work items, cost model, LPT sort and
 // zigzag deal to persistent CTAs.
 //
 // The pages describe this step for the forward pass: tiles are sorted on the
