@@ -71,8 +71,11 @@ def accounting(x):
     bytes_fwd = q_b + 2 * kv_b + o_b + stat_b                       # Q, K, V in; O, LSE out
     bytes_pre = 2 * o_b + stat_b                                     # O, dO in; Delta out
     bytes_bwd = q_b + 2 * kv_b + o_b + 2 * stat_b + 2 * kv_b + 2 * q_b  # Q,K,V,dO,LSE,Delta in; dK,dV,dQ(fp32) out
+    dq_groups = 0  # partial dQ buffers are off by default in the library (JFA_DQ_GROUPS = 1)
+    bytes_sum = 4 * q_rows * e * (dq_groups + 1) if dq_groups else 0      # G partial dQ in, dQ out
     return dict(pairs=pairs, flops_fwd=f_fwd, flops_bwd=f_bwd, bytes_fwd=bytes_fwd, bytes_pre=bytes_pre,
-                bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e)
+                bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e, bytes_sum=bytes_sum,
+                flops_sum=float(q_rows * e * max(dq_groups - 1, 0)))
 
 
 def load_peaks():
@@ -367,14 +370,15 @@ def main():
     kernels = {}
     for name, flops, nbytes in (("fwd", acc["flops_fwd"], acc["bytes_fwd"]),
                                 ("bwd_pre", acc["flops_pre"], acc["bytes_pre"]),
-                                ("bwd", acc["flops_bwd"], acc["bytes_bwd"])):
+                                ("bwd", acc["flops_bwd"], acc["bytes_bwd"]),
+                                ("dq_sum", acc["flops_sum"], acc["bytes_sum"])):
         ms, n = prof[name]
         avg = ms / max(n, 1)
         tflops = flops / (avg * 1e-3) / 1e12 if avg > 0 else 0.0
         gbs = nbytes / (avg * 1e-3) / 1e9 if avg > 0 else 0.0
         t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
         t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-        bound = "tensor" if (t_tensor >= t_hbm and name != "bwd_pre") else "hbm"
+        bound = "tensor" if (t_tensor >= t_hbm and name in ("fwd", "bwd")) else "hbm"
         kernels[name] = {"launches": n, "avg_ms": avg, "share": None, "tflops": tflops, "gbs": gbs,
                          "tensor_frac": tflops / peaks["bf16_tflops"], "hbm_frac": gbs / peaks["hbm_gbs"],
                          "model_bound": bound, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
@@ -443,7 +447,7 @@ def main():
                    "l2": "no flush: K+V inputs (~390 MB) exceed the 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd_tflops": kernels["fwd"]["tflops"], "bwd_tflops": acc["flops_bwd"] / (
-            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"]) * 1e-3) / 1e12,
+            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]) * 1e-3) / 1e12,
         "tensor_peak_frac": {"fwd": kernels["fwd"]["tensor_frac"], "bwd_kernel": kernels["bwd"]["tensor_frac"],
                              "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
         "roofline": roof,

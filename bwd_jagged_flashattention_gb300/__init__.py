@@ -70,8 +70,7 @@ def lib() -> ctypes.CDLL:
             L.jfa_num_ctas.restype = ci
             L.jfa_profile_enable.argtypes = [ci]
             L.jfa_profile_enable.restype = ci
-            dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)
-            L.jfa_profile_read.argtypes = [dp, ip, dp, ip, dp, ip]
+            L.jfa_profile_read.argtypes = [vp, vp, ci]
             L.jfa_profile_read.restype = ci
             L.jfa_selftest_mma.argtypes = [ci, vp, vp, vp, vp, vp]
             L.jfa_selftest_mma.restype = ci
@@ -180,11 +179,16 @@ def profile_enable(on: bool = True) -> None:
     _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
 
 
+PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum")
+
+
 def profile_read() -> dict:
     """Per-kernel event-timed totals since the previous read: {kernel: (ms, launches)}."""
-    v = [ctypes.c_double(), ctypes.c_int(), ctypes.c_double(), ctypes.c_int(), ctypes.c_double(), ctypes.c_int()]
-    _check(lib().jfa_profile_read(*[ctypes.byref(x) for x in v]), "jfa_profile_read")
-    return {"fwd": (v[0].value, v[1].value), "bwd_pre": (v[2].value, v[3].value), "bwd": (v[4].value, v[5].value)}
+    n = len(PROFILE_KINDS)
+    ms, cnt = (ctypes.c_double * n)(), (ctypes.c_int * n)()
+    _check(lib().jfa_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p), n),
+           "jfa_profile_read")
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(PROFILE_KINDS)}
 
 
 def num_ctas() -> int:

@@ -180,6 +180,25 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint64_t ds_desc_mn, u
     for (int kk = 0; kk < 8; ++kk) mma_ss(d_tmem, ds_desc_mn + kk * (2048 / 16), k_desc_mn + kk * (2048 / 16), idesc, kk > 0);
 }
 
+// LSE (as log2; -inf rows become +inf so P = 0) and Delta of queries
+// 128*i + 4*lane .. +3 of item `it` (out-of-range queries: +inf and 0).
+__device__ __forceinline__ void load_stats(const BwdParams& p, const BwdItem& it, int i, int lane, float (&l2)[4],
+                                           float (&dl)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int qi = 128 * i + lane * 4 + e;
+        l2[e] = INFINITY;
+        dl[e] = 0.0f;
+        if (qi < it.q_rows) {
+            const int64_t si = p.broadcast_q ? (static_cast<int64_t>(it.b) * p.H + it.h) * p.Lq + qi
+                                             : static_cast<int64_t>(it.h) * p.N + it.q_row0 + qi;
+            const float lv = p.lse[si];
+            l2[e] = lv == -INFINITY ? INFINITY : lv * kLog2e;
+            dl[e] = p.delta[si];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Load warp (all 32 lanes: lane 0 issues TMA, every lane stages statistics).
 // ---------------------------------------------------------------------------
@@ -233,22 +252,13 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             const int st = q_cnt % 2;
             if (!mbar_wait_warp(&bars.q_empty[st], ((q_cnt / 2) & 1) ^ 1, ab)) goto done;
             // LSE_i (as log2) and Delta_i for the 128 queries of the tile.
+            // (Loading them a tile ahead measured slower: they stay in L2.)
             float* lse2 = reinterpret_cast<float*>(smem + L::kStats + st * 1024);
             float* delta = lse2 + 128;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int qi = 128 * i + lane * 4 + e;
-                float l2 = INFINITY, dl = 0.0f;
-                if (qi < it.q_rows) {
-                    const int64_t si = p.broadcast_q ? (static_cast<int64_t>(it.b) * p.H + it.h) * p.Lq + qi
-                                                     : static_cast<int64_t>(it.h) * p.N + it.q_row0 + qi;
-                    const float lv = p.lse[si];
-                    l2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
-                    dl = p.delta[si];
-                }
-                lse2[lane * 4 + e] = l2;
-                delta[lane * 4 + e] = dl;
-            }
+            float l2[4], dl[4];
+            load_stats(p, it, i, lane, l2, dl);
+            *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(l2[0], l2[1], l2[2], l2[3]);
+            *reinterpret_cast<float4*>(delta + lane * 4) = make_float4(dl[0], dl[1], dl[2], dl[3]);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars.q_full[st], L::kTileBytes);
@@ -524,6 +534,9 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
     if (issuer) prefetch_tensormap(map_dq);
     for (int idx = ib; idx < ie; ++idx) {
         const BwdItem it = decode_bwd(p.items[idx], p);
+        // Broadcast dQ goes to this CTA's partial buffer (group blockIdx % G);
+        // a final pass sums the G partials.
+        const int dq_row0 = p.broadcast_q ? static_cast<int>(blockIdx.x % p.dq_groups) * p.Lq : it.q_row0;
         for (int i = it.i0; i < it.i1; ++i) {
             bool ok = mbar_wait_warp(&bars.dq_full, tile_cnt & 1, ab);
             if (!group_all(1, ok)) goto done;
@@ -554,7 +567,7 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
                 fence_proxy_async_smem();
                 group_sync(1);
                 if (issuer) {
-                    tma_reduce_add_2d(map_dq, stage, it.h * D + sl * 16, it.q_row0 + 128 * i);
+                    tma_reduce_add_2d(map_dq, stage, it.h * D + sl * 16, dq_row0 + 128 * i);
                     bulk_commit_group();
                 }
                 ++stage_uses;
@@ -747,6 +760,23 @@ __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
     }
 }
 
+// dq[e] = sum over g of partial[g * n + e] (float4 lanes; n is a multiple of 4).
+__global__ void __launch_bounds__(256) jfa_dq_sum_kernel(const float4* __restrict__ partial, float4* __restrict__ dq,
+                                                         int64_t n4, int groups) {
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 acc = partial[e];
+        for (int g = 1; g < groups; ++g) {
+            const float4 v = partial[g * n4 + e];
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        dq[e] = acc;
+    }
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
     using L = BwdLayout<D>;
@@ -777,6 +807,16 @@ cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s) {
         jfa_bwd_pre_kernel<128><<<static_cast<int>(blocks), 256, 0, s>>>(p);
     else
         jfa_bwd_pre_kernel<64><<<static_cast<int>(blocks), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t n4 = n / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    jfa_dq_sum_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const float4*>(partial),
+                                                               reinterpret_cast<float4*>(dq), n4, groups);
     return cudaGetLastError();
 }
 

@@ -18,16 +18,25 @@ namespace jfa {
 namespace {
 
 constexpr size_t kStatusBytes = 256;
+
+// Broadcast-Q dQ is summed over the batch by every CTA.  With G > 1 the
+// reduce-adds go to G partial buffers (CTA index mod G), spreading them over
+// G times more L2 lines, and a final pass adds the partials.  G = 8 measured
+// no faster than G = 1 on the ads workload, so the default is the direct sum.
+#ifndef JFA_DQ_GROUPS
+#define JFA_DQ_GROUPS 1
+#endif
+constexpr int kDqGroups = JFA_DQ_GROUPS;
 constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-    size_t fwd_off, bwd_off, region_bytes, delta_off, delta_bytes, total;
+    size_t fwd_off, bwd_off, region_bytes, delta_off, delta_bytes, dqp_off, dqp_bytes, total;
     int64_t max_items;
 };
 
-bool ws_layout(int B, int64_t N, int Lq, int H, int broadcast_q, WsLayout* w) {
+bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout* w) {
     if (B < 0 || N < 0 || H <= 0) return false;
     w->max_items = max_work_items(B, N, Lq, H, broadcast_q);
     w->region_bytes = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
@@ -36,7 +45,11 @@ bool ws_layout(int B, int64_t N, int Lq, int H, int broadcast_q, WsLayout* w) {
     w->delta_off = w->bwd_off + w->region_bytes;
     const int64_t stat_elems = broadcast_q ? static_cast<int64_t>(B) * H * Lq : static_cast<int64_t>(H) * N;
     w->delta_bytes = align_up(static_cast<size_t>(stat_elems) * sizeof(float), 256);
-    w->total = w->delta_off + w->delta_bytes;
+    w->dqp_off = w->delta_off + w->delta_bytes;
+    w->dqp_bytes = (broadcast_q && kDqGroups > 1)
+                       ? align_up(static_cast<size_t>(kDqGroups) * Lq * H * D * sizeof(float), 256)
+                       : 0;
+    w->total = w->dqp_off + w->dqp_bytes;
     return true;
 }
 
@@ -161,7 +174,7 @@ jfa_status check_common(int B, int Lq, int H, int D, int broadcast_q, int causal
 }
 
 jfa_status check_workspace(const Problem& pr, void* workspace, size_t ws_bytes, WsLayout* w) {
-    if (!ws_layout(pr.B, pr.N, pr.Lq, pr.H, pr.broadcast_q, w)) return JFA_ERR_INVALID_ARG;
+    if (!ws_layout(pr.B, pr.N, pr.Lq, pr.H, pr.D, pr.broadcast_q, w)) return JFA_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || ws_bytes < w->total) return JFA_ERR_WORKSPACE;
     return JFA_OK;
 }
@@ -208,7 +221,7 @@ int64_t count_items(const Problem& pr, int is_bwd) {
 // ---------------------------------------------------------------------------
 // Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
 // ---------------------------------------------------------------------------
-enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2 };
+enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfKinds = 4 };
 
 struct Profiler {
     std::mutex mu;
@@ -264,7 +277,7 @@ extern "C" size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D
     (void)causal;
     if (D != 64 && D != 128) return 0;
     WsLayout w;
-    if (!ws_layout(B, total_len, broadcast_q ? Lq : 0, H, broadcast_q, &w)) return 0;
+    if (!ws_layout(B, total_len, broadcast_q ? Lq : 0, H, D, broadcast_q, &w)) return 0;
     return w.total;
 }
 
@@ -335,7 +348,15 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
         return JFA_ERR_UNSUPPORTED;
 
     const size_t elems_kv = static_cast<size_t>(pr.N) * H * D;
-    if (q_rows > 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(q_rows) * H * D * sizeof(float), s) != cudaSuccess)
+    const size_t elems_q = static_cast<size_t>(q_rows) * H * D;
+    char* ws = static_cast<char*>(workspace);
+    // Broadcast dQ with work to do accumulates into kDqGroups partial buffers
+    // in the workspace (zeroed here) and is summed into dq at the end; every
+    // other case accumulates into (or just zeroes) dq itself.
+    const bool partial = pr.broadcast_q && kDqGroups > 1 && o_rows > 0 && pr.N > 0;
+    float* dq_target = partial ? reinterpret_cast<float*>(ws + w.dqp_off) : dq;
+    const size_t dq_target_elems = partial ? elems_q * kDqGroups : elems_q;
+    if (q_rows > 0 && cudaMemsetAsync(dq_target, 0, dq_target_elems * sizeof(float), s) != cudaSuccess)
         return JFA_ERR_CUDA;
     if (o_rows == 0) {  // no query rows: every key gets a zero gradient
         if (elems_kv && (cudaMemsetAsync(dk, 0, elems_kv * 2, s) != cudaSuccess ||
@@ -345,7 +366,6 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     }
     if (pr.N == 0) return JFA_OK;
 
-    char* ws = static_cast<char*>(workspace);
     float* delta = reinterpret_cast<float*>(ws + w.delta_off);
     PreParams pp;
     pp.o = static_cast<const uint16_t*>(o);
@@ -365,12 +385,15 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w.max_items,
                                      ws + w.bwd_off, s, &st);
     if (n < 0) return st;
-    if (n == 0) return JFA_OK;
+    if (n == 0) {
+        if (partial && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
+        return JFA_OK;
+    }
 
     BwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
         !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dout, dout, o_rows, H, D, workspace) ||
-        !map_rows_f32(&maps.dq, dq, q_rows, H, D, workspace))
+        !map_rows_f32(&maps.dq, dq_target, partial ? q_rows * kDqGroups : q_rows, H, D, workspace))
         return JFA_ERR_CUDA;
     BwdParams p;
     p.cta_start = reinterpret_cast<const int32_t*>(ws + w.bwd_off);
@@ -385,10 +408,15 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     p.N = static_cast<int>(pr.N);
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
+    p.dq_groups = partial ? kDqGroups : 1;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
-    return timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, P, s); }) == cudaSuccess ? JFA_OK
-                                                                                                : JFA_ERR_CUDA;
+    if (timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
+    if (partial && timed_launch(kProfDqSum, s, [&] {
+                       return launch_dq_sum(dq_target, dq, static_cast<int64_t>(elems_q), kDqGroups, s);
+                   }) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    return JFA_OK;
 }
 
 extern "C" jfa_status jfa_device_status(void* workspace, void* stream) {
@@ -420,29 +448,26 @@ extern "C" jfa_status jfa_profile_enable(int on) {
     return JFA_OK;
 }
 
-extern "C" jfa_status jfa_profile_read(double* fwd_ms, int* fwd_launches, double* pre_ms, int* pre_launches,
-                                       double* bwd_ms, int* bwd_launches) {
+extern "C" jfa_status jfa_profile_read(double* ms, int* launches, int count) {
     Profiler& p = profiler();
     std::lock_guard<std::mutex> lock(p.mu);
-    double ms[3] = {0, 0, 0};
-    int n[3] = {0, 0, 0};
+    double t_ms[kProfKinds] = {0, 0, 0, 0};
+    int n[kProfKinds] = {0, 0, 0, 0};
     jfa_status st = JFA_OK;
     for (auto& e : p.pending) {
         float t = 0.0f;
         if (cudaEventSynchronize(e.second.second) != cudaSuccess ||
             cudaEventElapsedTime(&t, e.second.first, e.second.second) != cudaSuccess)
             st = JFA_ERR_CUDA;
-        ms[e.first] += t;
+        t_ms[e.first] += t;
         n[e.first] += 1;
         p.pool.push_back(e.second.first);
         p.pool.push_back(e.second.second);
     }
     p.pending.clear();
-    if (fwd_ms) *fwd_ms = ms[kProfFwd];
-    if (fwd_launches) *fwd_launches = n[kProfFwd];
-    if (pre_ms) *pre_ms = ms[kProfPre];
-    if (pre_launches) *pre_launches = n[kProfPre];
-    if (bwd_ms) *bwd_ms = ms[kProfBwd];
-    if (bwd_launches) *bwd_launches = n[kProfBwd];
+    for (int k = 0; k < count && k < kProfKinds; ++k) {
+        if (ms) ms[k] = t_ms[k];
+        if (launches) launches[k] = n[k];
+    }
     return st;
 }

@@ -31,6 +31,7 @@ struct BwdParams {
     uint32_t* status;
     int Lq, H, N;
     int broadcast_q, causal;
+    int dq_groups;             // broadcast: number of partial dQ buffers (rows g*Lq ..)
     float scale, scale_log2;
 };
 
@@ -55,5 +56,6 @@ struct BwdMaps {
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s);
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
+cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s);
 
 }  // namespace jfa

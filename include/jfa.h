@@ -148,15 +148,15 @@ jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, c
 /*
  * Measurement aid (computes nothing).  While enabled, every jfa_fwd and
  * jfa_bwd call also records a pair of CUDA events on its stream around each
- * of the library's kernels (the forward kernel; the backward's Delta
- * pre-pass and its main kernel).  jfa_profile_read() waits for the recorded
- * events, writes the summed kernel milliseconds and launch counts since the
- * previous read into the non-NULL pointers, and clears the totals.  The
- * events are host-owned CUDA events; no device memory is allocated.
+ * of the library's kernels.  jfa_profile_read() waits for the recorded
+ * events and writes, for kernel kind k < count, the summed milliseconds into
+ * ms[k] and the launch count into launches[k] (either pointer may be NULL),
+ * then clears the totals.  Kinds: 0 forward kernel, 1 backward Delta
+ * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum.  The events
+ * are host-owned CUDA events; no device memory is allocated.
  */
 jfa_status jfa_profile_enable(int on);
-jfa_status jfa_profile_read(double *fwd_ms, int *fwd_launches, double *pre_ms, int *pre_launches, double *bwd_ms,
-                            int *bwd_launches);
+jfa_status jfa_profile_read(double *ms, int *launches, int count);
 
 /*
  * jfa_num_ctas -- number of persistent CTAs the kernels launch on the current
