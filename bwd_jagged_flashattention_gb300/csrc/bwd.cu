@@ -49,6 +49,17 @@ namespace {
 // dK/dV epilogue: 1 = staged through the dS buffer (free at the end of an
 // item) with coalesced copies, 0 = each thread stores its own row (measured
 // faster on the ads workload: it never holds up the compute warps' dS).
+// Exponent pairs (of every 16) computed on the FMA pipe in unmasked tiles.
+// Measured: any share > 0 is slower on GB300 (the passes are latency-bound,
+// not special-function-bound), so the default keeps every exponential on the SFU.
+#ifndef JFA_BWD_POLY_PAIRS
+#define JFA_BWD_POLY_PAIRS 0
+#endif
+// Issue the last tile's dQ before its dK, releasing K one product earlier
+// (measured slower on the ads workload: 622 vs 582 us).
+#ifndef JFA_BWD_DQ_FIRST
+#define JFA_BWD_DQ_FIRST 0
+#endif
 #ifndef JFA_BWD_EPI_STAGED
 #define JFA_BWD_EPI_STAGED 0
 #endif
@@ -218,18 +229,6 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int kv_row = it.kv_start + 128 * it.n;
         if (lane == 0) JFA_TRACE_EVENT(1, 8, idx, 0);
-        if (JFA_BWD_PREFETCH && lane == 0 && idx + 1 < ie) {  // pull the next item's K, V, Q, dO tiles into L2
-            const BwdItem nx = decode_bwd(p.items[idx + 1], p);
-#pragma unroll
-            for (int s = 0; s < L::kSlabs; ++s) {
-                tma_prefetch_2d(&m->k, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
-                tma_prefetch_2d(&m->v, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
-                for (int i = nx.i0; i < nx.i1; ++i) {
-                    tma_prefetch_2d(&m->dout, nx.h * D + 64 * s, nx.o_row0 + 128 * i);
-                    if (!p.broadcast_q) tma_prefetch_2d(&m->q, nx.h * D + 64 * s, nx.q_row0 + 128 * i);
-                }
-            }
-        }
         if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
         if (lane == 0) JFA_TRACE_EVENT(2, 8, idx, 0);
         if (lane == 0) {
@@ -248,6 +247,19 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         }
         ++v_cnt;
         if (lane == 0) JFA_TRACE_EVENT(3, 8, idx, 0);
+        if (JFA_BWD_PREFETCH && lane == 0 && idx + 1 < ie) {  // next item's K, V, Q, dO tiles into L2 (after this item's loads)
+            const BwdItem nx = decode_bwd(p.items[idx + 1], p);
+#pragma unroll
+            for (int s = 0; s < L::kSlabs; ++s) {
+                tma_prefetch_2d(&m->k, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
+                tma_prefetch_2d(&m->v, nx.h * D + 64 * s, nx.kv_start + 128 * nx.n);
+                for (int i = nx.i0; i < nx.i1; ++i) {
+                    tma_prefetch_2d(&m->dout, nx.h * D + 64 * s, nx.o_row0 + 128 * i);
+                    if (!p.broadcast_q) tma_prefetch_2d(&m->q, nx.h * D + 64 * s, nx.q_row0 + 128 * i);
+                }
+            }
+        }
+
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             if (!mbar_wait_warp(&bars.q_empty[st], ((q_cnt / 2) & 1) ^ 1, ab)) goto done;
@@ -357,16 +369,27 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
                 if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
             }
             tc_fence_after();
-            issue_dk<D>(tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
-            mma_commit(&bars.q_empty[st]);
-            issue_dq<D>(tmem + L::kColDP, dDS_mn, dK_mn);
-            mma_commit(&bars.dq_full);
-            mma_commit(&bars.ds_empty);
+            if (JFA_BWD_DQ_FIRST && i == it.i1 - 1) {
+                // Last tile: dQ first, so K can be released (and the next item's K
+                // loaded) while dK runs.
+                issue_dq<D>(tmem + L::kColDP, dDS_mn, dK_mn);
+                mma_commit(&bars.dq_full);
+                mma_commit(&bars.k_empty);
+                issue_dk<D>(tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
+                mma_commit(&bars.q_empty[st]);
+                mma_commit(&bars.ds_empty);
+            } else {
+                issue_dk<D>(tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
+                mma_commit(&bars.q_empty[st]);
+                issue_dq<D>(tmem + L::kColDP, dDS_mn, dK_mn);
+                mma_commit(&bars.dq_full);
+                mma_commit(&bars.ds_empty);
+            }
             ++q_cnt;
             ++tile_cnt;
         }
         mma_commit(&bars.dkv_full);
-        mma_commit(&bars.k_empty);
+        if (!JFA_BWD_DQ_FIRST) mma_commit(&bars.k_empty);
         ++it_cnt;
     }
 done:
@@ -408,8 +431,13 @@ __device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* l
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1]), p.scale_log2,
                   p.scale_log2, -l2[2 * e], -l2[2 * e + 1]);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
+            float p0, p1;
+            if (!kMask && poly_pair<JFA_BWD_POLY_PAIRS>(e)) {  // part of the exponentials on the FMA pipe (no -inf here)
+                exp2_fma2(x0, x1, p0, p1);
+            } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+            }
             if (kMask) {
                 if (q0 >= nvis || (p.causal && key > qbase + q0)) p0 = 0.0f;
                 if (q0 + 1 >= nvis || (p.causal && key > qbase + q0 + 1)) p1 = 0.0f;

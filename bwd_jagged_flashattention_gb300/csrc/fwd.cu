@@ -37,6 +37,12 @@ namespace {
 #ifndef JFA_FWD_PREFETCH
 #define JFA_FWD_PREFETCH 0
 #endif
+// Exponent pairs (of every 16) computed on the FMA pipe in unmasked blocks.
+// Measured: any share > 0 is slower on GB300 (the passes are latency-bound,
+// not special-function-bound), so the default keeps every exponential on the SFU.
+#ifndef JFA_FWD_POLY_PAIRS
+#define JFA_FWD_POLY_PAIRS 0
+#endif
 
 // 384 threads = three warpgroups: two softmax warpgroups and one holding the
 // TMA warp, the MMA warp and two idle warps.  Registers are moved from the
@@ -365,11 +371,15 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            float x0, x1;
+            float x0, x1, p0, p1;
             ffma2(x0, x1, __uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1]), p.scale_log2, p.scale_log2,
                   -base, -base);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
+            if (!kMask && poly_pair<JFA_FWD_POLY_PAIRS>(e)) {  // part of the exponentials on the FMA pipe (no -inf here)
+                exp2_fma2(x0, x1, p0, p1);
+            } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+            }
             rss[(c * 2 + e / 8)] += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
         }

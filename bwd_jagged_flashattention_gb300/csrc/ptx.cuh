@@ -387,6 +387,49 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// d = a + b on two fp32 lanes at once.
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}\n"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// 2^x for a pair of values on the FMA/ALU pipes instead of the special-
+// function unit (which runs at a quarter of the FMA rate).  Our own scheme:
+//   * range reduction: t = x + 1.5*2^23 rounds x to the nearest integer n
+//     (held in t's low mantissa bits); f = x - n lies in [-1/2, 1/2];
+//   * 2^f by a degree-3 polynomial fitted for minimum relative error on
+//     [-1/2, 1/2] (iteratively reweighted least squares on Chebyshev nodes;
+//     max relative error 7.5e-5, far below the bf16 rounding of P);
+//   * 2^n by adding n to the exponent field (t's low bits shifted by 23).
+// x is clamped to >= -125 so results stay normal (callers only use this where
+// no entry is masked to -inf) and must be <= 127.
+constexpr float kExp2C0 = 0.999928057f, kExp2C1 = 0.693260968f, kExp2C2 = 0.242611140f, kExp2C3 = 0.0551716685f;
+__device__ __forceinline__ void exp2_fma2(float x0, float x1, float& y0, float& y1) {
+    x0 = fmaxf(x0, -125.0f);
+    x1 = fmaxf(x1, -125.0f);
+    float t0, t1, n0, n1, f0, f1, p0, p1;
+    fadd2(t0, t1, x0, x1, 12582912.0f, 12582912.0f);
+    fadd2(n0, n1, t0, t1, -12582912.0f, -12582912.0f);
+    fadd2(f0, f1, x0, x1, -n0, -n1);
+    ffma2(p0, p1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
+    ffma2(p0, p1, p0, p1, f0, f1, kExp2C1, kExp2C1);
+    ffma2(p0, p1, p0, p1, f0, f1, kExp2C0, kExp2C0);
+    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
+// Whether exponent pair e (of every 16) uses exp2_fma2 when N of 16 pairs
+// go to the FMA pipe (spread evenly); the rest use the special-function unit.
+template <int N>
+__host__ __device__ constexpr bool poly_pair(int e) {
+    return (e * N) % 16 < N;
+}
+
 // max of three fp32 values in one instruction (sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
