@@ -225,6 +225,10 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         prefetch_tensormap(&m->dout);
     }
     uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, do_cnt = 0;
+    // Broadcast Q: the (head, query tile) each Q stage holds, so a tile that
+    // is already resident is not loaded again (the statistics still are).
+    // Key = head << 16 | tile (tiles < 2^16 since Lq <= 2^23); -1 = empty.
+    int stage_key0 = -1, stage_key1 = -1;
     for (int idx = ib; idx < ie; ++idx) {
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int kv_row = it.kv_start + 128 * it.n;
@@ -272,12 +276,21 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             *reinterpret_cast<float4*>(lse2 + lane * 4) = make_float4(l2[0], l2[1], l2[2], l2[3]);
             *reinterpret_cast<float4*>(delta + lane * 4) = make_float4(dl[0], dl[1], dl[2], dl[3]);
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&bars.q_full[st], L::kTileBytes);
+            const int key = (it.h << 16) | i;
+            if (p.broadcast_q && (st == 0 ? stage_key0 : stage_key1) == key) {
+                if (lane == 0) mbar_arrive(&bars.q_full[st]);  // Q_i already resident: statistics only
+            } else {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars.q_full[st], L::kTileBytes);
 #pragma unroll
-                for (int s = 0; s < L::kSlabs; ++s)
-                    tma_load_2d(smem + L::kQ + st * L::kTileBytes + s * L::kSlabBytes, &m->q, &bars.q_full[st],
-                                it.h * D + 64 * s, it.q_row0 + 128 * i);
+                    for (int s = 0; s < L::kSlabs; ++s)
+                        tma_load_2d(smem + L::kQ + st * L::kTileBytes + s * L::kSlabBytes, &m->q, &bars.q_full[st],
+                                    it.h * D + 64 * s, it.q_row0 + 128 * i);
+                }
+                if (st == 0)
+                    stage_key0 = key;
+                else
+                    stage_key1 = key;
             }
             ++q_cnt;
             if (lane == 0) JFA_TRACE_EVENT(4, 8, i, 0);

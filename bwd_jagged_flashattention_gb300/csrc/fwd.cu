@@ -118,6 +118,32 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
     return it;
 }
 
+// Broadcast Q: an item reuses the Q tiles already in shared memory when it
+// reads the same ones (same head, first tile and tile count) as the last item
+// that loaded them.  The TMA and MMA threads take the same decision from the
+// same item sequence; Q is released (q_empty) only after the last item of a
+// run, so loads and releases stay one-to-one.
+struct QKey {
+    int h = -1, m0 = -1, nq = -1;
+    __device__ __forceinline__ bool same(const FwdItem& it) const { return it.h == h && it.m0 == m0 && it.nq == nq; }
+    __device__ __forceinline__ void set(const FwdItem& it) {
+        h = it.h;
+        m0 = it.m0;
+        nq = it.nq;
+    }
+};
+
+// Whether the next item that uses Q after item i reads the same Q tiles.
+__device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const FwdItem& it, int i, int ie) {
+    if (!p.broadcast_q) return false;
+    for (int k = i + 1; k < ie; ++k) {
+        const FwdItem nx = decode_fwd(p.items[k], p);
+        if (nx.nb == 0) continue;
+        return nx.h == it.h && nx.m0 == it.m0 && nx.nq == it.nq;
+    }
+    return false;
+}
+
 // Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
@@ -194,20 +220,24 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     prefetch_tensormap(mk);
     prefetch_tensormap(mv);
     uint32_t ring = 0, q_loads = 0;
+    QKey qk;
     PrefetchCursor pf{ib - 1, 0, 0, 0, 0};
     for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D>(pf, p, ie, mk, mv);
     for (int i = ib; i < ie; ++i) {
         const FwdItem it = decode_fwd(p.items[i], p);
         JFA_TRACE_EVENT(1, 8, i, it.nb);
         if (it.nb == 0) continue;
-        if (!mbar_wait(&bars.q_empty, (q_loads & 1) ^ 1, ab)) goto done;
-        mbar_arrive_expect_tx(&bars.q_full, it.nq * L::kTileBytes);
-        for (int t = 0; t < it.nq; ++t)
+        if (!(p.broadcast_q && qk.same(it))) {  // else: the resident Q tiles serve this item too
+            if (!mbar_wait(&bars.q_empty, (q_loads & 1) ^ 1, ab)) goto done;
+            mbar_arrive_expect_tx(&bars.q_full, it.nq * L::kTileBytes);
+            for (int t = 0; t < it.nq; ++t)
 #pragma unroll
-            for (int s = 0; s < L::kSlabs; ++s)
-                tma_load_2d(smem + L::kQOff + t * L::kTileBytes + s * L::kSlabBytes, mq, &bars.q_full,
-                            it.h * D + 64 * s, it.q_row0 + 128 * (it.m0 + t));
-        ++q_loads;
+                for (int s = 0; s < L::kSlabs; ++s)
+                    tma_load_2d(smem + L::kQOff + t * L::kTileBytes + s * L::kSlabBytes, mq, &bars.q_full,
+                                it.h * D + 64 * s, it.q_row0 + 128 * (it.m0 + t));
+            ++q_loads;
+            qk.set(it);
+        }
         JFA_TRACE_EVENT(2, 8, i, 0);
         for (int j = 0; j < it.nb; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
@@ -247,12 +277,17 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
     constexpr uint64_t kTileUnits = L::kTileBytes / 16;  // descriptor step between tiles
     uint32_t ring = 0, q_ph = 0;
     uint32_t p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
+    QKey qk;
     for (int i = ib; i < ie; ++i) {
         const FwdItem it = decode_fwd(p.items[i], p);
         JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
-        if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
-        q_ph ^= 1;
+        if (!(p.broadcast_q && qk.same(it))) {
+            if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
+            q_ph ^= 1;
+            qk.set(it);
+        }
+        const bool release_q = !next_item_reuses_q(p, it, i, ie);  // this item is the run's last Q user
         JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
         if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
@@ -266,7 +301,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 mma_commit(&bars.s_full[t]);
             }
         mma_commit(&bars.kv_empty[kslot]);
-        if (it.nb == 1) mma_commit(&bars.q_empty);
+        if (it.nb == 1 && release_q) mma_commit(&bars.q_empty);
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
             if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
@@ -304,7 +339,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             mma_commit(&bars.kv_empty[vslot]);
             if (has_next) {
                 mma_commit(&bars.kv_empty[kslot]);
-                if (j + 2 == it.nb) mma_commit(&bars.q_empty);
+                if (j + 2 == it.nb && release_q) mma_commit(&bars.q_empty);
             }
         }
     }

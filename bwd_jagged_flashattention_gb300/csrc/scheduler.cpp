@@ -10,6 +10,8 @@ namespace {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 }  // namespace
 
+bool head_partition(int broadcast_q, int H, int P) { return broadcast_q && H > 1 && H <= 255 && P % H == 0; }
+
 int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q) {
     if (B <= 0 || H <= 0) return 0;
     // backward: sum_b ceil(L_b/128) <= N/128 + B; forward pairs of q tiles
@@ -37,6 +39,45 @@ int64_t item_cost(const WorkItem& w, int Lq, int broadcast_q, int causal, int is
     const int64_t visited = causal ? (nq - tile) : nq;
     return visited + 1;
 }
+
+namespace {
+
+// CTA of the item at position pos of head h's cost-sorted items, dealt
+// zigzag over that head's G CTAs {h, h + H, h + 2H, ...}: the H CTAs that
+// work on the same sequences at the same time have neighbouring indices.
+inline int32_t zigzag_head_cta(int64_t pos, int h, int G, int H) {
+    const int64_t r = pos / G, lane = pos % G;
+    return static_cast<int32_t>(((r & 1) ? (G - 1 - lane) : lane) * H + h);
+}
+
+// Key of the Q tiles an item reads in broadcast mode: the head and (forward)
+// the first query tile.  Consecutive items of one CTA with equal keys share
+// the resident Q tiles, so the kernels load them once per run of equal keys.
+inline uint32_t q_key(const WorkItem& w, int is_bwd) {
+    const uint32_t h = w.packed & 0xFFu;
+    const uint32_t tile = (w.packed >> 8) & 0x7FFFFFu;
+    return is_bwd ? h : (h << 23) | tile;
+}
+
+// Stable in-place grouping of each CTA's items by q_key (insertion sort: the
+// CTA's item count is small, and no allocation is needed).  The deal -- which
+// CTA owns which item, and so every CTA's total cost -- is unchanged.
+void group_by_q(WorkItem* items, const int32_t* cta_start, int P, int is_bwd) {
+    for (int p = 0; p < P; ++p) {
+        for (int64_t i = cta_start[p] + 1; i < cta_start[p + 1]; ++i) {
+            const WorkItem w = items[i];
+            const uint32_t k = q_key(w, is_bwd);
+            int64_t j = i;
+            while (j > cta_start[p] && q_key(items[j - 1], is_bwd) > k) {
+                items[j] = items[j - 1];
+                --j;
+            }
+            items[j] = w;
+        }
+    }
+}
+
+}  // namespace
 
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
                        int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items) {
@@ -80,17 +121,29 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
 
     // 3. Deal.  Zigzag: sorted position i, round r = i / P, lane p = i % P;
     //    CTA p on even rounds, CTA P-1-p on odd rounds.  Naive: round-robin.
+    //    Broadcast Q with H | P: the same zigzag within each head's own group
+    //    of P/H CTAs (head_partition()).
     std::vector<int32_t> owner(static_cast<size_t>(n));
     std::fill(cta_start, cta_start + P + 1, 0);
+    const bool by_head = policy == kSchedLptZigzag && head_partition(broadcast_q, H, P);
+    std::vector<int64_t> head_pos(by_head ? static_cast<size_t>(H) : 0, 0);
     for (int64_t i = 0; i < n; ++i) {
-        const int64_t r = i / P, p = i % P;
-        const int32_t cta = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
+        int32_t cta;
+        if (by_head) {
+            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
+            cta = zigzag_head_cta(head_pos[h]++, h, P / H, H);
+        } else {
+            const int64_t r = i / P, p = i % P;
+            cta = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
+        }
         owner[i] = cta;
         ++cta_start[cta + 1];
     }
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
     std::vector<int32_t> fill(cta_start, cta_start + P);
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
+    // 4. Broadcast Q: group each CTA's items by the Q tiles they read.
+    if (broadcast_q && policy == kSchedLptZigzag) group_by_q(items, cta_start, P, is_bwd);
     return n;
 }
 
@@ -122,16 +175,25 @@ int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int
         const int64_t cost = std::min<int64_t>(item_cost(gen[i], Lq, broadcast_q, causal, is_bwd), kCostBuckets - 1);
         order[buckets[kCostBuckets - 1 - cost]++] = i;
     }
-    // Zigzag deal over P CTAs, then CSR placement in deal order.
+    // Zigzag deal over P CTAs (per head group when head_partition()), then
+    // CSR placement in deal order.
     for (int p = 0; p <= P; ++p) cta_start[p] = 0;
+    const bool by_head = head_partition(broadcast_q, H, P);
+    int64_t head_pos[256] = {0};
     for (int64_t i = 0; i < n; ++i) {
-        const int64_t r = i / P, p = i % P;
-        owner[i] = static_cast<int32_t>((r & 1) ? (P - 1 - p) : p);
+        if (by_head) {
+            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
+            owner[i] = zigzag_head_cta(head_pos[h]++, h, P / H, H);
+        } else {
+            const int64_t r = i / P, p = i % P;
+            owner[i] = static_cast<int32_t>((r & 1) ? (P - 1 - p) : p);
+        }
         ++cta_start[owner[i] + 1];
     }
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
     for (int p = 0; p < P; ++p) fill[p] = cta_start[p];
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
+    if (broadcast_q) group_by_q(items, cta_start, P, is_bwd);
     return n;
 }
 

@@ -8,6 +8,17 @@
 // Code, section "Optimizations layered on top", the paragraph after the
 // list; "Scheduling jagged tiles across SMs" in the same list).  The backward
 // uses the same sort and deal over its own items.
+//
+// Broadcast Q (one dense Q shared by every sequence): when the head count H
+// divides the CTA count P, each head gets its own group of P/H CTAs (CTAs
+// h, h+H, h+2H, ...) and the sort-and-zigzag deal runs within each group.  Every head has the same item
+// costs, so the groups' loads match and CTA g of every group works on the
+// same sequences at the same time (their K/V/dO rows, which interleave the
+// heads in memory, are read together), while each CTA only ever reads one
+// head's Q tiles.  Each CTA's items are then grouped (stably) by the Q tiles
+// they read -- head, and for the forward the first query tile -- so that runs
+// of consecutive items share the resident Q tiles.  The order of a CTA's own
+// items does not change its total work, only how often it reloads Q.
 #pragma once
 #include <cstdint>
 
@@ -36,6 +47,9 @@ enum SchedPolicy {
     kSchedLptZigzag = 0,  // cost-descending stable sort, then zigzag deal
     kSchedNaive = 1,      // generation order, round-robin deal (ablation)
 };
+
+// Whether broadcast-Q items are dealt per head group (H divides P).
+bool head_partition(int broadcast_q, int H, int P);
 
 // Upper bound on the number of items either pass produces.
 int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q);

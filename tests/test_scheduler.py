@@ -117,3 +117,48 @@ def test_causal_costs_and_pairs(jfa):
     assert torch.all(two == 1)
     costs = [_cost(1000, int(tile[i]), 1, 0, False, True, False) for i in range(len(tile))]
     assert costs == sorted(costs, reverse=True) or len(set(starts.tolist())) > 1
+
+
+@pytest.mark.parametrize("name,is_bwd", [("ads_fwd", 0), ("ads_bwd", 1), ("extreme", 0), ("extreme", 1)])
+def test_broadcast_deal_per_head_group(jfa, name, is_bwd):
+    """Broadcast Q with H dividing P: head h's items go to CTAs h, h+H, ...
+    (G = P/H of them), dealt by the same cost sort and zigzag within the group; each
+    CTA reads one head's Q tiles, in runs grouped by query tile, keeping the
+    deal order (cost descending) inside a run."""
+    w = jfa_inputs.WORKLOADS[name]
+    g = torch.Generator().manual_seed(7)
+    off = jfa_inputs.offsets_from_lengths(jfa_inputs.draw_lengths(w.lengths, w.B, g))
+    P = 152
+    assert P % w.H == 0
+    G = P // w.H
+    items, starts = jfa.host_schedule(off, w.Lq, w.H, True, False, bool(is_bwd), P)
+    b, start, length, h, tile, two = _decode(items)
+    cost = [_cost(int(length[i]), int(tile[i]), int(two[i]), w.Lq, True, False, bool(is_bwd)) for i in range(len(b))]
+    for p in range(P):
+        s, e = int(starts[p]), int(starts[p + 1])
+        assert set(h[s:e].tolist()) <= {p % w.H}
+        # runs of equal Q key: the forward's first query tile (the backward's
+        # tile field is a key/value tile, and its Q key is the head alone)
+        k = [0] * (e - s) if is_bwd else tile[s:e].tolist()
+        assert k == sorted(k)
+        for i in range(s + 1, e):
+            if k[i - s] == k[i - 1 - s]:
+                assert cost[i] <= cost[i - 1]
+    # per-CTA loads equal the deal restated here: per head, stable cost sort
+    # of the (b, tile) generation order, zigzag over the head's G CTAs
+    loads = [0] * P
+    for hh in range(w.H):
+        gen = []
+        for bb in range(w.B):
+            Lk = int(off[bb + 1] - off[bb])
+            nkv = (Lk + 127) // 128
+            nq = (w.Lq + 127) // 128
+            if is_bwd:
+                gen += [_cost(Lk, n, 0, w.Lq, True, False, True) for n in range(nkv)]
+            else:
+                gen += [_cost(Lk, m, 1 if m + 1 < nq else 0, w.Lq, True, False, False) for m in range(0, nq, 2)]
+        order = sorted(range(len(gen)), key=lambda i: -gen[i])
+        for pos, o in enumerate(order):
+            r, lane = divmod(pos, G)
+            loads[((G - 1 - lane) if (r & 1) else lane) * w.H + hh] += gen[o]
+    assert loads == [sum(cost[int(starts[p]):int(starts[p + 1])]) for p in range(P)]
