@@ -26,7 +26,7 @@
 // kernel outruns FlashAttention-4 on jagged Blackwell attention, second
 // paragraph).  dK/dV stay in TMEM for the whole item and are written once.
 //
-// Roles (320 threads):
+// Roles (384 threads):
 //   warps 0-3  compute: P^T and dS^T (thread r = key row r = TMEM lane r)
 //   warps 4-7  dQ readout + reduce-add; dK/dV epilogue (staged, coalesced)
 //   warp  8    loads: K, V per item; Q_i (+ LSE_i, Delta_i) and dO_i per tile
@@ -47,8 +47,8 @@ namespace {
 #define JFA_BWD_PREFETCH 0
 #endif
 // dK/dV epilogue: 1 = staged through the dS buffer (free at the end of an
-// item) with coalesced copies, 0 = each thread stores its own row (measured
-// faster on the ads workload: it never holds up the compute warps' dS).
+// item) with coalesced copies, 0 = each thread stores its own row (ads step
+// with the last dQ first: 478 vs 483 us).
 // Exponent pairs (of every 16) computed on the FMA pipe in unmasked tiles.
 // Measured: any share > 0 is slower on GB300 (the passes are latency-bound,
 // not special-function-bound), so the default keeps every exponential on the SFU.
@@ -56,12 +56,12 @@ namespace {
 #define JFA_BWD_POLY_PAIRS 0
 #endif
 // Issue the last tile's dQ before its dK, releasing K one product earlier
-// (measured slower on the ads workload: 622 vs 582 us).
+// (ads step, per-head CTA groups: 483 vs 492 us).
 #ifndef JFA_BWD_DQ_FIRST
-#define JFA_BWD_DQ_FIRST 0
+#define JFA_BWD_DQ_FIRST 1
 #endif
 #ifndef JFA_BWD_EPI_STAGED
-#define JFA_BWD_EPI_STAGED 0
+#define JFA_BWD_EPI_STAGED 1
 #endif
 
 // 384 threads = three warpgroups (compute, dQ, and load + MMA + two idle
