@@ -40,6 +40,18 @@ namespace {
 // Exponent pairs (of every 16) computed on the FMA pipe in unmasked blocks.
 // Measured: any share > 0 is slower on GB300 (the passes are latency-bound,
 // not special-function-bound), so the default keeps every exponential on the SFU.
+// Ragged last KV block: cover only the keys up to the sequence end instead
+// of all 128 -- bit 0: in the products (rounded up to 16 keys), bit 1: in the
+// softmax (whole 32-column chunks; needs bit 0).  Measured on the ads step:
+// slower either way (products only 166.6 us, both 174.9 us, off 158.6 us).
+#ifndef JFA_FWD_TRIM_TAIL
+#define JFA_FWD_TRIM_TAIL 0
+#endif
+// Row sums of P: 1 = four paired partial sums (add.f32x2), 0 = eight scalar
+// (ads step: 158.7 vs 164.4 us).
+#ifndef JFA_FWD_PAIRED_SUMS
+#define JFA_FWD_PAIRED_SUMS 1
+#endif
 #ifndef JFA_FWD_POLY_PAIRS
 #define JFA_FWD_POLY_PAIRS 0
 #endif
@@ -170,13 +182,36 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
     }
 }
 
+// The same product for a ragged last KV block: only the first n keys
+// (n a multiple of 16 covering the sequence's remaining keys); the S columns
+// past n keep stale values, which the softmax masks to -inf.
+template <int D>
+__device__ __forceinline__ void issue_qk_n(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, uint32_t n) {
+    const uint32_t idesc = idesc_bf16_f32(128, 0, 0, 0) | ((n >> 3) << 17);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        constexpr uint64_t unit = 16;
+        const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) / unit;
+        mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0);
+    }
+}
+
 // O(tmem) (+)= P(tmem, bf16) V: V is MN-major (D contiguous); one K=16 step
 // covers 16 key rows = 2048 bytes; the 64-column slabs are 16 KB apart.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc) {
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc,
+                                         int ksteps = 8) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) mma_ts(d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
+    for (int kk = 0; kk < 8; ++kk)
+        if (kk < ksteps) mma_ts(d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
+}
+
+// Keys of KV block j the products cover: 128, or for a ragged last block the
+// remaining keys rounded up to 16 (the MMA's N granularity).
+__device__ __forceinline__ uint32_t block_keys(int Lk, int j) {
+    const int nv = Lk - 128 * j;
+    return (!(JFA_FWD_TRIM_TAIL & 1) || nv >= 128) ? 128u : static_cast<uint32_t>((nv + 15) & ~15);
 }
 
 // L2 prefetch runs this many KV blocks ahead of the smem ring, so the ring's
@@ -297,7 +332,8 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
 #pragma unroll
         for (int t = 0; t < 2; ++t)
             if (it.nblk[t] > 0) {
-                issue_qk<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
+                              block_keys(it.Lk, 0));
                 mma_commit(&bars.s_full[t]);
             }
         mma_commit(&bars.kv_empty[kslot]);
@@ -327,11 +363,13 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 p_ph[t] ^= 1;
                 JFA_TRACE_EVENT(15, 9, t, j);
                 tc_fence_after();
-                issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0,
+                            static_cast<int>(block_keys(it.Lk, j) / 16));
                 JFA_TRACE_EVENT(16, 9, t, j);
                 if (j == it.nblk[t] - 1) mma_commit(&bars.o_full[t]);
                 if (j + 1 < it.nblk[t]) {
-                    issue_qk<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                    issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
+                                  block_keys(it.Lk, j + 1));
                     JFA_TRACE_EVENT(18, 9, t, j + 1);
                     mma_commit(&bars.s_full[t]);
                 }
@@ -353,12 +391,19 @@ done:
 // Softmax / correction / epilogue (one warpgroup per query tile; thread r
 // owns query row r of the tile = TMEM lane r).
 // ---------------------------------------------------------------------------
-template <int D, bool kMask>
+// kChunks: 32-column chunks of S that hold visible keys.  A ragged last
+// block (JFA_FWD_TRIM_TAIL) uses only its first kChunks; the products skip
+// the keys past them too, so those P columns are never read.
+template <int D, bool kMask, int kChunks = 4>
 __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem& it, int j, int qpos,
                                               uint32_t s_addr, uint32_t o_addr, float& m_use, float& l) {
     uint32_t sr[4][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+    for (int c = 0; c < kChunks; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+#pragma unroll
+    for (int c = kChunks; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sr[c][i] = __float_as_uint(-INFINITY);
     tmem_ld_wait();
     if (kMask) {
         // Keys kbase .. kbase + nvis - 1 are visible to this row: the
@@ -402,7 +447,7 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
 #pragma unroll
     for (int a = 0; a < 8; ++a) rss[a] = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -415,7 +460,18 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
                 p0 = ex2_approx(x0);
                 p1 = ex2_approx(x1);
             }
-            rss[(c * 2 + e / 8)] += p0 + p1;
+            if (JFA_FWD_PAIRED_SUMS) {  // 4 paired (add.f32x2) partial sums
+                const int a = (c * 2 + e / 8) & 6;
+                float s0 = a == 0 ? rss[0] : a == 2 ? rss[2] : a == 4 ? rss[4] : rss[6];
+                float s1 = a == 0 ? rss[1] : a == 2 ? rss[3] : a == 4 ? rss[5] : rss[7];
+                fadd2(s0, s1, s0, s1, p0, p1);
+                if (a == 0) { rss[0] = s0; rss[1] = s1; }
+                else if (a == 2) { rss[2] = s0; rss[3] = s1; }
+                else if (a == 4) { rss[4] = s0; rss[5] = s1; }
+                else { rss[6] = s0; rss[7] = s1; }
+            } else {
+                rss[(c * 2 + e / 8)] += p0 + p1;
+            }
             pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
@@ -490,7 +546,15 @@ __device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bar
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
-            softmax_block<D, true>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            const int nch = (JFA_FWD_TRIM_TAIL & 2) ? min(4, (it.Lk - 128 * j + 31) / 32) : 4;
+            if (nch == 4)
+                softmax_block<D, true, 4>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            else if (nch == 3)
+                softmax_block<D, true, 3>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            else if (nch == 2)
+                softmax_block<D, true, 2>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            else
+                softmax_block<D, true, 1>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
             tc_fence_before();
             mbar_arrive(&bars.p_full[t]);
