@@ -39,9 +39,26 @@ sys.path.insert(0, ROOT)
 import jfa_inputs  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-WORKLOAD = "ads_bwd"
+WORKLOAD = "ads_bwd"  # default: the configuration the headline metric is quoted on
 WORKLOAD_DESC = ("jagged broadcast-Q attention fwd+bwd, ads shape: B=512, KV lengths lognormal(median 256, "
                  "sigma 1) clipped to [8,4096], Q [256,4,128] shared, packed K/V [N,4,128], bf16, non-causal")
+
+
+def workload_desc(name):
+    """One-line description of a workload (the ads step keeps its fixed wording)."""
+    if name == WORKLOAD:
+        return WORKLOAD_DESC
+    w = jfa_inputs.WORKLOADS[name]
+    mode = (f"broadcast Q [{w.Lq},{w.H},{w.D}] shared" if w.broadcast_q else f"per-sequence Q [N,{w.H},{w.D}]")
+    return (f"jagged attention {'fwd+bwd' if w.backward else 'fwd only'}, {name}: B={w.B}, KV lengths {w.lengths}, "
+            f"{mode}, packed K/V [N,{w.H},{w.D}], bf16, {'causal' if w.causal else 'non-causal'}")
+
+
+def metric_name(name, backward):
+    what = "fwd+bwd" if backward else "fwd"
+    if name == WORKLOAD:
+        return f"{what} TFLOPS (bf16, 1 GB300) on jagged broadcast-Q"
+    return f"{what} TFLOPS (bf16, 1 GB300) on {name}"
 
 
 # ----------------------------------------------------------------------------
@@ -255,7 +272,8 @@ def first_sequences(x, n):
     off = x["offsets"][: n + 1].clone()
     N = int(off[-1])
     y = dict(x, B=n, offsets=off, N=N, k=x["k"][:N].contiguous(), v=x["v"][:N].contiguous())
-    y["do"] = (x["do"][:n] if x["broadcast_q"] else x["do"][:N]).contiguous()
+    if "do" in x:
+        y["do"] = (x["do"][:n] if x["broadcast_q"] else x["do"][:N]).contiguous()
     if not x["broadcast_q"]:
         y["q"] = x["q"][:N].contiguous()
     return y
@@ -265,7 +283,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    x = jfa_inputs.make(WORKLOAD)
+    x = jfa_inputs.make(args.workload)
     budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
     n = size_oracle_sample(x, budget)
     for _ in range(args.warmup):
@@ -276,13 +294,13 @@ def run_reference(args, world, rank):
         tot_f += f
         tot_t += t
     value = tot_f / tot_t / 1e12
-    line = {"impl": "reference", "metric": "fwd+bwd TFLOPS (bf16, 1 GB300) on jagged broadcast-Q",
+    line = {"impl": "reference", "metric": metric_name(args.workload, True),
             "value": value, "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "sample": f"first {n} of 512 sequences per step"},
+            "config": {"workload": workload_desc(args.workload), "sample": f"first {n} of {x['B']} sequences per step"},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
-                             "sample": f"fp64 oracle fwd+bwd on the first {n} of 512 sequences, per step"},
+                             "sample": f"fp64 oracle fwd+bwd on the first {n} of {x['B']} sequences, per step"},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -301,6 +319,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first BATCH sequences (small profiling case; not a bench line)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=list(jfa_inputs.WORKLOAD_ORDER),
+                    help="synthetic workload (default: the ads fwd+bwd step the headline metric is quoted on)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -311,27 +331,33 @@ def main():
     jfa.lib()  # raises if the CUDA library is missing: no fallback
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = jfa_inputs.make(WORKLOAD)
+    x = jfa_inputs.make(args.workload)
+    backward = "do" in x
     if args.batch:
         x = first_sequences(x, args.batch)
     acc = accounting(x)
+    if not backward:
+        acc.update(flops_bwd=0.0, bytes_bwd=0, flops_pre=0.0, bytes_pre=0)
     B, Lq, H, D, N = x["B"], x["Lq"], x["H"], x["D"], x["N"]
-    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    bq, causal = x["broadcast_q"], x["causal"]
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    do = x["do"].to(dev) if backward else None
     off_h = x["offsets"]
     off_d = off_h.to(dev)
-    o = torch.empty((B, Lq, H, D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=dev)
-    dq = torch.empty((Lq, H, D), dtype=torch.float32, device=dev)
+    o = torch.empty((B, Lq, H, D) if bq else (N, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Lq) if bq else (H, N), dtype=torch.float32, device=dev)
+    dq = torch.empty((Lq, H, D) if bq else (N, H, D), dtype=torch.float32, device=dev)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    ws = jfa.new_workspace(B, N, Lq, H, D, True, False, dev)
+    ws = jfa.new_workspace(B, N, Lq if bq else 0, H, D, bq, causal, dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        jfa.fwd(q, k, v, off_d, broadcast_q=True, causal=False, scale=x["scale"], offsets_host=off_h,
+        jfa.fwd(q, k, v, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h,
                 workspace=ws, out=o, lse=lse)
-        jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=True, causal=False, scale=x["scale"],
-                offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+        if backward:
+            jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=bq, causal=causal, scale=x["scale"],
+                    offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
 
     for _ in range(args.warmup):
         step()
@@ -398,25 +424,19 @@ def main():
                 algorithmic_per_launch=dom["algorithmic_bytes"] if roof["bound"] == "hbm" else dom["algorithmic_flops"])
 
     # End to end: pinned host inputs -> device, both passes, outputs -> host, per step.
-    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "do"))
-    ho, hl = torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hdq = torch.empty(dq.shape, dtype=dq.dtype).pin_memory()
-    hdk, hdv = torch.empty(dk.shape, dtype=dk.dtype).pin_memory(), torch.empty(dv.shape, dtype=dv.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, off_h))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    ins = [(q, x["q"]), (k, x["k"]), (v, x["v"])] + ([(do, x["do"])] if backward else []) + [(off_d, off_h)]
+    ins = [(dst, src.pin_memory()) for dst, src in ins]
+    outs = [o, lse] + ([dq, dk, dv] if backward else [])
+    outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
+    d2h = sum(h.numel() * h.element_size() for _, h in outs)
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        off_d.copy_(off_h, non_blocking=True)
+        for dst, h in ins:
+            dst.copy_(h, non_blocking=True)
         step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dv, non_blocking=True)
+        for src, h in outs:
+            h.copy_(src, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -436,18 +456,22 @@ def main():
         return 0
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(x)
+        cpu = cpu_baseline(x) if backward else None
     line = {
-        "metric": "fwd+bwd TFLOPS (bf16, 1 GB300) on jagged broadcast-Q",
+        "metric": metric_name(args.workload, backward),
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC if not args.batch else f"first {B} sequences of: " + WORKLOAD_DESC,
+        "config": {"workload": workload_desc(args.workload) if not args.batch
+                   else f"first {B} sequences of: " + workload_desc(args.workload),
                    "B": B, "Lq": Lq, "H": H, "D": D, "N": N, "pairs": acc["pairs"],
-                   "l2": "no flush: K+V inputs (~390 MB) exceed the 129 MB L2",
+                   "l2": (f"no flush: K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) exceed the 129 MB L2"
+                          if 4 * N * H * D > 129e6 else
+                          f"no flush; K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) fit in the 129 MB L2"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "fwd_tflops": kernels["fwd"]["tflops"], "bwd_tflops": acc["flops_bwd"] / (
-            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]) * 1e-3) / 1e12,
+            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]) * 1e-3) / 1e12
+        if backward else None,
         "tensor_peak_frac": {"fwd": kernels["fwd"]["tensor_frac"], "bwd_kernel": kernels["bwd"]["tensor_frac"],
                              "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
         "roofline": roof,
