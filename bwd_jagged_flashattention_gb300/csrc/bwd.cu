@@ -60,6 +60,12 @@ namespace {
 #ifndef JFA_BWD_DQ_FIRST
 #define JFA_BWD_DQ_FIRST 1
 #endif
+// The compute warps keep P (packed bf16) in registers from the P pass to the
+// dS pass, so the next query tile's S^T may overwrite the S^T/P^T columns as
+// soon as dV has read P^T: it is issued right after dV instead of after dS.
+#ifndef JFA_BWD_EARLY_S
+#define JFA_BWD_EARLY_S 1
+#endif
 #ifndef JFA_BWD_EPI_STAGED
 #define JFA_BWD_EPI_STAGED 1
 #endif
@@ -369,9 +375,16 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
             tc_fence_after();
             issue_dv<D>(tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
             mma_commit(&bars.do_empty);
+            if (JFA_BWD_EARLY_S && i + 1 < it.i1) {  // next tile's S^T right behind dV (which reads P^T first)
+                const int st2 = (q_cnt + 1) % 2;
+                if (!mbar_wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1, ab)) goto done;
+                tc_fence_after();
+                issue_kmajor<D>(tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
+                mma_commit(&bars.s_full);
+            }
             if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
             JFA_TRACE_EVENT(20, 9, i, 0);
-            if (i + 1 < it.i1) {  // next tile's S^T: T_S is free (P^T read by dV and by the dS pass)
+            if (!JFA_BWD_EARLY_S && i + 1 < it.i1) {  // next tile's S^T: T_S is free (P^T read by dV and by the dS pass)
                 const int st2 = (q_cnt + 1) % 2;
                 if (!mbar_wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1, ab)) goto done;
                 tc_fence_after();
@@ -415,7 +428,7 @@ done:
 // ---------------------------------------------------------------------------
 template <int D, bool kMask>
 __device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* lse2, uint32_t s_addr, int key,
-                                              int qbase, int q_rows, bool row_valid) {
+                                              int qbase, int q_rows, bool row_valid, uint32_t (&pkeep)[64]) {
     // All 128 scores of this key row in one batch of TMEM loads, one wait.
     uint32_t sr[4][32];
 #pragma unroll
@@ -456,10 +469,45 @@ __device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* l
                 if (q0 + 1 >= nvis || (p.causal && key > qbase + q0 + 1)) p1 = 0.0f;
             }
             pk[e] = pack_bf16x2(p0, p1);
+            pkeep[c * 16 + e] = pk[e];
         }
         tmem_st16(s_addr + c * 16, pk);
     }
     tmem_st_wait();
+}
+
+// dS^T from dP^T (TMEM, 32 columns at a time) and P kept in registers.
+template <int D>
+__device__ __forceinline__ void bwd_compute_ds_regs(const float* delta, uint32_t dp_addr, uint8_t* ds_tile, int row,
+                                                    const uint32_t (&pkeep)[64]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld32(dp_addr + c * 32, dp);
+        float dl[32];  // Delta of the 32 queries, read 4 at a time
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float4 f = reinterpret_cast<const float4*>(delta)[c * 8 + v];
+            dl[4 * v] = f.x;
+            dl[4 * v + 1] = f.y;
+            dl[4 * v + 2] = f.z;
+            dl[4 * v + 3] = f.w;
+        }
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float d0 = bf16lo_to_f32(pkeep[c * 16 + e]) * (__uint_as_float(dp[2 * e]) - dl[2 * e]);
+            const float d1 = bf16hi_to_f32(pkeep[c * 16 + e]) * (__uint_as_float(dp[2 * e + 1]) - dl[2 * e + 1]);
+            pk[e] = pack_bf16x2(d0, d1);
+        }
+        uint8_t* slab = ds_tile + (c / 2) * 16384 + row * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int chunk = ((c % 2) * 4 + v) ^ (row % 8);
+            *reinterpret_cast<uint4*>(slab + chunk * 16) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+    }
 }
 
 template <int D>
@@ -531,10 +579,11 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             if (row == 0) JFA_TRACE_EVENT(31, 0, i, 0);
             tc_fence_after();
             const bool unmasked = kv_full_tile && 128 * (i + 1) <= it.q_rows && !(p.causal && i == it.n);
+            uint32_t pkeep[64];
             if (unmasked)
-                bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
+                bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
             else
-                bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid);
+                bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
             if (row == 0) JFA_TRACE_EVENT(32, 0, i, 0);
             tc_fence_before();
             mbar_arrive(&bars.p_full);
@@ -546,7 +595,10 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             }
             if (row == 0) JFA_TRACE_EVENT(34, 0, i, 0);
             tc_fence_after();
-            bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
+            if (JFA_BWD_EARLY_S)
+                bwd_compute_ds_regs<D>(delta, dp_addr, ds_tile, row, pkeep);
+            else
+                bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
             fence_proxy_async_smem();
             if (row == 0) JFA_TRACE_EVENT(35, 0, i, 0);
             tc_fence_before();
