@@ -55,10 +55,11 @@ namespace {
 #ifndef JFA_BWD_POLY_PAIRS
 #define JFA_BWD_POLY_PAIRS 0
 #endif
-// Issue the last tile's dQ before its dK, releasing K one product earlier
-// (ads step, per-head CTA groups: 483 vs 492 us).
+// dQ before dK: 1 = on the last query tile of an item (releases K one
+// product earlier; ads step 483 vs 492 us), 2 = on every tile (the dQ
+// readout, and so the next dP^T, also comes sooner; 467.6 vs 470.4 us).
 #ifndef JFA_BWD_DQ_FIRST
-#define JFA_BWD_DQ_FIRST 1
+#define JFA_BWD_DQ_FIRST 2
 #endif
 // The compute warps keep P (packed bf16) in registers from the P pass to the
 // dS pass, so the next query tile's S^T may overwrite the S^T/P^T columns as
@@ -68,6 +69,13 @@ namespace {
 #endif
 #ifndef JFA_BWD_EPI_STAGED
 #define JFA_BWD_EPI_STAGED 1
+#endif
+// Who stores an item's dK / dV: 1 = the compute warpgroup (staged through its
+// own dS tile, while the next item's K loads), 0 = the dQ warpgroup after the
+// item's last dQ reduce (staged per JFA_BWD_EPI_STAGED).  Ads step: 453.9 vs
+// 467.4 us.
+#ifndef JFA_BWD_EPI_ON_COMPUTE
+#define JFA_BWD_EPI_ON_COMPUTE 1
 #endif
 
 // 384 threads = three warpgroups (compute, dQ, and load + MMA + two idle
@@ -153,6 +161,9 @@ __device__ __forceinline__ bool group_all(int id, bool pred) {
 }
 
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// Barrier over the compute warpgroup (warps 0-3; the dQ warpgroup uses id 1).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // Operand descriptors are built once per buffer; each MMA adds a
 // compile-time offset (16-byte units) so the issuing thread stays lean.
@@ -395,12 +406,13 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
                 if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
             }
             tc_fence_after();
-            if (JFA_BWD_DQ_FIRST && i == it.i1 - 1) {
-                // Last tile: dQ first, so K can be released (and the next item's K
-                // loaded) while dK runs.
+            if ((JFA_BWD_DQ_FIRST && i == it.i1 - 1) || JFA_BWD_DQ_FIRST == 2) {
+                // dQ first: on the last tile K can then be released (and the next
+                // item's K loaded) while dK runs; on every tile (mode 2) the dQ
+                // readout, and with it the next dP^T, comes one product sooner.
                 issue_dq<D>(tmem + L::kColDP, dDS_mn, dK_mn);
                 mma_commit(&bars.dq_full);
-                mma_commit(&bars.k_empty);
+                if (i == it.i1 - 1) mma_commit(&bars.k_empty);
                 issue_dk<D>(tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
                 mma_commit(&bars.q_empty[st]);
                 mma_commit(&bars.ds_empty);
@@ -590,7 +602,7 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
             if (row == 0) JFA_TRACE_EVENT(33, 0, i, 0);
             if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
-            if (JFA_BWD_EPI_STAGED && i == it.i0) {  // the previous item's dK/dV staging has left the buffer
+            if (!JFA_BWD_EPI_ON_COMPUTE && JFA_BWD_EPI_STAGED && i == it.i0) {  // the previous item's dK/dV staging has left the buffer
                 if (!mbar_wait_warp(&bars.ds_free, (item_cnt & 1) ^ 1, ab)) goto done;
             }
             if (row == 0) JFA_TRACE_EVENT(34, 0, i, 0);
@@ -605,6 +617,58 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             mbar_arrive(&bars.ds_full);
             ++q_cnt;
             ++tile_cnt;
+        }
+        if (JFA_BWD_EPI_ON_COMPUTE) {
+            // This item's dK / dV, while the next item's K tile loads: once
+            // every product of the item is done (dkv_full, which also means
+            // the last dK / dQ have read dS), 64-column halves go TMEM ->
+            // registers -> 128-byte-swizzled stage in the dS tile -> coalesced
+            // row copies (a warp store covers 4 whole lines; rows past the
+            // sequence end are skipped).  Each accumulator's columns are
+            // released after its last half is read.
+            if (!mbar_wait_warp(&bars.dkv_full, item_cnt & 1, ab)) goto done;
+            if (row == 0) JFA_TRACE_EVENT(36, 0, idx, 0);
+            tc_fence_after();
+            const int rows_valid = min(128, it.Lk - 128 * it.n);
+            const int64_t row0 = static_cast<int64_t>(it.kv_start) + 128 * it.n;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled)
+                const uint32_t col = which ? L::kColDK : L::kColDV;
+                const float sc = which ? p.scale : 1.0f;
+                uint16_t* out = which ? p.dk : p.dv;
+#pragma unroll
+                for (int half = 0; half < D / 64; ++half) {
+                    uint32_t v[2][32];
+                    tmem_ld32(tmem + lane_off + col + half * 64, v[0]);
+                    tmem_ld32(tmem + lane_off + col + half * 64 + 32, v[1]);
+                    tmem_ld_wait();
+                    if (half == D / 64 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(which ? &bars.dk_empty : &bars.dv_empty);
+                    }
+                    uint8_t* stage = ds_tile + half * 16384;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t* f = &v[ch / 4][(ch % 4) * 8];
+                        *reinterpret_cast<uint4*>(stage + row * 128 + ((ch ^ (row & 7)) * 16)) =
+                            make_uint4(pack_bf16x2(__uint_as_float(f[0]) * sc, __uint_as_float(f[1]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
+                                       pack_bf16x2(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
+                    }
+                    compute_sync();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int q = row + 128 * k;
+                        const int rr = q >> 3, ch = q & 7;
+                        if (rr < rows_valid)
+                            *reinterpret_cast<uint4*>(out + ((row0 + rr) * p.H + it.h) * D + half * 64 + ch * 8) =
+                                *reinterpret_cast<const uint4*>(stage + rr * 128 + ((ch ^ (rr & 7)) * 16));
+                    }
+                    compute_sync();
+                }
+            }
+            if (row == 0) JFA_TRACE_EVENT(37, 0, idx, 0);
         }
     }
 done:;
@@ -668,6 +732,7 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
             if (issuer) JFA_TRACE_EVENT(43, 4, i, 0);
             ++tile_cnt;
         }
+        if (JFA_BWD_EPI_ON_COMPUTE) continue;  // the compute warpgroup stores this item's dK / dV
         // dK / dV epilogue in 64-column halves: TMEM -> registers -> the dS
         // tile's smem (free once the item's last dK/dQ products are done;
         // 128-byte swizzle) -> coalesced row copies (each warp store covers
