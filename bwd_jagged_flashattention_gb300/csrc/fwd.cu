@@ -145,15 +145,18 @@ struct QKey {
     }
 };
 
-// Whether the next item that uses Q after item i reads the same Q tiles.
-__device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const FwdItem& it, int i, int ie) {
-    if (!p.broadcast_q) return false;
-    for (int k = i + 1; k < ie; ++k) {
-        const FwdItem nx = decode_fwd(p.items[k], p);
-        if (nx.nb == 0) continue;
-        return nx.h == it.h && nx.m0 == it.m0 && nx.nq == it.nq;
+// Whether the next item that uses Q after item i reads the same Q tiles
+// (`next` = item i + 1, already loaded; empty sequences in between are rare
+// and read on the spot).
+__device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const FwdItem& it, const WorkItem& next, int i,
+                                                   int ie) {
+    if (!p.broadcast_q || i + 1 >= ie) return false;
+    FwdItem nx = decode_fwd(next, p);
+    for (int k = i + 1; nx.nb == 0;) {
+        if (++k >= ie) return false;
+        nx = decode_fwd(p.items[k], p);
     }
-    return false;
+    return nx.h == it.h && nx.m0 == it.m0 && nx.nq == it.nq;
 }
 
 // Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
@@ -258,8 +261,11 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     QKey qk;
     PrefetchCursor pf{ib - 1, 0, 0, 0, 0};
     for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D>(pf, p, ie, mk, mv);
+    WorkItem wn = load_item(p.items, ib, ie);
     for (int i = ib; i < ie; ++i) {
-        const FwdItem it = decode_fwd(p.items[i], p);
+        const WorkItem wc = wn;
+        wn = load_item(p.items, i + 1, ie);
+        const FwdItem it = decode_fwd(wc, p);
         JFA_TRACE_EVENT(1, 8, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {  // else: the resident Q tiles serve this item too
@@ -313,8 +319,12 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
     uint32_t ring = 0, q_ph = 0;
     uint32_t p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
     QKey qk;
+    WorkItem wn = load_item(p.items, ib, ie), wn2 = load_item(p.items, ib + 1, ie);
     for (int i = ib; i < ie; ++i) {
-        const FwdItem it = decode_fwd(p.items[i], p);
+        const WorkItem wc = wn;
+        wn = wn2;  // item i + 1, loaded an iteration ago
+        wn2 = load_item(p.items, i + 2, ie);
+        const FwdItem it = decode_fwd(wc, p);
         JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {
@@ -322,7 +332,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             q_ph ^= 1;
             qk.set(it);
         }
-        const bool release_q = !next_item_reuses_q(p, it, i, ie);  // this item is the run's last Q user
+        const bool release_q = !next_item_reuses_q(p, it, wn, i, ie);  // this item is the run's last Q user
         JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
         if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
@@ -508,8 +518,11 @@ __device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bar
     const uint32_t s_addr = tmem + lane_off + t * 128;
     const uint32_t o_addr = tmem + lane_off + L::kOCol + t * D;
     uint32_t s_ph = 0, o_ph = 0;
+    WorkItem wn = load_item(p.items, ib, ie);
     for (int i = ib; i < ie; ++i) {
-        const FwdItem it = decode_fwd(p.items[i], p);
+        const WorkItem wc = wn;
+        wn = load_item(p.items, i + 1, ie);
+        const FwdItem it = decode_fwd(wc, p);
         if (t >= it.nq) continue;
         const int nblk = t == 0 ? it.nblk[0] : it.nblk[1];   // scalar copies: no
         const int nfull = t == 0 ? it.nfull[0] : it.nfull[1];  // dynamic array indexing

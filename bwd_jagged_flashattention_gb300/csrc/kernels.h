@@ -44,6 +44,17 @@ struct PreParams {
     int broadcast_q;
 };
 
+#ifdef __CUDACC__
+// Work item i of a CTA's list as one 16-byte load (an all-zero item past the
+// end).  The kernels read each item one iteration ahead, so the load's latency
+// hides behind the previous item's work instead of delaying the item's start.
+__device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i, int ie) {
+    if (i >= ie) return WorkItem{0, 0, 0, 0u};
+    const int4 v = __ldg(reinterpret_cast<const int4*>(items) + i);
+    return WorkItem{v.x, v.y, v.z, static_cast<uint32_t>(v.w)};
+}
+#endif
+
 // Tensor maps for one call.  Q/K/V/dO are viewed as 2D [rows, H*D] bf16
 // with 64x128 boxes (128-byte swizzle); dQ as 2D [rows, H*D] fp32.
 struct FwdMaps {
