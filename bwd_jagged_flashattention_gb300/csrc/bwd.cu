@@ -877,11 +877,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// Delta[row] = sum_d dO[row, d] * O[row, d] (fp32), one 16-byte chunk per
-// lane; D/8 consecutive lanes own one (row, head) pair.
+// Delta pre-pass shape: 16-byte chunks each lane reads from O and from dO per
+// (row, head) pair (ads step: 1 -> 59.3 us, 2 -> 49.4 us, 4 -> 51.3 us), and
+// the grid cap in blocks per SM (8 -> 70 us, 16 and 32 alike).
+#ifndef JFA_PRE_VEC
+#define JFA_PRE_VEC 2
+#endif
+#ifndef JFA_PRE_BLOCKS_PER_SM
+#define JFA_PRE_BLOCKS_PER_SM 16
+#endif
+
+// Delta[row] = sum_d dO[row, d] * O[row, d] (fp32), JFA_PRE_VEC 16-byte
+// chunks per lane; D / (8 * JFA_PRE_VEC) consecutive lanes own one (row, head)
+// pair.
 template <int D>
 __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
-    constexpr int kLanes = D / 8;
+    constexpr int kVec = JFA_PRE_VEC;
+    constexpr int kLanes = D / (8 * kVec);
     const int64_t total = p.rows;
     const int sub = threadIdx.x % kLanes;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x / kLanes);
@@ -892,13 +904,20 @@ __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
         float acc = 0.0f;
         const bool in = pair < total;
         if (in) {
-            const uint4 a = reinterpret_cast<const uint4*>(p.o + pair * D)[sub];
-            const uint4 b = reinterpret_cast<const uint4*>(p.dout + pair * D)[sub];
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            uint4 a[kVec], b[kVec];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                acc = fmaf(bf16lo_to_f32(aw[w]), bf16lo_to_f32(bw[w]), acc);
-                acc = fmaf(bf16hi_to_f32(aw[w]), bf16hi_to_f32(bw[w]), acc);
+            for (int u = 0; u < kVec; ++u) {
+                a[u] = reinterpret_cast<const uint4*>(p.o + pair * D)[sub * kVec + u];
+                b[u] = reinterpret_cast<const uint4*>(p.dout + pair * D)[sub * kVec + u];
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    acc = fmaf(bf16lo_to_f32(aw[w]), bf16lo_to_f32(bw[w]), acc);
+                    acc = fmaf(bf16hi_to_f32(aw[w]), bf16hi_to_f32(bw[w]), acc);
+                }
             }
         }
 #pragma unroll
@@ -957,10 +976,10 @@ cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStr
 
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;
-    const int lanes = p.D / 8;
+    const int lanes = p.D / (8 * JFA_PRE_VEC);
     const int pairs_per_block = 256 / lanes;
     int64_t blocks = (p.rows + pairs_per_block - 1) / pairs_per_block;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > 152 * JFA_PRE_BLOCKS_PER_SM) blocks = 152 * JFA_PRE_BLOCKS_PER_SM;
     if (p.D == 128)
         jfa_bwd_pre_kernel<128><<<static_cast<int>(blocks), 256, 0, s>>>(p);
     else
