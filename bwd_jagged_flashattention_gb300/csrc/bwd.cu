@@ -74,6 +74,12 @@ namespace {
 // own dS tile, while the next item's K loads), 0 = the dQ warpgroup after the
 // item's last dQ reduce (staged per JFA_BWD_EPI_STAGED).  Ads step: 453.9 vs
 // 467.4 us.
+// With the compute warpgroup's epilogue: whole 128-row tiles of dK/dV leave
+// through TMA stores issued by one thread (the warpgroup only stages them;
+// ads step 443.1 vs 453.5 us).
+#ifndef JFA_BWD_EPI_TMA
+#define JFA_BWD_EPI_TMA 1
+#endif
 #ifndef JFA_BWD_EPI_ON_COMPUTE
 #define JFA_BWD_EPI_ON_COMPUTE 1
 #endif
@@ -567,8 +573,8 @@ __device__ __forceinline__ void bwd_compute_ds(const float* delta, uint32_t s_ad
 }
 
 template <int D>
-__device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
-                                 const AbortState& ab) {
+__device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_t* smem, BwdBars& bars,
+                                 uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = BwdLayout<D>;
     const int row = threadIdx.x;  // 0..127
     const uint32_t lane_off = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
@@ -607,6 +613,10 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             }
             if (row == 0) JFA_TRACE_EVENT(34, 0, i, 0);
             tc_fence_after();
+            if (JFA_BWD_EPI_ON_COMPUTE && JFA_BWD_EPI_TMA && i == it.i0) {  // the last item's dK/dV stores have read the tile
+                if (row == 0) bulk_wait_group_read<0>();
+                compute_sync();
+            }
             if (JFA_BWD_EARLY_S)
                 bwd_compute_ds_regs<D>(delta, dp_addr, ds_tile, row, pkeep);
             else
@@ -631,6 +641,13 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             tc_fence_after();
             const int rows_valid = min(128, it.Lk - 128 * it.n);
             const int64_t row0 = static_cast<int64_t>(it.kv_start) + 128 * it.n;
+            // Whole tiles leave by TMA stores; a ragged tail tile (which must not
+            // touch the next sequence's rows) by coalesced row copies.
+            const bool tma_ok = JFA_BWD_EPI_TMA && rows_valid == 128;
+            if (!tma_ok && JFA_BWD_EPI_TMA) {  // the last item's stores have read the stages
+                if (row == 0) bulk_wait_group_read<0>();
+                compute_sync();
+            }
 #pragma unroll
             for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled)
                 const uint32_t col = which ? L::kColDK : L::kColDV;
@@ -646,7 +663,13 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
                         tc_fence_before();
                         mbar_arrive(which ? &bars.dk_empty : &bars.dv_empty);
                     }
-                    uint8_t* stage = ds_tile + half * 16384;
+                    // Stage (which * halves + half) % 2: dV's halves, then dK's, alternate
+                    // the two 16 KB halves of the dS tile.
+                    uint8_t* stage = ds_tile + ((which * (D / 64) + half) % 2) * 16384;
+                    if (tma_ok && which == 1) {  // the dV store that used this stage has read it
+                        if (row == 0) bulk_wait_group_read<1>();
+                        compute_sync();
+                    }
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         const uint32_t* f = &v[ch / 4][(ch % 4) * 8];
@@ -655,6 +678,16 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
                                        pack_bf16x2(__uint_as_float(f[2]) * sc, __uint_as_float(f[3]) * sc),
                                        pack_bf16x2(__uint_as_float(f[4]) * sc, __uint_as_float(f[5]) * sc),
                                        pack_bf16x2(__uint_as_float(f[6]) * sc, __uint_as_float(f[7]) * sc));
+                    }
+                    if (tma_ok) {  // whole tile: one TMA store of the 128 x 64 stage
+                        fence_proxy_async_smem();
+                        compute_sync();
+                        if (row == 0) {
+                            tma_store_2d(which ? &maps->dk : &maps->dv, stage, it.h * D + half * 64,
+                                         static_cast<int>(row0));
+                            bulk_commit_group();
+                        }
+                        continue;
                     }
                     compute_sync();
 #pragma unroll
@@ -671,7 +704,8 @@ __device__ void bwd_compute_role(const BwdParams& p, uint8_t* smem, BwdBars& bar
             if (row == 0) JFA_TRACE_EVENT(37, 0, idx, 0);
         }
     }
-done:;
+done:
+    if (JFA_BWD_EPI_TMA && row == 0) bulk_wait_group<0>();  // every dK/dV store has completed
 }
 
 // ---------------------------------------------------------------------------
@@ -857,7 +891,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp < 4) {
         regs_inc<kComputeRegs>();
-        bwd_compute_role<D>(p, smem, bars, tmem, ib, ie, ab);
+        bwd_compute_role<D>(p, &maps, smem, bars, tmem, ib, ie, ab);
     } else if (warp < 8) {
         if constexpr (kDqRegs > kLaunchRegs) regs_inc<kDqRegs>();
         bwd_dq_role<D>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);

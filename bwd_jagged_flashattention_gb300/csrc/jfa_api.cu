@@ -393,7 +393,8 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     BwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
         !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dout, dout, o_rows, H, D, workspace) ||
-        !map_rows_f32(&maps.dq, dq_target, partial ? q_rows * kDqGroups : q_rows, H, D, workspace))
+        !map_rows_f32(&maps.dq, dq_target, partial ? q_rows * kDqGroups : q_rows, H, D, workspace) ||
+        !map_rows_bf16(&maps.dk, dk, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dv, dv, pr.N, H, D, workspace))
         return JFA_ERR_CUDA;
     BwdParams p;
     p.cta_start = reinterpret_cast<const int32_t*>(ws + w.bwd_off);

@@ -62,6 +62,7 @@ struct FwdMaps {
 };
 struct BwdMaps {
     CUtensorMap q, k, v, dout, dq;
+    CUtensorMap dk, dv;  // bf16 [N, H*D] outputs, same boxes as K/V (dK/dV TMA stores)
 };
 
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s);
