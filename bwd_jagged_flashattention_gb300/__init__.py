@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
             L.jfa_selftest_mma.restype = ci
             L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
             L.jfa_host_build_schedule.restype = ctypes.c_longlong
+            if hasattr(L, "jfa_host_build_schedule_noalloc"):  # host-only test entry
+                L.jfa_host_build_schedule_noalloc.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, vp, vp,
+                                                              ctypes.c_longlong]
+                L.jfa_host_build_schedule_noalloc.restype = ctypes.c_longlong
             _lib = L
     return _lib
 
@@ -195,18 +199,27 @@ def num_ctas() -> int:
     return int(lib().jfa_num_ctas())
 
 
+SCHED_ZIGZAG, SCHED_NAIVE, SCHED_GREEDY = 0, 1, 2  # deal policies (SCHED_GREEDY is the library's)
+
+
 def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool, is_bwd: bool, P: int,
-                  policy: int = 0):
-    """The host scheduler alone (no GPU): returns (items int32 [n,4], cta_start int32 [P+1])."""
+                  policy: int = SCHED_ZIGZAG, noalloc: bool = False):
+    """The host scheduler alone (no GPU): returns (items int32 [n,4], cta_start int32 [P+1]).
+    noalloc=True runs the allocation-free builder (always the greedy deal)."""
     off = offsets_host.to(torch.int32).contiguous()
     B = off.numel() - 1
     N = int(off[-1]) if B > 0 else 0
     cap = H * (N // 128 + B) + H * B * ((max(Lq, 0) + 255) // 256) + 1
     items = torch.zeros((cap, 4), dtype=torch.int32)
     starts = torch.zeros(P + 1, dtype=torch.int32)
-    n = lib().jfa_host_build_schedule(ctypes.c_void_p(off.data_ptr()), B, Lq, H, int(broadcast_q), int(causal),
-                                      int(is_bwd), P, policy, ctypes.c_void_p(items.data_ptr()),
-                                      ctypes.c_void_p(starts.data_ptr()), cap)
+    if noalloc:
+        n = lib().jfa_host_build_schedule_noalloc(ctypes.c_void_p(off.data_ptr()), B, Lq, H, int(broadcast_q),
+                                                  int(causal), int(is_bwd), P, ctypes.c_void_p(items.data_ptr()),
+                                                  ctypes.c_void_p(starts.data_ptr()), cap)
+    else:
+        n = lib().jfa_host_build_schedule(ctypes.c_void_p(off.data_ptr()), B, Lq, H, int(broadcast_q),
+                                          int(causal), int(is_bwd), P, policy, ctypes.c_void_p(items.data_ptr()),
+                                          ctypes.c_void_p(starts.data_ptr()), cap)
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
     return items[:n].clone(), starts

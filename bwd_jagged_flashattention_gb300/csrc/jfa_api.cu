@@ -108,7 +108,8 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     }
     int32_t* cta_start = static_cast<int32_t*>(slot.buf);
     WorkItem* items = reinterpret_cast<WorkItem*>(static_cast<char*>(slot.buf) + kCtaStartBytes);
-    const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, kSchedLptZigzag, items,
+    const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P,
+                                     is_bwd ? kSchedLptZigzag : kSchedLptGreedy, items,
                                      cta_start, max_items);
     if (n < 0) {
         *st = JFA_ERR_WORKSPACE;

@@ -50,6 +50,57 @@ inline int32_t zigzag_head_cta(int64_t pos, int h, int G, int H) {
     return static_cast<int32_t>(((r & 1) ? (G - 1 - lane) : lane) * H + h);
 }
 
+// Restore the min-heap property below slot k of heap[0..size).
+inline void sift_down(int64_t* heap, int size, int k) {
+    for (;;) {
+        int c = 2 * k + 1;
+        if (c >= size) return;
+        if (c + 1 < size && heap[c + 1] < heap[c]) ++c;
+        if (heap[k] <= heap[c]) return;
+        std::swap(heap[k], heap[c]);
+        k = c;
+    }
+}
+
+// Deal the n cost-sorted items gen[order[i]] to CTAs (owner[i]).
+//   zigzag: sorted position i, round r = i / P, lane p = i % P; CTA p on even
+//           rounds, CTA P-1-p on odd rounds (the pages' deal);
+//   greedy: each item to the CTA with the least cost so far (ties: lowest
+//           lane) -- the longest-processing-time rule zigzag approximates;
+//   naive:  round-robin.
+// Broadcast Q with H | P (head_partition()): the deal runs within each head's
+// group of G = P/H CTAs {h, h+H, ...}.  heap: scratch of P int64 (greedy).
+void deal(const WorkItem* gen, const int64_t* order, int64_t n, int Lq, int H, int broadcast_q, int causal,
+          int is_bwd, int P, int policy, int32_t* owner, int64_t* heap) {
+    const bool by_head = policy != kSchedNaive && head_partition(broadcast_q, H, P);
+    const int groups = by_head ? H : 1, G = P / groups;
+    if (policy == kSchedLptGreedy) {
+        // One min-heap per group of keys load * 1024 + lane (lane < 1024).
+        for (int g = 0; g < groups; ++g)
+            for (int lane = 0; lane < G; ++lane) heap[g * G + lane] = lane;  // sorted: a valid heap
+        for (int64_t i = 0; i < n; ++i) {
+            const WorkItem& w = gen[order[i]];
+            const int g = by_head ? static_cast<int>(w.packed & 0xFFu) : 0;
+            int64_t* hs = heap + static_cast<int64_t>(g) * G;
+            const int lane = static_cast<int>(hs[0] & 1023);
+            hs[0] += item_cost(w, Lq, broadcast_q, causal, is_bwd) * 1024;
+            sift_down(hs, G, 0);
+            owner[i] = by_head ? lane * H + g : lane;
+        }
+        return;
+    }
+    int64_t head_pos[256] = {0};
+    for (int64_t i = 0; i < n; ++i) {
+        if (by_head) {
+            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
+            owner[i] = zigzag_head_cta(head_pos[h]++, h, G, H);
+        } else {
+            const int64_t r = i / P, p = i % P;
+            owner[i] = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
+        }
+    }
+}
+
 // Key of the Q tiles an item reads in broadcast mode: the head and (forward)
 // the first query tile.  Consecutive items of one CTA with equal keys share
 // the resident Q tiles, so the kernels load them once per run of equal keys.
@@ -104,7 +155,7 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
 
     // 2. Order: cost-descending, stable (counting sort on the integer cost).
     std::vector<int64_t> order(static_cast<size_t>(n));
-    if (policy == kSchedLptZigzag && n > 0) {
+    if (policy != kSchedNaive && n > 0) {
         std::vector<int64_t> cost(static_cast<size_t>(n));
         int64_t cmax = 0;
         for (int64_t i = 0; i < n; ++i) {
@@ -119,31 +170,17 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         for (int64_t i = 0; i < n; ++i) order[i] = i;
     }
 
-    // 3. Deal.  Zigzag: sorted position i, round r = i / P, lane p = i % P;
-    //    CTA p on even rounds, CTA P-1-p on odd rounds.  Naive: round-robin.
-    //    Broadcast Q with H | P: the same zigzag within each head's own group
-    //    of P/H CTAs (head_partition()).
+    // 3. Deal (see deal()).
     std::vector<int32_t> owner(static_cast<size_t>(n));
+    std::vector<int64_t> heap(static_cast<size_t>(P));
+    deal(gen.data(), order.data(), n, Lq, H, broadcast_q, causal, is_bwd, P, policy, owner.data(), heap.data());
     std::fill(cta_start, cta_start + P + 1, 0);
-    const bool by_head = policy == kSchedLptZigzag && head_partition(broadcast_q, H, P);
-    std::vector<int64_t> head_pos(by_head ? static_cast<size_t>(H) : 0, 0);
-    for (int64_t i = 0; i < n; ++i) {
-        int32_t cta;
-        if (by_head) {
-            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
-            cta = zigzag_head_cta(head_pos[h]++, h, P / H, H);
-        } else {
-            const int64_t r = i / P, p = i % P;
-            cta = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
-        }
-        owner[i] = cta;
-        ++cta_start[cta + 1];
-    }
+    for (int64_t i = 0; i < n; ++i) ++cta_start[owner[i] + 1];
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
     std::vector<int32_t> fill(cta_start, cta_start + P);
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
     // 4. Broadcast Q: group each CTA's items by the Q tiles they read.
-    if (broadcast_q && policy == kSchedLptZigzag) group_by_q(items, cta_start, P, is_bwd);
+    if (broadcast_q && policy != kSchedNaive) group_by_q(items, cta_start, P, is_bwd);
     return n;
 }
 
@@ -175,21 +212,11 @@ int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int
         const int64_t cost = std::min<int64_t>(item_cost(gen[i], Lq, broadcast_q, causal, is_bwd), kCostBuckets - 1);
         order[buckets[kCostBuckets - 1 - cost]++] = i;
     }
-    // Zigzag deal over P CTAs (per head group when head_partition()), then
-    // CSR placement in deal order.
+    // Greedy deal (the sort's buckets now serve as the heaps), then CSR
+    // placement in deal order.
+    deal(gen, order, n, Lq, H, broadcast_q, causal, is_bwd, P, kSchedLptGreedy, owner, buckets);
     for (int p = 0; p <= P; ++p) cta_start[p] = 0;
-    const bool by_head = head_partition(broadcast_q, H, P);
-    int64_t head_pos[256] = {0};
-    for (int64_t i = 0; i < n; ++i) {
-        if (by_head) {
-            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
-            owner[i] = zigzag_head_cta(head_pos[h]++, h, P / H, H);
-        } else {
-            const int64_t r = i / P, p = i % P;
-            owner[i] = static_cast<int32_t>((r & 1) ? (P - 1 - p) : p);
-        }
-        ++cta_start[owner[i] + 1];
-    }
+    for (int64_t i = 0; i < n; ++i) ++cta_start[owner[i] + 1];
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
     for (int p = 0; p < P; ++p) fill[p] = cta_start[p];
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
@@ -199,7 +226,19 @@ int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int
 
 }  // namespace jfa
 
-// Host-only C entry used by the scheduler's unit tests (no GPU needed).
+// Host-only C entries used by the scheduler's unit tests (no GPU needed).
+extern "C" long long jfa_host_build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int broadcast_q,
+                                                     int causal, int is_bwd, int P, void* items, int32_t* cta_start,
+                                                     long long max_items) {
+    const size_t cap = static_cast<size_t>(max_items > 0 ? max_items : 1);
+    std::vector<jfa::WorkItem> gen(cap);
+    std::vector<int64_t> order(cap), buckets(static_cast<size_t>(jfa::kCostBuckets + 2));
+    std::vector<int32_t> owner(cap), fill(static_cast<size_t>(P > 0 ? P : 1));
+    return jfa::build_schedule_noalloc(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P,
+                                       static_cast<jfa::WorkItem*>(items), cta_start, max_items, gen.data(),
+                                       order.data(), owner.data(), fill.data(), buckets.data());
+}
+
 extern "C" long long jfa_host_build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q,
                                              int causal, int is_bwd, int P, int policy, void* items,
                                              int32_t* cta_start, long long max_items) {
