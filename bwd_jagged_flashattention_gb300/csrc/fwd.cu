@@ -47,6 +47,13 @@ namespace {
 #ifndef JFA_FWD_TRIM_TAIL
 #define JFA_FWD_TRIM_TAIL 0
 #endif
+// O epilogue of whole 128-row tiles through TMA stores (each softmax
+// warpgroup stages a 64-column half in its 16 KB stage, one thread stores it).
+// Measured slower on the ads step (140.9 vs 135.8 us): with one stage per
+// warpgroup the second half waits for the first half's store.
+#ifndef JFA_FWD_EPI_TMA
+#define JFA_FWD_EPI_TMA 0
+#endif
 // Row sums of P: 1 = four paired partial sums (add.f32x2), 0 = eight scalar
 // (ads step: 158.7 vs 164.4 us).
 #ifndef JFA_FWD_PAIRED_SUMS
@@ -508,8 +515,8 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
 }
 
 template <int D>
-__device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
-                                 const AbortState& ab) {
+__device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, uint8_t* smem, FwdBars& bars,
+                                 uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = FwdLayout<D>;
     const int t = threadIdx.x / 128;
     const int row = threadIdx.x % 128;
@@ -593,8 +600,19 @@ __device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bar
             const int64_t row0 = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + 128 * (it.m0 + t)
                                                : static_cast<int64_t>(it.q_row0) + 128 * (it.m0 + t);
             const int rows_valid = min(128, it.q_rows - 128 * (it.m0 + t));
+            // Whole tiles leave by TMA stores (one thread issues, the
+            // warpgroup only stages); a ragged tile by coalesced copies.
+            const bool tma_ok = JFA_FWD_EPI_TMA && rows_valid == 128;
+            if (JFA_FWD_EPI_TMA && !tma_ok) {  // the last store has read the stage
+                if (row == 0) bulk_wait_group_read<0>();
+                group_sync(1 + t);
+            }
 #pragma unroll
             for (int half = 0; half < D / 64; ++half) {
+                if (tma_ok) {  // the previous store (last half, or the last item's) has read the stage
+                    if (row == 0) bulk_wait_group_read<0>();
+                    group_sync(1 + t);
+                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {  // 8 bf16 per 16-byte chunk
                     const uint32_t* f = &orr[half * 2 + ch / 4][(ch % 4) * 8];
@@ -603,6 +621,15 @@ __device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bar
                                                pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv),
                                                pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv));
                     *reinterpret_cast<uint4*>(stage + row * 128 + ((ch ^ (row & 7)) * 16)) = u;
+                }
+                if (tma_ok) {
+                    fence_proxy_async_smem();
+                    group_sync(1 + t);
+                    if (row == 0) {
+                        tma_store_2d(map_o, stage, it.h * D + half * 64, static_cast<int>(row0));
+                        bulk_commit_group();
+                    }
+                    continue;
                 }
                 group_sync(1 + t);
                 // 128 rows x 8 chunks: thread k of the warpgroup copies chunks k, k+128, ...
@@ -620,13 +647,15 @@ __device__ void fwd_softmax_role(const FwdParams& p, uint8_t* smem, FwdBars& bar
         }
         if (row == 0) JFA_TRACE_EVENT(24, t, i, 0);
     }
-done:;
+done:
+    if (JFA_FWD_EPI_TMA && row == 0) bulk_wait_group<0>();  // every O store has completed
 }
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     jfa_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_o) {
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -666,7 +695,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     if (warp < 8) {
         regs_inc<kSoftmaxRegs>();
-        fwd_softmax_role<D>(p, smem, bars, tmem, ib, ie, ab);
+        fwd_softmax_role<D>(p, &map_o, smem, bars, tmem, ib, ie, ab);
     } else {
         regs_dec<kAuxRegs>();
         if (warp == kWarpTma) {
@@ -701,7 +730,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v);
+    jfa_fwd_kernel<D><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v, m.o);
     return cudaGetLastError();
 }
 

@@ -311,7 +311,7 @@ extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const
 
     FwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
-        !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace))
+        !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.o, o, o_rows, H, D, workspace))
         return JFA_ERR_CUDA;
     FwdParams p;
     p.cta_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off);

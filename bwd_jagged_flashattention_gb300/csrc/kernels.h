@@ -59,6 +59,7 @@ __device__ __forceinline__ WorkItem load_item(const WorkItem* items, int i, int 
 // with 64x128 boxes (128-byte swizzle); dQ as 2D [rows, H*D] fp32.
 struct FwdMaps {
     CUtensorMap q, k, v;
+    CUtensorMap o;  // bf16 [O rows, H*D] output, same boxes (O TMA stores)
 };
 struct BwdMaps {
     CUtensorMap q, k, v, dout, dq;

@@ -127,7 +127,7 @@ extern "C" jfa_status jfa_fwd_static_scratch(const void* q, const void* k, const
 
     FwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, scratch) || !map_rows_bf16(&maps.k, k, N, H, D, scratch) ||
-        !map_rows_bf16(&maps.v, v, N, H, D, scratch))
+        !map_rows_bf16(&maps.v, v, N, H, D, scratch) || !map_rows_bf16(&maps.o, o, o_rows, H, D, scratch))
         return JFA_ERR_CUDA;
     FwdParams p;
     p.status = reinterpret_cast<uint32_t*>(scratch);
