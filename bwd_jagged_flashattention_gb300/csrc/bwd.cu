@@ -26,7 +26,7 @@
 // kernel outruns FlashAttention-4 on jagged Blackwell attention, second
 // paragraph).  dK/dV stay in TMEM for the whole item and are written once.
 //
-// Roles (384 threads):
+// Roles (128 x (JFA_BWD_COMPUTE_WGS + 2) threads; listed for one compute warpgroup):
 //   warps 0-3  compute: P^T and dS^T (thread r = key row r = TMEM lane r)
 //   warps 4-7  dQ readout + reduce-add; dK/dV epilogue (staged, coalesced)
 //   warp  8    loads: K, V per item; Q_i (+ LSE_i, Delta_i) and dO_i per tile
@@ -84,18 +84,27 @@ namespace {
 #define JFA_BWD_EPI_ON_COMPUTE 1
 #endif
 
-// 384 threads = three warpgroups (compute, dQ, and load + MMA + two idle
-// warps).  Registers move from the load/MMA warpgroup (which needs ~144 to
-// keep its descriptors without spilling) to the compute warpgroup: launch
-// 384 x 168 = 64,512 = 128 x (kComputeRegs + kDqRegs + kAuxRegs).
-constexpr int kBwdThreads = 384;
-constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kComputeRegs = 192;
+// Compute warpgroups: 1 = one warpgroup computes every query column of its
+// key rows; 2 = two warpgroups, 64 columns each (and one dK/dV store each).
+#ifndef JFA_BWD_COMPUTE_WGS
+#define JFA_BWD_COMPUTE_WGS 2
+#endif
+constexpr int kCW = JFA_BWD_COMPUTE_WGS;
+static_assert(kCW == 1 || kCW == 2, "one or two compute warpgroups");
+// (kCW + 2) warpgroups: compute, dQ, and load + MMA + two idle warps.
+// Registers move from the load/MMA warpgroup to the others, never beyond the
+// launch budget: one compute warpgroup 384 x 168 = 64,512 =
+// 128 x (192 + 168 + 144); two, 512 x 128 = 65,536 = 128 x (2 x 120 + 168 + 104).
+constexpr int kBwdThreads = 128 * (kCW + 2);
+constexpr uint32_t kLaunchRegs = kCW == 1 ? 168 : 128;
+constexpr uint32_t kComputeRegs = kCW == 1 ? 192 : 120;
 constexpr uint32_t kDqRegs = 168;
-constexpr uint32_t kAuxRegs = 144;
-static_assert(128 * (kComputeRegs + kDqRegs + kAuxRegs) <= kBwdThreads * kLaunchRegs, "register split exceeds launch");
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr uint32_t kAuxRegs = kCW == 1 ? 144 : 104;
+static_assert(128 * (kCW * kComputeRegs + kDqRegs + kAuxRegs) <= kBwdThreads * kLaunchRegs,
+              "register split exceeds launch");
+constexpr int kWarpDq = 4 * kCW;        // first warp of the dQ warpgroup
+constexpr int kWarpLoad = 4 * kCW + 4;
+constexpr int kWarpMma = 4 * kCW + 5;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -168,8 +177,8 @@ __device__ __forceinline__ bool group_all(int id, bool pred) {
 
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
 
-// Barrier over the compute warpgroup (warps 0-3; the dQ warpgroup uses id 1).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Barrier over compute warpgroup wg (ids 2 and 3; the dQ warpgroup uses id 1).
+__device__ __forceinline__ void compute_sync(int wg) { asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory"); }
 
 // Operand descriptors are built once per buffer; each MMA adds a
 // compile-time offset (16-byte units) so the issuing thread stays lean.
@@ -188,11 +197,18 @@ __device__ __forceinline__ void issue_kmajor(uint32_t d_tmem, uint64_t a_desc, u
 }
 
 // dV (+)= P^T dO: A = P^T from TMEM (bf16 pairs), B = dO_i [q][D] MN-major.
+// TMEM column of P^T for K step kk (16 queries = 8 columns of bf16 pairs):
+// packed from column 0 with one compute warpgroup, each 32-query chunk over
+// its own S^T columns with two.
+__device__ __forceinline__ constexpr uint32_t p_col(int kk) {
+    return kCW == 1 ? static_cast<uint32_t>(kk * 8) : static_cast<uint32_t>((kk / 2) * 32 + (kk % 2) * 8);
+}
+
 template <int D>
 __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint64_t do_desc, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) mma_ts(d_tmem, p_tmem + kk * 8, do_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
+    for (int kk = 0; kk < 8; ++kk) mma_ts(d_tmem, p_tmem + p_col(kk), do_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
 }
 
 // dK (+)= dS^T Q: A = dS^T [key][q] K-major (smem), B = Q_i [q][D] MN-major.
@@ -494,6 +510,82 @@ __device__ __forceinline__ void bwd_compute_p(const BwdParams& p, const float* l
     tmem_st_wait();
 }
 
+// Two compute warpgroups: warpgroup g owns query columns 64g .. 64g+63 of
+// every key row (32-column chunks c0 = 2g and c0 + 1).  One chunk of S^T is
+// in registers at a time and the log2-LSE values are read 4 at a time, so a
+// thread needs about half the registers of the one-warpgroup pass.  The two
+// warpgroups run concurrently, so chunk c's P^T (16 columns of bf16 pairs)
+// goes over the first half of chunk c's own S^T columns (c * 32), never over
+// S^T columns the other warpgroup may not have read yet; the dV product
+// reads it from there (p_col()).
+template <int D, bool kMask>
+__device__ __forceinline__ void bwd_compute_p_cols(const BwdParams& p, const float* lse2, uint32_t s_addr, int key,
+                                                   int qbase, int q_rows, bool row_valid, int c0,
+                                                   uint32_t (&pkeep)[32]) {
+    int nvis = 128;
+    if (kMask) nvis = row_valid ? min(128, q_rows - qbase) : 0;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + cc;
+        uint32_t sr[32];
+        tmem_ld32(s_addr + c * 32, sr);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) {
+            const float4 f = reinterpret_cast<const float4*>(lse2)[c * 8 + e2];  // queries c*32 + 4*e2 .. +3
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = 2 * e2 + h;
+                const int q0 = c * 32 + 2 * e;
+                float x0, x1;
+                ffma2(x0, x1, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]), p.scale_log2, p.scale_log2,
+                      -(h ? f.z : f.x), -(h ? f.w : f.y));
+                float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if (kMask) {
+                    if (q0 >= nvis || (p.causal && key > qbase + q0)) p0 = 0.0f;
+                    if (q0 + 1 >= nvis || (p.causal && key > qbase + q0 + 1)) p1 = 0.0f;
+                }
+                pk[e] = pack_bf16x2(p0, p1);
+                pkeep[cc * 16 + e] = pk[e];
+            }
+        }
+        tmem_st16(s_addr + c * 32, pk);  // over the first half of its own S^T chunk
+    }
+    tmem_st_wait();
+}
+
+// dS^T for warpgroup g's 64 query columns (slab g of the dS^T tile).
+template <int D>
+__device__ __forceinline__ void bwd_compute_ds_cols(const float* delta, uint32_t dp_addr, uint8_t* ds_tile, int row,
+                                                    int c0, const uint32_t (&pkeep)[32]) {
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+        const int c = c0 + cc;
+        uint32_t dp[32];
+        tmem_ld32(dp_addr + c * 32, dp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) {
+            const float4 f = reinterpret_cast<const float4*>(delta)[c * 8 + e2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = 2 * e2 + h;
+                const float d0 = bf16lo_to_f32(pkeep[cc * 16 + e]) * (__uint_as_float(dp[2 * e]) - (h ? f.z : f.x));
+                const float d1 = bf16hi_to_f32(pkeep[cc * 16 + e]) * (__uint_as_float(dp[2 * e + 1]) - (h ? f.w : f.y));
+                pk[e] = pack_bf16x2(d0, d1);
+            }
+        }
+        uint8_t* slab = ds_tile + (c / 2) * 16384 + row * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int chunk = ((c % 2) * 4 + v) ^ (row % 8);
+            *reinterpret_cast<uint4*>(slab + chunk * 16) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+    }
+}
+
 // dS^T from dP^T (TMEM, 32 columns at a time) and P kept in registers.
 template <int D>
 __device__ __forceinline__ void bwd_compute_ds_regs(const float* delta, uint32_t dp_addr, uint8_t* ds_tile, int row,
@@ -576,8 +668,9 @@ template <int D>
 __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_t* smem, BwdBars& bars,
                                  uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = BwdLayout<D>;
-    const int row = threadIdx.x;  // 0..127
-    const uint32_t lane_off = static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16;
+    const int row = threadIdx.x % 128;  // key row = TMEM lane
+    const int wg = threadIdx.x / 128;   // compute warpgroup (its query columns with two)
+    const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x / 32) % 4) * 32) << 16;
     const uint32_t s_addr = tmem + lane_off + L::kColS;
     const uint32_t dp_addr = tmem + lane_off + L::kColDP;
     uint8_t* ds_tile = smem + L::kDS;
@@ -587,42 +680,53 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
         const int key = 128 * it.n + row;
         const bool row_valid = key < it.Lk;
         const bool kv_full_tile = 128 * (it.n + 1) <= it.Lk;
-        if (row == 0) JFA_TRACE_EVENT(30, 0, idx, 0);
+        if (threadIdx.x == 0) JFA_TRACE_EVENT(30, 0, idx, 0);
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             const float* lse2 = reinterpret_cast<const float*>(smem + L::kStats + st * 1024);
             const float* delta = lse2 + 128;
             if (!mbar_wait_warp(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
             if (!mbar_wait_warp(&bars.s_full, tile_cnt & 1, ab)) goto done;
-            if (row == 0) JFA_TRACE_EVENT(31, 0, i, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(31, 0, i, 0);
             tc_fence_after();
             const bool unmasked = kv_full_tile && 128 * (i + 1) <= it.q_rows && !(p.causal && i == it.n);
-            uint32_t pkeep[64];
-            if (unmasked)
-                bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
-            else
-                bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
-            if (row == 0) JFA_TRACE_EVENT(32, 0, i, 0);
+            uint32_t pkeep[kCW == 1 ? 64 : 32];
+            if constexpr (kCW == 1) {
+                if (unmasked)
+                    bwd_compute_p<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
+                else
+                    bwd_compute_p<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, pkeep);
+            } else {
+                if (unmasked)
+                    bwd_compute_p_cols<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, 2 * wg, pkeep);
+                else
+                    bwd_compute_p_cols<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, 2 * wg, pkeep);
+            }
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(32, 0, i, 0);
             tc_fence_before();
             mbar_arrive(&bars.p_full);
             if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
-            if (row == 0) JFA_TRACE_EVENT(33, 0, i, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(33, 0, i, 0);
             if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
             if (!JFA_BWD_EPI_ON_COMPUTE && JFA_BWD_EPI_STAGED && i == it.i0) {  // the previous item's dK/dV staging has left the buffer
                 if (!mbar_wait_warp(&bars.ds_free, (item_cnt & 1) ^ 1, ab)) goto done;
             }
-            if (row == 0) JFA_TRACE_EVENT(34, 0, i, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(34, 0, i, 0);
             tc_fence_after();
             if (JFA_BWD_EPI_ON_COMPUTE && JFA_BWD_EPI_TMA && i == it.i0) {  // the last item's dK/dV stores have read the tile
                 if (row == 0) bulk_wait_group_read<0>();
-                compute_sync();
+                compute_sync(wg);
             }
-            if (JFA_BWD_EARLY_S)
-                bwd_compute_ds_regs<D>(delta, dp_addr, ds_tile, row, pkeep);
-            else
-                bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
+            if constexpr (kCW == 2) {
+                bwd_compute_ds_cols<D>(delta, dp_addr, ds_tile, row, 2 * wg, pkeep);
+            } else {
+                if (JFA_BWD_EARLY_S)
+                    bwd_compute_ds_regs<D>(delta, dp_addr, ds_tile, row, pkeep);
+                else
+                    bwd_compute_ds<D>(delta, s_addr, dp_addr, ds_tile, row);
+            }
             fence_proxy_async_smem();
-            if (row == 0) JFA_TRACE_EVENT(35, 0, i, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(35, 0, i, 0);
             tc_fence_before();
             mbar_arrive(&bars.ds_full);
             ++q_cnt;
@@ -637,7 +741,7 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
             // sequence end are skipped).  Each accumulator's columns are
             // released after its last half is read.
             if (!mbar_wait_warp(&bars.dkv_full, item_cnt & 1, ab)) goto done;
-            if (row == 0) JFA_TRACE_EVENT(36, 0, idx, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(36, 0, idx, 0);
             tc_fence_after();
             const int rows_valid = min(128, it.Lk - 128 * it.n);
             const int64_t row0 = static_cast<int64_t>(it.kv_start) + 128 * it.n;
@@ -646,10 +750,11 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
             const bool tma_ok = JFA_BWD_EPI_TMA && rows_valid == 128;
             if (!tma_ok && JFA_BWD_EPI_TMA) {  // the last item's stores have read the stages
                 if (row == 0) bulk_wait_group_read<0>();
-                compute_sync();
+                compute_sync(wg);
             }
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled)
+            for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK (scaled); with two warpgroups, warpgroup `which`
+                if (kCW == 2 && which != wg) continue;
                 const uint32_t col = which ? L::kColDK : L::kColDV;
                 const float sc = which ? p.scale : 1.0f;
                 uint16_t* out = which ? p.dk : p.dv;
@@ -665,10 +770,11 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                     }
                     // Stage (which * halves + half) % 2: dV's halves, then dK's, alternate
                     // the two 16 KB halves of the dS tile.
-                    uint8_t* stage = ds_tile + ((which * (D / 64) + half) % 2) * 16384;
-                    if (tma_ok && which == 1) {  // the dV store that used this stage has read it
-                        if (row == 0) bulk_wait_group_read<1>();
-                        compute_sync();
+                    // (two warpgroups: each its own slab, both halves in turn)
+                    uint8_t* stage = ds_tile + (kCW == 2 ? wg : ((which * (D / 64) + half) % 2)) * 16384;
+                    if (tma_ok && (kCW == 2 ? half > 0 : which == 1)) {  // the store that used this stage has read it
+                        if (row == 0) bulk_wait_group_read<kCW == 2 ? 0 : 1>();
+                        compute_sync(wg);
                     }
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -681,7 +787,7 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                     }
                     if (tma_ok) {  // whole tile: one TMA store of the 128 x 64 stage
                         fence_proxy_async_smem();
-                        compute_sync();
+                        compute_sync(wg);
                         if (row == 0) {
                             tma_store_2d(which ? &maps->dk : &maps->dv, stage, it.h * D + half * 64,
                                          static_cast<int>(row0));
@@ -689,7 +795,7 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                         }
                         continue;
                     }
-                    compute_sync();
+                    compute_sync(wg);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int q = row + 128 * k;
@@ -698,10 +804,10 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                             *reinterpret_cast<uint4*>(out + ((row0 + rr) * p.H + it.h) * D + half * 64 + ch * 8) =
                                 *reinterpret_cast<const uint4*>(stage + rr * 128 + ((ch ^ (rr & 7)) * 16));
                     }
-                    compute_sync();
+                    compute_sync(wg);
                 }
             }
-            if (row == 0) JFA_TRACE_EVENT(37, 0, idx, 0);
+            if (threadIdx.x == 0) JFA_TRACE_EVENT(37, 0, idx, 0);
         }
     }
 done:
@@ -716,7 +822,7 @@ template <int D>
 __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8_t* smem, BwdBars& bars,
                             uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = BwdLayout<D>;
-    const int r = threadIdx.x - 128;  // query row of the tile (TMEM lane)
+    const int r = threadIdx.x - 32 * kWarpDq;  // query row of the tile (TMEM lane)
     const bool issuer = r == 0;
     const uint32_t lane_off = static_cast<uint32_t>(((threadIdx.x / 32) % 4) * 32) << 16;
     const uint32_t dq_addr = tmem + lane_off + L::kColDP;
@@ -868,8 +974,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars.do_empty, 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.p_full, 128);
-        mbar_init(&bars.ds_full, 128);
+        mbar_init(&bars.p_full, 128 * kCW);
+        mbar_init(&bars.ds_full, 128 * kCW);
         mbar_init(&bars.ds_empty, 1);
         mbar_init(&bars.dq_full, 1);
         mbar_init(&bars.dq_empty, 128);
@@ -889,10 +995,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp < 4) {
-        regs_inc<kComputeRegs>();
+    if (warp < kWarpDq) {
+        if constexpr (kComputeRegs > kLaunchRegs) regs_inc<kComputeRegs>();
+        if constexpr (kComputeRegs < kLaunchRegs) regs_dec<kComputeRegs>();
         bwd_compute_role<D>(p, &maps, smem, bars, tmem, ib, ie, ab);
-    } else if (warp < 8) {
+    } else if (warp < kWarpDq + 4) {
         if constexpr (kDqRegs > kLaunchRegs) regs_inc<kDqRegs>();
         bwd_dq_role<D>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);
     } else {
