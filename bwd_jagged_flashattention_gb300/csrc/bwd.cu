@@ -94,12 +94,22 @@ static_assert(kCW == 1 || kCW == 2, "one or two compute warpgroups");
 // (kCW + 2) warpgroups: compute, dQ, and load + MMA + two idle warps.
 // Registers move from the load/MMA warpgroup to the others, never beyond the
 // launch budget: one compute warpgroup 384 x 168 = 64,512 =
-// 128 x (192 + 168 + 144); two, 512 x 128 = 65,536 = 128 x (2 x 120 + 168 + 104).
+// 128 x (192 + 168 + 144); two, 512 x 128 = 65,536 = 128 x (2 x 120 + 160 + 112).
 constexpr int kBwdThreads = 128 * (kCW + 2);
 constexpr uint32_t kLaunchRegs = kCW == 1 ? 168 : 128;
-constexpr uint32_t kComputeRegs = kCW == 1 ? 192 : 120;
-constexpr uint32_t kDqRegs = 168;
-constexpr uint32_t kAuxRegs = kCW == 1 ? 144 : 104;
+// Registers per thread of each warpgroup with two compute warpgroups.
+#ifndef JFA_BWD_CW2_CREGS
+#define JFA_BWD_CW2_CREGS 120
+#endif
+#ifndef JFA_BWD_CW2_DQREGS
+#define JFA_BWD_CW2_DQREGS 160
+#endif
+#ifndef JFA_BWD_CW2_AREGS
+#define JFA_BWD_CW2_AREGS 112
+#endif
+constexpr uint32_t kComputeRegs = kCW == 1 ? 192 : JFA_BWD_CW2_CREGS;
+constexpr uint32_t kDqRegs = kCW == 1 ? 168 : JFA_BWD_CW2_DQREGS;
+constexpr uint32_t kAuxRegs = kCW == 1 ? 144 : JFA_BWD_CW2_AREGS;
 static_assert(128 * (kCW * kComputeRegs + kDqRegs + kAuxRegs) <= kBwdThreads * kLaunchRegs,
               "register split exceeds launch");
 constexpr int kWarpDq = 4 * kCW;        // first warp of the dQ warpgroup
