@@ -31,6 +31,13 @@ namespace {
 
 // Tuning knobs (compile-time): K/V ring depth in 128-row tiles at D=128, and
 // how many KV blocks ahead of the ring the L2 prefetch runs (0 = off).
+// O epilogue without a shared-memory stage: each thread stores its own row
+// (frees 32 KB, e.g. for a fifth K/V ring slot).  Ads step: 140.5 us with
+// four slots, 141.6 us with five, vs 138.2 us staged (a fifth slot does not
+// help; three slots cost 23 us).
+#ifndef JFA_FWD_O_ROWSTORE
+#define JFA_FWD_O_ROWSTORE 0
+#endif
 #ifndef JFA_FWD_SLOTS
 #define JFA_FWD_SLOTS 4
 #endif
@@ -88,7 +95,7 @@ struct FwdLayout {
     static constexpr int kRingOff = 2 * kTileBytes;
     // Epilogue staging: 128 rows x 64 columns of bf16 (16 KB) per softmax warpgroup.
     static constexpr int kStageOff = (2 + kSlots) * kTileBytes;
-    static constexpr int kStageBytes = 16384;
+    static constexpr int kStageBytes = JFA_FWD_O_ROWSTORE ? 0 : 16384;
     static constexpr int kBytes = kStageOff + 2 * kStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
@@ -602,6 +609,21 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             const int rows_valid = min(128, it.q_rows - 128 * (it.m0 + t));
             // Whole tiles leave by TMA stores (one thread issues, the
             // warpgroup only stages); a ragged tile by coalesced copies.
+            if (JFA_FWD_O_ROWSTORE) {
+                if (valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.o + ((row0 + row) * p.H + it.h) * D);
+#pragma unroll
+                    for (int ch = 0; ch < D / 8; ++ch) {
+                        const uint32_t* f = &orr[ch / 4][(ch % 4) * 8];
+                        dst[ch] = make_uint4(pack_bf16x2(__uint_as_float(f[0]) * inv, __uint_as_float(f[1]) * inv),
+                                             pack_bf16x2(__uint_as_float(f[2]) * inv, __uint_as_float(f[3]) * inv),
+                                             pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv),
+                                             pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv));
+                    }
+                }
+                if (threadIdx.x % 128 == 0) JFA_TRACE_EVENT(24, t, i, 0);
+                continue;
+            }
             const bool tma_ok = JFA_FWD_EPI_TMA && rows_valid == 128;
             if (JFA_FWD_EPI_TMA && !tma_ok) {  // the last store has read the stage
                 if (row == 0) bulk_wait_group_read<0>();
