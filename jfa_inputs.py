@@ -137,3 +137,18 @@ def custom(B: int, Lq: int, H: int, D: int, lengths, broadcast_q: bool, causal: 
                  lengths="fixed:" + ",".join(str(int(x)) for x in lengths) if B else "fixed:",
                  backward=backward)
     return make(w, seed=seed, lengths=lengths, backward=backward)
+
+
+def num_kv_blocks(offsets: torch.Tensor) -> int:
+    """Number of 128-key blocks over all sequences: sum_b ceil(len_b / 128)."""
+    lens = (offsets[1:] - offsets[:-1]).to(torch.int64)
+    return int(((lens + 127) // 128).sum())
+
+
+def kv_block_mask(offsets: torch.Tensor, H: int, ratio: float, seed: int = 0) -> torch.Tensor:
+    """Seeded block selection for the block-sparse variant: uint8 [NB, H],
+    each (128-key block, head) selected independently with probability
+    `ratio` (a Bernoulli draw from its own generator)."""
+    gen = torch.Generator().manual_seed(10_000 + seed)
+    nb = num_kv_blocks(offsets)
+    return (torch.rand((nb, H), generator=gen) < ratio).to(torch.uint8)

@@ -13,7 +13,11 @@ jagged Blackwell attention, second paragraph).
 Every function here is pinned by ``tests/test_oracle_pins.py`` (brute force
 against padded dense attention with torch autograd in fp64, invariants,
 closed forms, a hand-derived worked example under ``tests/golden/``, central
-finite differences, and the broadcast dQ batch sum).
+finite differences, and the broadcast dQ batch sum).  The block-sparse
+variant (``kv_block_mask``) is pinned by ``tests/test_oracle_block_sparse.py``
+(dense attention over only the gathered selected keys, per sequence and head,
+with torch autograd; exact zeros and -inf for empty selections; planted mask
+bugs).
 """
 from __future__ import annotations
 
@@ -58,6 +62,16 @@ def _offsets_arg(offsets):
     return offsets, ctypes.cast(offsets.data_ptr(), ctypes.POINTER(ctypes.c_int32))
 
 
+def _mask_arg(mask, offsets, H):
+    """uint8 [NB, H] block mask (checked against the offsets) and its pointer."""
+    mask = mask.detach().cpu().to(torch.uint8).contiguous()
+    lens = offsets[1:] - offsets[:-1]
+    nb = int(((lens.to(torch.int64) + 127) // 128).sum())
+    if tuple(mask.shape) != (nb, H):
+        raise ValueError(f"kv_block_mask must be [{nb}, {H}], got {tuple(mask.shape)}")
+    return mask, ctypes.cast(mask.data_ptr(), ctypes.POINTER(ctypes.c_uint8))
+
+
 def _inputs(*ts):
     """All-bf16 inputs pass as raw bf16 (widened exactly in C); anything else as fp64."""
     ts = [t.detach().cpu().contiguous() for t in ts]
@@ -77,6 +91,12 @@ class Oracle:
         lib.jfa_oracle_fwd.restype = None
         lib.jfa_oracle_bwd.argtypes = [vp, vp, vp, vp, ci, i32p, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp]
         lib.jfa_oracle_bwd.restype = None
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.jfa_oracle_fwd_block_sparse.argtypes = [vp, vp, vp, ci, i32p, ci, ci, ci, ci, ci, ci, cd, u8p, vp, vp]
+        lib.jfa_oracle_fwd_block_sparse.restype = None
+        lib.jfa_oracle_bwd_block_sparse.argtypes = [vp, vp, vp, vp, ci, i32p, ci, ci, ci, ci, ci, ci, cd, u8p,
+                                                    vp, vp, vp]
+        lib.jfa_oracle_bwd_block_sparse.restype = None
         lib.jfa_oracle_max_threads.argtypes = []
         lib.jfa_oracle_max_threads.restype = ci
         self.lib = lib
@@ -86,8 +106,11 @@ class Oracle:
         return int(self.lib.jfa_oracle_max_threads())
 
     def fwd(self, q, k, v, offsets, Lq: int, broadcast_q: bool, causal: bool, scale: float,
-            want_o: bool = True, want_lse: bool = True):
-        """O (fp64, [B,Lq,H,D] or [N,H,D]) and LSE (fp64, [B,H,Lq] or [H,N])."""
+            want_o: bool = True, want_lse: bool = True, kv_block_mask=None):
+        """O (fp64, [B,Lq,H,D] or [N,H,D]) and LSE (fp64, [B,H,Lq] or [H,N]).
+
+        kv_block_mask: optional uint8 [NB, H] (NB = sum_b ceil(len_b / 128));
+        a zero entry hides that 128-key block of that head (block-sparse)."""
         offsets, off_p = _offsets_arg(offsets)
         B = offsets.numel() - 1
         N = int(offsets[-1]) if B > 0 else 0
@@ -95,13 +118,19 @@ class Oracle:
         (qq, kk, vv), bf = _inputs(q, k, v)
         o = torch.zeros((B, Lq, H, D) if broadcast_q else (N, H, D), dtype=torch.float64) if want_o else None
         lse = torch.zeros((B, H, Lq) if broadcast_q else (H, N), dtype=torch.float64) if want_lse else None
-        self.lib.jfa_oracle_fwd(_ptr(qq), _ptr(kk), _ptr(vv), bf, off_p, B, Lq, H, D,
-                                int(broadcast_q), int(causal), float(scale), _ptr(o), _ptr(lse))
+        args = (_ptr(qq), _ptr(kk), _ptr(vv), bf, off_p, B, Lq, H, D, int(broadcast_q), int(causal), float(scale))
+        if kv_block_mask is None:
+            self.lib.jfa_oracle_fwd(*args, _ptr(o), _ptr(lse))
+        else:
+            mask, mask_p = _mask_arg(kv_block_mask, offsets, H)
+            self.lib.jfa_oracle_fwd_block_sparse(*args, mask_p, _ptr(o), _ptr(lse))
         return o, lse
 
     def bwd(self, q, k, v, do, offsets, Lq: int, broadcast_q: bool, causal: bool, scale: float,
-            want_dq: bool = True, want_dkv: bool = True):
-        """dQ (fp64, shaped like Q), dK and dV (fp64, [N,H,D]) for upstream gradient dO."""
+            want_dq: bool = True, want_dkv: bool = True, kv_block_mask=None):
+        """dQ (fp64, shaped like Q), dK and dV (fp64, [N,H,D]) for upstream gradient dO.
+
+        kv_block_mask: as for fwd()."""
         offsets, off_p = _offsets_arg(offsets)
         B = offsets.numel() - 1
         N = int(offsets[-1]) if B > 0 else 0
@@ -110,9 +139,13 @@ class Oracle:
         dq = torch.zeros(tuple(q.shape), dtype=torch.float64) if want_dq else None
         dk = torch.zeros((N, H, D), dtype=torch.float64) if want_dkv else None
         dv = torch.zeros((N, H, D), dtype=torch.float64) if want_dkv else None
-        self.lib.jfa_oracle_bwd(_ptr(qq), _ptr(kk), _ptr(vv), _ptr(dd), bf, off_p, B, Lq, H, D,
-                                int(broadcast_q), int(causal), float(scale),
-                                _ptr(dq), _ptr(dk), _ptr(dv))
+        args = (_ptr(qq), _ptr(kk), _ptr(vv), _ptr(dd), bf, off_p, B, Lq, H, D, int(broadcast_q), int(causal),
+                float(scale))
+        if kv_block_mask is None:
+            self.lib.jfa_oracle_bwd(*args, _ptr(dq), _ptr(dk), _ptr(dv))
+        else:
+            mask, mask_p = _mask_arg(kv_block_mask, offsets, H)
+            self.lib.jfa_oracle_bwd_block_sparse(*args, mask_p, _ptr(dq), _ptr(dk), _ptr(dv))
         return dq, dk, dv
 
 

@@ -42,6 +42,19 @@
  *   - Layouts: Q [Lq,H,D] (broadcast) or [N,H,D]; K,V [N,H,D];
  *     O [B,Lq,H,D] or [N,H,D]; LSE [B,H,Lq] or [H,N]; dQ like Q.
  *
+ * Block-sparse variant (the *_block_sparse entry points): the pages say only
+ * that it only adds iteration over selected blocks, the rest of the kernel
+ * staying as it is (TLX porta l'attenzione jagged su Blackwell oltre FA4 con
+ * un terzo del codice, section "The turning point").  Reading taken:
+ * keys come in blocks of 128 counted from each sequence's start, and a
+ * selection applies to one (sequence, head) pair as a whole: key j of
+ * sequence b is visible to every query of head h iff
+ *     kv_block_mask[(block_start[b] + j / 128) * H + h] != 0,
+ * where block_start[b] = sum over b' < b of ceil(len_b' / 128).  Keys of
+ * unselected blocks behave exactly like keys outside the sequence: score
+ * -inf, no weight in O, zero dK and dV; a row with no visible key is an
+ * empty row (O = 0, LSE = -inf, no gradient).
+ *
  * Inputs are either fp64 or bf16 bit patterns (uint16) that are widened
  * exactly to fp64 before any arithmetic.  All arithmetic is fp64.  Outputs
  * are fp64; an output pointer may be NULL, in which case that output is
@@ -113,17 +126,31 @@ static int64_t lse_index(const int32_t *off, int b, int h, int i, int Lq, int H,
  * Returns the number of visible keys (j <= i under causal).
  */
 static int scores(double *s, const double *qi, const double *kmat, int Lk, int D, int i,
-                  int causal, double scale) {
+                  int causal, double scale, const uint8_t *sel, int sel_stride) {
     int visible = 0;
     for (int j = 0; j < Lk; ++j) {
         if (causal && j > i) {
             s[j] = -INFINITY;
+        } else if (sel && !sel[(int64_t)(j / 128) * sel_stride]) {
+            s[j] = -INFINITY; /* key block not selected */
         } else {
             s[j] = scale * dot(qi, kmat + (int64_t)j * D, D);
             ++visible;
         }
     }
     return visible;
+}
+
+/*
+ * First global block index of every sequence (block_start above), or NULL
+ * when there is no mask.  The caller frees it.
+ */
+static int64_t *block_starts(const int32_t *offsets, int B, const uint8_t *mask) {
+    if (!mask) return NULL;
+    int64_t *bs = (int64_t *)malloc(sizeof(int64_t) * ((size_t)B + 1));
+    bs[0] = 0;
+    for (int b = 0; b < B; ++b) bs[b + 1] = bs[b] + (offsets[b + 1] - offsets[b] + 127) / 128;
+    return bs;
 }
 
 /* LSE_i = max + ln sum exp(s - max) over visible keys; -inf when none. */
@@ -137,10 +164,11 @@ static double log_sum_exp(const double *s, int Lk) {
     return m + log(acc);
 }
 
-void jfa_oracle_fwd(const void *q, const void *k, const void *v, int in_bf16,
-                    const int32_t *offsets, int B, int Lq, int H, int D,
-                    int broadcast_q, int causal, double scale,
-                    double *o, double *lse) {
+void jfa_oracle_fwd_block_sparse(const void *q, const void *k, const void *v, int in_bf16,
+                                 const int32_t *offsets, int B, int Lq, int H, int D,
+                                 int broadcast_q, int causal, double scale, const uint8_t *kv_block_mask,
+                                 double *o, double *lse) {
+    int64_t *bstart = block_starts(offsets, B, kv_block_mask);
     const int N = B > 0 ? offsets[B] : 0;
     const int64_t pairs = (int64_t)B * H;
 #pragma omp parallel
@@ -163,9 +191,10 @@ void jfa_oracle_fwd(const void *q, const void *k, const void *v, int in_bf16,
                 load_row(kmat + (int64_t)j * D, k, (int64_t)offsets[b] + j, h, H, D, in_bf16);
                 load_row(vmat + (int64_t)j * D, v, (int64_t)offsets[b] + j, h, H, D, in_bf16);
             }
+            const uint8_t *sel = kv_block_mask ? kv_block_mask + bstart[b] * H + h : NULL;
             for (int i = 0; i < Lqb; ++i) {
                 load_row(qi, q, q_row(offsets, b, i, broadcast_q), h, H, D, in_bf16);
-                scores(s, qi, kmat, Lk, D, i, causal, scale);
+                scores(s, qi, kmat, Lk, D, i, causal, scale, sel, H);
                 const double L = log_sum_exp(s, Lk);
                 if (lse) lse[lse_index(offsets, b, h, i, Lq, H, N, broadcast_q)] = L;
                 if (o) {
@@ -184,12 +213,21 @@ void jfa_oracle_fwd(const void *q, const void *k, const void *v, int in_bf16,
         free(vmat);
         free(s);
     }
+    free(bstart);
 }
 
-void jfa_oracle_bwd(const void *q, const void *k, const void *v, const void *dout, int in_bf16,
+void jfa_oracle_fwd(const void *q, const void *k, const void *v, int in_bf16,
                     const int32_t *offsets, int B, int Lq, int H, int D,
                     int broadcast_q, int causal, double scale,
-                    double *dq, double *dk, double *dv) {
+                    double *o, double *lse) {
+    jfa_oracle_fwd_block_sparse(q, k, v, in_bf16, offsets, B, Lq, H, D, broadcast_q, causal, scale, NULL, o, lse);
+}
+
+void jfa_oracle_bwd_block_sparse(const void *q, const void *k, const void *v, const void *dout, int in_bf16,
+                                 const int32_t *offsets, int B, int Lq, int H, int D,
+                                 int broadcast_q, int causal, double scale, const uint8_t *kv_block_mask,
+                                 double *dq, double *dk, double *dv) {
+    int64_t *bstart = block_starts(offsets, B, kv_block_mask);
     const int N = B > 0 ? offsets[B] : 0;
     const int64_t pairs = (int64_t)B * H;
     const int64_t q_elems = (int64_t)(broadcast_q ? Lq : N) * H * D;
@@ -234,10 +272,11 @@ void jfa_oracle_bwd(const void *q, const void *k, const void *v, const void *dou
                 memset(dkacc, 0, sizeof(double) * (size_t)Lk * D);
                 memset(dvacc, 0, sizeof(double) * (size_t)Lk * D);
             }
+            const uint8_t *sel = kv_block_mask ? kv_block_mask + bstart[b] * H + h : NULL;
             for (int i = 0; i < Lqb; ++i) {
                 load_row(qi, q, q_row(offsets, b, i, broadcast_q), h, H, D, in_bf16);
                 load_row(doi, dout, o_row(offsets, b, i, Lq, broadcast_q), h, H, D, in_bf16);
-                scores(s, qi, kmat, Lk, D, i, causal, scale);
+                scores(s, qi, kmat, Lk, D, i, causal, scale, sel, H);
                 const double L = log_sum_exp(s, Lk);
                 if (L == -INFINITY) continue; /* no visible key: no gradient */
                 /* P_ij overwrites s_ij; dP_ij and Delta_i from the definition. */
@@ -280,4 +319,13 @@ void jfa_oracle_bwd(const void *q, const void *k, const void *v, const void *dou
             for (int64_t e = 0; e < q_elems; ++e) dq[e] += dq_private[(int64_t)t * q_elems + e];
         free(dq_private);
     }
+    free(bstart);
+}
+
+void jfa_oracle_bwd(const void *q, const void *k, const void *v, const void *dout, int in_bf16,
+                    const int32_t *offsets, int B, int Lq, int H, int D,
+                    int broadcast_q, int causal, double scale,
+                    double *dq, double *dk, double *dv) {
+    jfa_oracle_bwd_block_sparse(q, k, v, dout, in_bf16, offsets, B, Lq, H, D, broadcast_q, causal, scale, NULL,
+                                dq, dk, dv);
 }
