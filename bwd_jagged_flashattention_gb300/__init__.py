@@ -28,7 +28,8 @@ JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUD
 
 # Every symbol include/jfa.h and include/jfa_selftest.h declare.
 EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
-            "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma", "jfa_fwd_static_scratch")
+            "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma", "jfa_fwd_static_scratch",
+            "jfa_fwd_block_sparse", "jfa_bwd_block_sparse", "jfa_num_kv_blocks")
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,15 @@ def lib() -> ctypes.CDLL:
             L.jfa_fwd.restype = ci
             L.jfa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp, vp, sz, vp]
             L.jfa_bwd.restype = ci
+            if hasattr(L, "jfa_fwd_block_sparse"):  # (absent only from builds that predate it)
+                L.jfa_fwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp, vp, sz,
+                                                   vp]
+                L.jfa_fwd_block_sparse.restype = ci
+                L.jfa_bwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, vp,
+                                                   vp, vp, sz, vp]
+                L.jfa_bwd_block_sparse.restype = ci
+                L.jfa_num_kv_blocks.argtypes = [vp, ci]
+                L.jfa_num_kv_blocks.restype = ctypes.c_int64
             L.jfa_device_status.argtypes = [vp, vp]
             L.jfa_device_status.restype = ci
             L.jfa_status_string.argtypes = [ci]
@@ -75,6 +85,11 @@ def lib() -> ctypes.CDLL:
             L.jfa_selftest_mma.argtypes = [ci, vp, vp, vp, vp, vp]
             L.jfa_selftest_mma.restype = ci
             L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
+            ll = ctypes.c_longlong
+            if hasattr(L, "jfa_host_build_schedule_sparse"):
+                L.jfa_host_build_schedule_sparse.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ll, vp, vp, vp,
+                                                             ll, ctypes.POINTER(ll)]
+                L.jfa_host_build_schedule_sparse.restype = ll
             L.jfa_host_build_schedule.restype = ctypes.c_longlong
             if hasattr(L, "jfa_host_build_schedule_noalloc"):  # host-only test entry
                 L.jfa_host_build_schedule_noalloc.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, vp, vp,
@@ -173,6 +188,74 @@ def bwd(q, k, v, o, lse, do, offsets, broadcast_q: bool = True, causal: bool = F
     return dq, dk, dv
 
 
+def num_kv_blocks(offsets_host) -> int:
+    """NB = sum_b ceil(len_b / 128), the row count of a block-sparse mask."""
+    off = offsets_host.detach().to("cpu", torch.int32).contiguous()
+    n = int(lib().jfa_num_kv_blocks(ctypes.c_void_p(off.data_ptr()), off.numel() - 1))
+    if n < 0:
+        raise JFAError(JFA_ERR_INVALID_ARG, "jfa_num_kv_blocks")
+    return n
+
+
+def _host_mask(kv_block_mask, offsets_host, H):
+    mask = kv_block_mask.detach().to("cpu", torch.uint8).contiguous()
+    nb = num_kv_blocks(offsets_host)
+    if tuple(mask.shape) != (nb, H):
+        raise ValueError(f"kv_block_mask must be uint8 [{nb}, {H}] (key blocks x heads), got {tuple(mask.shape)}")
+    return mask
+
+
+def fwd_block_sparse(q, k, v, offsets, kv_block_mask, broadcast_q: bool = True, scale: float | None = None,
+                     offsets_host=None, workspace=None, out=None, lse=None):
+    """Block-sparse O and LSE: only the key blocks kv_block_mask (host uint8 [NB, H]) selects."""
+    assert q.is_cuda and q.dtype == torch.bfloat16 and k.dtype == torch.bfloat16 and v.dtype == torch.bfloat16
+    H, D = k.shape[1], k.shape[2]
+    offsets_host = _host_offsets(offsets, offsets_host)
+    mask = _host_mask(kv_block_mask, offsets_host, H)
+    B = offsets_host.numel() - 1
+    N = int(offsets_host[-1]) if B > 0 else 0
+    Lq = q.shape[0] if broadcast_q else 0
+    out = torch.empty((B, Lq, H, D) if broadcast_q else (N, H, D), dtype=torch.bfloat16,
+                      device=q.device) if out is None else out
+    lse = torch.empty((B, H, Lq) if broadcast_q else (H, N), dtype=torch.float32,
+                      device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = new_workspace(B, N, Lq, H, D, broadcast_q, False, q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    offsets_dev = offsets if (offsets is not None and offsets.is_cuda) else None
+    st = lib().jfa_fwd_block_sparse(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()),
+                                    _ptr(offsets_dev), ctypes.c_void_p(offsets_host.data_ptr()),
+                                    ctypes.c_void_p(mask.data_ptr()), B, Lq, H, D, int(broadcast_q), sc, _ptr(out),
+                                    _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q.device))
+    _check(st, "jfa_fwd_block_sparse")
+    return out, lse
+
+
+def bwd_block_sparse(q, k, v, o, lse, do, offsets, kv_block_mask, broadcast_q: bool = True,
+                     scale: float | None = None, offsets_host=None, workspace=None, dq=None, dk=None, dv=None):
+    """Block-sparse dQ, dK, dV (unselected keys get zero dK and dV)."""
+    H, D = k.shape[1], k.shape[2]
+    offsets_host = _host_offsets(offsets, offsets_host)
+    mask = _host_mask(kv_block_mask, offsets_host, H)
+    B = offsets_host.numel() - 1
+    N = int(offsets_host[-1]) if B > 0 else 0
+    Lq = q.shape[0] if broadcast_q else 0
+    dq = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device) if dv is None else dv
+    if workspace is None:
+        workspace = new_workspace(B, N, Lq, H, D, broadcast_q, False, q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    offsets_dev = offsets if (offsets is not None and offsets.is_cuda) else None
+    st = lib().jfa_bwd_block_sparse(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v.contiguous()),
+                                    _ptr(o.contiguous()), _ptr(lse.contiguous()), _ptr(do.contiguous()),
+                                    _ptr(offsets_dev), ctypes.c_void_p(offsets_host.data_ptr()),
+                                    ctypes.c_void_p(mask.data_ptr()), B, Lq, H, D, int(broadcast_q), sc, _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(q.device))
+    _check(st, "jfa_bwd_block_sparse")
+    return dq, dk, dv
+
+
 def device_status(workspace, device=None) -> int:
     """Synchronises the current stream and returns (and clears) the kernels' status word."""
     device = workspace.device if device is None else device
@@ -183,7 +266,7 @@ def profile_enable(on: bool = True) -> None:
     _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
 
 
-PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum")
+PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles")
 
 
 def profile_read() -> dict:
@@ -223,6 +306,32 @@ def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
     return items[:n].clone(), starts
+
+
+def host_schedule_sparse(offsets_host, kv_block_mask, Lq: int, H: int, broadcast_q: bool, is_bwd: bool, P: int):
+    """The block-sparse host schedule alone (no GPU): (items [n,4], cta_start [P+1], sel [B*H,4]
+    = (list offset, selected, full selected, 0), blocks [n_blocks], zero tiles [n_zero,4] =
+    (row0, rows, h, 0))."""
+    off = offsets_host.to(torch.int32).contiguous()
+    B = off.numel() - 1
+    N = int(off[-1]) if B > 0 else 0
+    mask = _host_mask(kv_block_mask, off, H)
+    cap_items = H * (N // 128 + B) + H * B * ((max(Lq, 0) + 255) // 256) + 1
+    cap = H * (N // 128 + B) + 1
+    items = torch.zeros((cap_items, 4), dtype=torch.int32)
+    starts = torch.zeros(P + 1, dtype=torch.int32)
+    sel = torch.zeros((max(B * H, 1), 4), dtype=torch.int32)
+    blocks = torch.zeros(cap, dtype=torch.int32)
+    zero = torch.zeros((cap, 4), dtype=torch.int32)
+    counts = (ctypes.c_longlong * 2)()
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    n = lib().jfa_host_build_schedule_sparse(vp(off), B, Lq, H, int(broadcast_q), int(is_bwd), P, vp(mask),
+                                             vp(items), vp(starts), cap_items, vp(sel), vp(blocks), vp(zero), cap,
+                                             counts)
+    if n < 0:
+        raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule_sparse")
+    return (items[:n].clone(), starts, sel[:B * H].clone(), blocks[:counts[0]].clone(),
+            zero[:counts[1]].clone())
 
 
 def selftest_mma(mode: int, a, b):

@@ -1123,7 +1123,31 @@ cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStr
     return cudaGetLastError();
 }
 
+// Block-sparse backward: the keys of an unselected tile have no weight in
+// any query's softmax, so their dK and dV rows are zero.  One tile per CTA
+// (grid-stride over the list), 16-byte stores of one head's D columns.
+__global__ void __launch_bounds__(256) jfa_zero_tiles_kernel(const ZeroTile* tiles, int64_t n, uint16_t* dk,
+                                                             uint16_t* dv, int H, int D) {
+    const int vecs = D / 8;  // 16-byte vectors per row
+    for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
+        const int4 z = __ldg(reinterpret_cast<const int4*>(tiles) + t);  // row0, rows, h
+        for (int e = threadIdx.x; e < z.y * vecs; e += blockDim.x) {
+            const int64_t off = ((static_cast<int64_t>(z.x) + e / vecs) * H + z.z) * D + (e % vecs) * 8;
+            *reinterpret_cast<uint4*>(dk + off) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(dv + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_zero_tiles(const ZeroTile* tiles, int64_t n, uint16_t* dk, uint16_t* dv, int H, int D,
+                              cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(n < 152 * 16 ? n : 152 * 16);
+    jfa_zero_tiles_kernel<<<grid, 256, 0, s>>>(tiles, n, dk, dv, H, D);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s) {
     if (p.rows <= 0) return cudaSuccess;

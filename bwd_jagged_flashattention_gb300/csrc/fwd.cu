@@ -113,10 +113,15 @@ struct FwdBars {
 
 struct FwdItem {
     int b, h, kv_start, Lk, m0, nq, q_row0, q_rows;
+    int Lk_trim;  // keys the ragged-tail trim sees (no trim under a block-sparse selection)
+    int sel_off;  // block-sparse: the item's first entry in the selected-block list
     int nblk[2], nfull[2], nb;
 };
 
 // Every role derives the same per-item loop bounds from the work item.
+// kSparse: the call has a block-sparse selection (p.sel set); the dense
+// kernel is a separate instantiation without the selection look-up.
+template <bool kSparse>
 __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams& p) {
     FwdItem it;
     it.b = w.b;
@@ -127,14 +132,23 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
     it.nq = 1 + static_cast<int>(w.packed >> 31);
     it.q_row0 = p.broadcast_q ? 0 : w.kv_start;
     it.q_rows = p.broadcast_q ? p.Lq : w.kv_len;
-    const int nkv = (it.Lk + 127) / 128;
+    int nkv = (it.Lk + 127) / 128, full = it.Lk / 128;
+    it.Lk_trim = it.Lk;
+    it.sel_off = 0;
+    if (kSparse) {  // block-sparse (never causal): visit only the selected blocks, in ascending order
+        const int4 s = __ldg(reinterpret_cast<const int4*>(p.sel) + static_cast<int64_t>(it.b) * p.H + it.h);
+        it.sel_off = s.x;
+        nkv = s.y;
+        full = s.z;  // a ragged last block, when selected, is the last one visited
+        it.Lk_trim = 1 << 30;
+    }
     it.nb = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         if (t < it.nq) {
             const int m = it.m0 + t;
             it.nblk[t] = p.causal ? min(m + 1, nkv) : nkv;
-            it.nfull[t] = p.causal ? min(m, it.Lk / 128) : it.Lk / 128;
+            it.nfull[t] = p.causal ? min(m, full) : full;
         } else {
             it.nblk[t] = 0;
             it.nfull[t] = 0;
@@ -142,6 +156,12 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
         it.nb = max(it.nb, it.nblk[t]);
     }
     return it;
+}
+
+// Key block (counted from the sequence start) of the item's j-th visited block.
+template <bool kSparse>
+__device__ __forceinline__ int kv_block(const FwdParams& p, const FwdItem& it, int j) {
+    return kSparse ? __ldg(p.sel_blocks + it.sel_off + j) : j;
 }
 
 // Broadcast Q: an item reuses the Q tiles already in shared memory when it
@@ -162,13 +182,14 @@ struct QKey {
 // Whether the next item that uses Q after item i reads the same Q tiles
 // (`next` = item i + 1, already loaded; empty sequences in between are rare
 // and read on the spot).
+template <bool kSparse>
 __device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const FwdItem& it, const WorkItem& next, int i,
                                                    int ie) {
     if (!p.broadcast_q || i + 1 >= ie) return false;
-    FwdItem nx = decode_fwd(next, p);
+    FwdItem nx = decode_fwd<kSparse>(next, p);
     for (int k = i + 1; nx.nb == 0;) {
         if (++k >= ie) return false;
-        nx = decode_fwd(p.items[k], p);
+        nx = decode_fwd<kSparse>(p.items[k], p);
     }
     return nx.h == it.h && nx.m0 == it.m0 && nx.nq == it.nq;
 }
@@ -240,12 +261,12 @@ struct PrefetchCursor {
     int i, j, nb, h, kv_start;
 };
 
-template <int D>
+template <int D, bool kSparse>
 __device__ __forceinline__ void prefetch_next_block(PrefetchCursor& c, const FwdParams& p, int ie,
                                                     const CUtensorMap* mk, const CUtensorMap* mv) {
     while (c.i < ie && c.j >= c.nb) {
         if (++c.i >= ie) return;
-        const FwdItem it = decode_fwd(p.items[c.i], p);
+        const FwdItem it = decode_fwd<kSparse>(p.items[c.i], p);
         c.j = 0;
         c.nb = it.nb;
         c.h = it.h;
@@ -263,7 +284,7 @@ __device__ __forceinline__ void prefetch_next_block(PrefetchCursor& c, const Fwd
 // ---------------------------------------------------------------------------
 // TMA producer (one thread).
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kSparse>
 __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CUtensorMap* mk,
                              const CUtensorMap* mv, uint8_t* smem, FwdBars& bars, int ib, int ie,
                              const AbortState& ab) {
@@ -274,12 +295,12 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     uint32_t ring = 0, q_loads = 0;
     QKey qk;
     PrefetchCursor pf{ib - 1, 0, 0, 0, 0};
-    for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D>(pf, p, ie, mk, mv);
+    for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D, kSparse>(pf, p, ie, mk, mv);
     WorkItem wn = load_item(p.items, ib, ie);
     for (int i = ib; i < ie; ++i) {
         const WorkItem wc = wn;
         wn = load_item(p.items, i + 1, ie);
-        const FwdItem it = decode_fwd(wc, p);
+        const FwdItem it = decode_fwd<kSparse>(wc, p);
         JFA_TRACE_EVENT(1, 8, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {  // else: the resident Q tiles serve this item too
@@ -302,11 +323,11 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
 #pragma unroll
                 for (int s = 0; s < L::kSlabs; ++s)
                     tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
-                                &bars.kv_full[slot], it.h * D + 64 * s, it.kv_start + 128 * j);
+                                &bars.kv_full[slot], it.h * D + 64 * s, it.kv_start + 128 * kv_block<kSparse>(p, it, j));
                 JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
                 ++ring;
             }
-            prefetch_next_block<D>(pf, p, ie, mk, mv);
+            prefetch_next_block<D, kSparse>(pf, p, ie, mk, mv);
         }
     }
 done:
@@ -322,7 +343,7 @@ done:
 //   S0=Q0K0, S1=Q1K0, then for each block j: O0+=P0Vj, S0=Q0K(j+1),
 //   O1+=P1Vj, S1=Q1K(j+1).
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kSparse>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
@@ -338,7 +359,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         const WorkItem wc = wn;
         wn = wn2;  // item i + 1, loaded an iteration ago
         wn2 = load_item(p.items, i + 2, ie);
-        const FwdItem it = decode_fwd(wc, p);
+        const FwdItem it = decode_fwd<kSparse>(wc, p);
         JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {
@@ -346,7 +367,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             q_ph ^= 1;
             qk.set(it);
         }
-        const bool release_q = !next_item_reuses_q(p, it, wn, i, ie);  // this item is the run's last Q user
+        const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
         JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
         if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
@@ -357,7 +378,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         for (int t = 0; t < 2; ++t)
             if (it.nblk[t] > 0) {
                 issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
-                              block_keys(it.Lk, 0));
+                              block_keys(it.Lk_trim, 0));
                 mma_commit(&bars.s_full[t]);
             }
         mma_commit(&bars.kv_empty[kslot]);
@@ -388,12 +409,12 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 JFA_TRACE_EVENT(15, 9, t, j);
                 tc_fence_after();
                 issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0,
-                            static_cast<int>(block_keys(it.Lk, j) / 16));
+                            static_cast<int>(block_keys(it.Lk_trim, j) / 16));
                 JFA_TRACE_EVENT(16, 9, t, j);
                 if (j == it.nblk[t] - 1) mma_commit(&bars.o_full[t]);
                 if (j + 1 < it.nblk[t]) {
                     issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
-                                  block_keys(it.Lk, j + 1));
+                                  block_keys(it.Lk_trim, j + 1));
                     JFA_TRACE_EVENT(18, 9, t, j + 1);
                     mma_commit(&bars.s_full[t]);
                 }
@@ -418,7 +439,7 @@ done:
 // kChunks: 32-column chunks of S that hold visible keys.  A ragged last
 // block (JFA_FWD_TRIM_TAIL) uses only its first kChunks; the products skip
 // the keys past them too, so those P columns are never read.
-template <int D, bool kMask, int kChunks = 4>
+template <int D, bool kSparse, bool kMask, int kChunks = 4>
 __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem& it, int j, int qpos,
                                               uint32_t s_addr, uint32_t o_addr, float& m_use, float& l) {
     uint32_t sr[4][32];
@@ -432,7 +453,7 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
     if (kMask) {
         // Keys kbase .. kbase + nvis - 1 are visible to this row: the
         // sequence end and (causal) the diagonal bound one count.
-        const int kbase = 128 * j;
+        const int kbase = 128 * kv_block<kSparse>(p, it, j);
         int nvis = it.Lk - kbase;
         if (p.causal) nvis = min(nvis, qpos - kbase + 1);
 #pragma unroll
@@ -521,7 +542,7 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
     tmem_st_wait();
 }
 
-template <int D>
+template <int D, bool kSparse>
 __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, uint8_t* smem, FwdBars& bars,
                                  uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = FwdLayout<D>;
@@ -536,7 +557,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
     for (int i = ib; i < ie; ++i) {
         const WorkItem wc = wn;
         wn = load_item(p.items, i + 1, ie);
-        const FwdItem it = decode_fwd(wc, p);
+        const FwdItem it = decode_fwd<kSparse>(wc, p);
         if (t >= it.nq) continue;
         const int nblk = t == 0 ? it.nblk[0] : it.nblk[1];   // scalar copies: no
         const int nfull = t == 0 ? it.nfull[0] : it.nfull[1];  // dynamic array indexing
@@ -563,7 +584,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 0);
             tc_fence_after();
-            softmax_block<D, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            softmax_block<D, kSparse, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 0);
             tc_fence_before();
             mbar_arrive(&bars.p_full[t]);
@@ -573,15 +594,15 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
-            const int nch = (JFA_FWD_TRIM_TAIL & 2) ? min(4, (it.Lk - 128 * j + 31) / 32) : 4;
+            const int nch = (JFA_FWD_TRIM_TAIL & 2) ? min(4, (it.Lk_trim - 128 * j + 31) / 32) : 4;
             if (nch == 4)
-                softmax_block<D, true, 4>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+                softmax_block<D, kSparse, true, 4>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             else if (nch == 3)
-                softmax_block<D, true, 3>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+                softmax_block<D, kSparse, true, 3>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             else if (nch == 2)
-                softmax_block<D, true, 2>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+                softmax_block<D, kSparse, true, 2>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             else
-                softmax_block<D, true, 1>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+                softmax_block<D, kSparse, true, 1>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
             tc_fence_before();
             mbar_arrive(&bars.p_full[t]);
@@ -673,7 +694,7 @@ done:
     if (JFA_FWD_EPI_TMA && row == 0) bulk_wait_group<0>();  // every O store has completed
 }
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     jfa_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -717,14 +738,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     if (warp < 8) {
         regs_inc<kSoftmaxRegs>();
-        fwd_softmax_role<D>(p, &map_o, smem, bars, tmem, ib, ie, ab);
+        fwd_softmax_role<D, kSparse>(p, &map_o, smem, bars, tmem, ib, ie, ab);
     } else {
         regs_dec<kAuxRegs>();
         if (warp == kWarpTma) {
-            if (lane == 0) fwd_tma_role<D>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
+            if (lane == 0) fwd_tma_role<D, kSparse>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            if (lane == 0) fwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
+            if (lane == 0) fwd_mma_role<D, kSparse>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }
@@ -737,7 +758,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int D>
+template <int D, bool kSparse>
 cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     using L = FwdLayout<D>;
     static bool configured = false;
@@ -745,14 +766,15 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
         // The register split above is only safe if the kernel launches with
         // exactly kLaunchRegs registers per thread; refuse to launch otherwise.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_fwd_kernel<D>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_fwd_kernel<D, kSparse>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(jfa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+        e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kDynSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v, m.o);
+    jfa_fwd_kernel<D, kSparse><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v, m.o);
     return cudaGetLastError();
 }
 
@@ -760,7 +782,8 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
 
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    return D == 128 ? launch_fwd_d<128>(p, m, grid, s) : launch_fwd_d<64>(p, m, grid, s);
+    if (p.sel) return D == 128 ? launch_fwd_d<128, true>(p, m, grid, s) : launch_fwd_d<64, true>(p, m, grid, s);
+    return D == 128 ? launch_fwd_d<128, false>(p, m, grid, s) : launch_fwd_d<64, false>(p, m, grid, s);
 }
 
 }  // namespace jfa

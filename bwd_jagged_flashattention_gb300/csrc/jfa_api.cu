@@ -31,18 +31,27 @@ constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// A schedule region holds the CTA bounds and the items, then (block-sparse
+// calls only) the selection tables: forward, one SparseSel per (b, h) and the
+// selected block indices; backward, the unselected tiles (ZeroTile).
 struct WsLayout {
-    size_t fwd_off, bwd_off, region_bytes, delta_off, delta_bytes, dqp_off, dqp_bytes, total;
-    int64_t max_items;
+    size_t fwd_off, bwd_off, fwd_region, bwd_region, delta_off, delta_bytes, dqp_off, dqp_bytes, total;
+    size_t sel_off, blocks_off, zero_off;  // offsets inside a region
+    int64_t max_items, sel_cap;            // sel_cap >= NB * H (NB = key blocks over all sequences)
 };
 
 bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout* w) {
     if (B < 0 || N < 0 || H <= 0) return false;
     w->max_items = max_work_items(B, N, Lq, H, broadcast_q);
-    w->region_bytes = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
+    w->sel_cap = (N / kTileRows + B) * H;
+    w->sel_off = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
+    w->blocks_off = w->sel_off + align_up(static_cast<size_t>(B) * H * sizeof(SparseSel), 256);
+    w->zero_off = w->sel_off;
+    w->fwd_region = w->blocks_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(int32_t), 256);
+    w->bwd_region = w->zero_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(ZeroTile), 256);
     w->fwd_off = kStatusBytes;
-    w->bwd_off = w->fwd_off + w->region_bytes;
-    w->delta_off = w->bwd_off + w->region_bytes;
+    w->bwd_off = w->fwd_off + w->fwd_region;
+    w->delta_off = w->bwd_off + w->bwd_region;
     const int64_t stat_elems = broadcast_q ? static_cast<int64_t>(B) * H * Lq : static_cast<int64_t>(H) * N;
     w->delta_bytes = align_up(static_cast<size_t>(stat_elems) * sizeof(float), 256);
     w->dqp_off = w->delta_off + w->delta_bytes;
@@ -75,10 +84,14 @@ DeviceStage& device_stage(int dev) {
     return stages[dev & 63];
 }
 
-// Builds the schedule into a pinned slot and enqueues its copy into
-// workspace + off.  Returns the item count (>= 0) or -1 on error.
+// Builds the schedule into a pinned slot laid out like the workspace region
+// (WsLayout) and enqueues its copy into ws_region.  With a block mask
+// (block-sparse) the selection tables follow; *n_zero receives the number of
+// unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
 int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
-                       int64_t max_items, void* ws_region, cudaStream_t stream, jfa_status* st) {
+                       const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
+                       int64_t* n_zero, jfa_status* st) {
+    const int64_t max_items = w.max_items;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         *st = JFA_ERR_CUDA;
@@ -91,7 +104,8 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         *st = JFA_ERR_CUDA;
         return -1;
     }
-    const size_t need = kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
+    const size_t need = mask ? (is_bwd ? w.bwd_region : w.fwd_region)
+                             : kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
     if (slot.cap < need) {
         if (slot.buf) cudaFreeHost(slot.buf);
         slot.buf = nullptr;
@@ -106,21 +120,42 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         *st = JFA_ERR_CUDA;
         return -1;
     }
-    int32_t* cta_start = static_cast<int32_t*>(slot.buf);
-    WorkItem* items = reinterpret_cast<WorkItem*>(static_cast<char*>(slot.buf) + kCtaStartBytes);
+    char* buf = static_cast<char*>(slot.buf);
+    int32_t* cta_start = reinterpret_cast<int32_t*>(buf);
+    WorkItem* items = reinterpret_cast<WorkItem*>(buf + kCtaStartBytes);
+    SparseSpec sp;
+    if (mask) {
+        sp.mask = mask;
+        sp.sel = reinterpret_cast<SparseSel*>(buf + w.sel_off);
+        sp.blocks = reinterpret_cast<int32_t*>(buf + w.blocks_off);
+        sp.zero = reinterpret_cast<ZeroTile*>(buf + w.zero_off);
+        sp.cap = w.sel_cap;
+    }
     const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P,
                                      is_bwd ? kSchedLptZigzag : kSchedLptGreedy, items,
-                                     cta_start, max_items);
+                                     cta_start, max_items, mask ? &sp : nullptr);
     if (n < 0) {
         *st = JFA_ERR_WORKSPACE;
         return -1;
     }
+    char* dst = static_cast<char*>(ws_region);
     const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
-    if (cudaMemcpyAsync(ws_region, slot.buf, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaEventRecord(slot.ev, stream) != cudaSuccess) {
+    bool ok = cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+    if (mask && !is_bwd) {
+        ok = ok && cudaMemcpyAsync(dst + w.sel_off, buf + w.sel_off, static_cast<size_t>(B) * H * sizeof(SparseSel),
+                                   cudaMemcpyHostToDevice, stream) == cudaSuccess;
+        ok = ok && (sp.n_blocks == 0 ||
+                    cudaMemcpyAsync(dst + w.blocks_off, buf + w.blocks_off, sp.n_blocks * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, stream) == cudaSuccess);
+    }
+    if (mask && is_bwd)
+        ok = ok && (sp.n_zero == 0 || cudaMemcpyAsync(dst + w.zero_off, buf + w.zero_off, sp.n_zero * sizeof(ZeroTile),
+                                                      cudaMemcpyHostToDevice, stream) == cudaSuccess);
+    if (!ok || cudaEventRecord(slot.ev, stream) != cudaSuccess) {
         *st = JFA_ERR_CUDA;
         return -1;
     }
+    if (n_zero) *n_zero = mask ? sp.n_zero : 0;
     slot.used = true;
     return n;
 }
@@ -222,7 +257,7 @@ int64_t count_items(const Problem& pr, int is_bwd) {
 // ---------------------------------------------------------------------------
 // Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
 // ---------------------------------------------------------------------------
-enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfKinds = 4 };
+enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfZero = 4, kProfKinds = 5 };
 
 struct Profiler {
     std::mutex mu;
@@ -284,10 +319,11 @@ extern "C" size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D
 
 extern "C" int jfa_num_ctas(void) { return ctas_for(1 << 30); }
 
-extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
-                              const int32_t* offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
-                              float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+// Forward for jfa_fwd (mask == NULL) and jfa_fwd_block_sparse.
+static jfa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
+                           const int32_t* offsets_host, const uint8_t* mask, int B, int Lq, int H, int D,
+                           int broadcast_q, int causal, float scale, void* o, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Problem pr;
     jfa_status st = check_common(B, Lq, H, D, broadcast_q, causal, scale, offsets_dev, offsets_host, s, &pr);
@@ -304,8 +340,8 @@ extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const
     char* ws = static_cast<char*>(workspace);
     const int64_t n_items = count_items(pr, 0);
     const int P = ctas_for(n_items);
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w.max_items,
-                                     ws + w.fwd_off, s, &st);
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w, mask,
+                                     ws + w.fwd_off, s, nullptr, &st);
     if (n < 0) return st;
     if (n == 0) return JFA_OK;
 
@@ -325,14 +361,34 @@ extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
+    p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
     return timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) == cudaSuccess ? JFA_OK
                                                                                                 : JFA_ERR_CUDA;
 }
 
-extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                              const void* dout, const int32_t* offsets_dev, const int32_t* offsets_host, int B,
-                              int Lq, int H, int D, int broadcast_q, int causal, float scale, float* dq, void* dk,
-                              void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
+                              const int32_t* offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
+                              float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    return fwd_impl(q, k, v, offsets_dev, offsets_host, nullptr, B, Lq, H, D, broadcast_q, causal, scale, o, lse,
+                    workspace, workspace_bytes, stream);
+}
+
+extern "C" jfa_status jfa_fwd_block_sparse(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
+                                           const int32_t* offsets_host, const uint8_t* kv_block_mask, int B, int Lq,
+                                           int H, int D, int broadcast_q, float scale, void* o, float* lse,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!kv_block_mask) return JFA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, offsets_dev, offsets_host, kv_block_mask, B, Lq, H, D, broadcast_q, 0, scale, o, lse,
+                    workspace, workspace_bytes, stream);
+}
+
+// Backward for jfa_bwd (mask == NULL) and jfa_bwd_block_sparse.
+static jfa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dout, const int32_t* offsets_dev, const int32_t* offsets_host,
+                           const uint8_t* mask, int B, int Lq, int H, int D, int broadcast_q, int causal, float scale,
+                           float* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Problem pr;
     jfa_status st = check_common(B, Lq, H, D, broadcast_q, causal, scale, offsets_dev, offsets_host, s, &pr);
@@ -383,9 +439,16 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
 
     const int64_t n_items = count_items(pr, 1);
     const int P = ctas_for(n_items);
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w.max_items,
-                                     ws + w.bwd_off, s, &st);
+    int64_t n_zero = 0;
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w, mask,
+                                     ws + w.bwd_off, s, &n_zero, &st);
     if (n < 0) return st;
+    if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
+                          return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
+                                                   n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
+                                                   D, s);
+                      }) != cudaSuccess)
+        return JFA_ERR_CUDA;
     if (n == 0) {
         if (partial && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
         return JFA_OK;
@@ -421,6 +484,29 @@ extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const
     return JFA_OK;
 }
 
+extern "C" jfa_status jfa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, const int32_t* offsets_dev, const int32_t* offsets_host, int B,
+                              int Lq, int H, int D, int broadcast_q, int causal, float scale, float* dq, void* dk,
+                              void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    return bwd_impl(q, k, v, o, lse, dout, offsets_dev, offsets_host, nullptr, B, Lq, H, D, broadcast_q, causal, scale,
+                    dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+extern "C" jfa_status jfa_bwd_block_sparse(const void* q, const void* k, const void* v, const void* o,
+                                           const float* lse, const void* dout, const int32_t* offsets_dev,
+                                           const int32_t* offsets_host, const uint8_t* kv_block_mask, int B, int Lq,
+                                           int H, int D, int broadcast_q, float scale, float* dq, void* dk, void* dv,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!kv_block_mask) return JFA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, lse, dout, offsets_dev, offsets_host, kv_block_mask, B, Lq, H, D, broadcast_q, 0,
+                    scale, dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
+extern "C" int64_t jfa_num_kv_blocks(const int32_t* offsets_host, int B) {
+    if (!offsets_host || B < 0) return -1;
+    return num_kv_blocks(offsets_host, B);
+}
+
 extern "C" jfa_status jfa_device_status(void* workspace, void* stream) {
     if (!workspace) return JFA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -453,8 +539,8 @@ extern "C" jfa_status jfa_profile_enable(int on) {
 extern "C" jfa_status jfa_profile_read(double* ms, int* launches, int count) {
     Profiler& p = profiler();
     std::lock_guard<std::mutex> lock(p.mu);
-    double t_ms[kProfKinds] = {0, 0, 0, 0};
-    int n[kProfKinds] = {0, 0, 0, 0};
+    double t_ms[kProfKinds] = {};
+    int n[kProfKinds] = {};
     jfa_status st = JFA_OK;
     for (auto& e : p.pending) {
         float t = 0.0f;

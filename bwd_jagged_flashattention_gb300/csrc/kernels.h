@@ -19,6 +19,8 @@ struct FwdParams {
     int Lq, H, N;
     int broadcast_q, causal;
     float scale_log2;          // softmax scale * log2(e)
+    const SparseSel* sel = nullptr;      // block-sparse: selection per (b, h) at b * H + h; null = dense
+    const int32_t* sel_blocks = nullptr; // block-sparse: the selected block indices the records point into
 };
 
 struct BwdParams {
@@ -70,5 +72,8 @@ cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cu
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
 cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s);
+// Block-sparse backward: zero the dK and dV rows of the n unselected key tiles.
+cudaError_t launch_zero_tiles(const ZeroTile* tiles, int64_t n, uint16_t* dk, uint16_t* dv, int H, int D,
+                              cudaStream_t s);
 
 }  // namespace jfa

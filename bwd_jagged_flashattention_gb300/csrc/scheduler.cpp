@@ -22,6 +22,12 @@ int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q)
     return std::max<int64_t>(std::max(bwd, fwd), 1);
 }
 
+int64_t num_kv_blocks(const int32_t* offsets, int B) {
+    int64_t nb = 0;
+    for (int b = 0; b < B; ++b) nb += ceil_div(offsets[b + 1] - offsets[b], kTileRows);
+    return nb;
+}
+
 int64_t item_cost(const WorkItem& w, int Lq, int broadcast_q, int causal, int is_bwd) {
     const int64_t Lk = w.kv_len;
     const int tile = static_cast<int>((w.packed >> 8) & 0x7FFFFFu);
@@ -70,8 +76,8 @@ inline void sift_down(int64_t* heap, int size, int k) {
 //   naive:  round-robin.
 // Broadcast Q with H | P (head_partition()): the deal runs within each head's
 // group of G = P/H CTAs {h, h+H, ...}.  heap: scratch of P int64 (greedy).
-void deal(const WorkItem* gen, const int64_t* order, int64_t n, int Lq, int H, int broadcast_q, int causal,
-          int is_bwd, int P, int policy, int32_t* owner, int64_t* heap) {
+void deal(const WorkItem* gen, const int64_t* order, const int64_t* cost, int64_t n, int Lq, int H, int broadcast_q,
+          int causal, int is_bwd, int P, int policy, int32_t* owner, int64_t* heap) {
     const bool by_head = policy != kSchedNaive && head_partition(broadcast_q, H, P);
     const int groups = by_head ? H : 1, G = P / groups;
     if (policy == kSchedLptGreedy) {
@@ -83,7 +89,7 @@ void deal(const WorkItem* gen, const int64_t* order, int64_t n, int Lq, int H, i
             const int g = by_head ? static_cast<int>(w.packed & 0xFFu) : 0;
             int64_t* hs = heap + static_cast<int64_t>(g) * G;
             const int lane = static_cast<int>(hs[0] & 1023);
-            hs[0] += item_cost(w, Lq, broadcast_q, causal, is_bwd) * 1024;
+            hs[0] += (cost ? cost[order[i]] : item_cost(w, Lq, broadcast_q, causal, is_bwd)) * 1024;
             sift_down(hs, G, 0);
             owner[i] = by_head ? lane * H + g : lane;
         }
@@ -131,24 +137,61 @@ void group_by_q(WorkItem* items, const int32_t* cta_start, int P, int is_bwd) {
 }  // namespace
 
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
-                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items) {
+                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items,
+                       SparseSpec* sparse) {
     if (P <= 0 || P > kMaxCtas) return -1;
-    // 1. Generate items in (b, h, tile) order.
+    if (sparse && causal) return -1;
+    // 1. Generate items in (b, h, tile) order, with their costs.
     std::vector<WorkItem> gen;
+    std::vector<int64_t> cost;
     gen.reserve(static_cast<size_t>(std::min<int64_t>(max_items, 1 << 22)));
+    int64_t bstart = 0;  // global index of the sequence's first key block
+    if (sparse) sparse->n_blocks = sparse->n_zero = 0;
     for (int b = 0; b < B; ++b) {
         const int32_t Lk = offsets[b + 1] - offsets[b];
         const int64_t nkv = ceil_div(Lk, kTileRows);
+        if (sparse && (bstart + nkv) * H > sparse->cap) return -1;
         if (!is_bwd) {
             const int64_t nq = broadcast_q ? ceil_div(Lq, kTileRows) : nkv;
             // broadcast rows exist even for an empty sequence (their O is 0, LSE -inf)
-            for (int h = 0; h < H; ++h)
-                for (int64_t m = 0; m < nq; m += 2)
-                    gen.push_back({b, offsets[b], Lk, pack_item(h, static_cast<int>(m), m + 1 < nq ? 1 : 0)});
+            for (int h = 0; h < H; ++h) {
+                int64_t blocks = nkv;  // key blocks each query tile of the item visits (non-causal)
+                if (sparse) {
+                    SparseSel& sel = sparse->sel[static_cast<int64_t>(b) * H + h];
+                    sel.off = static_cast<int32_t>(sparse->n_blocks);
+                    sel.n_full = 0;
+                    for (int64_t n = 0; n < nkv; ++n) {
+                        if (!sparse->mask[(bstart + n) * H + h]) continue;
+                        sparse->blocks[sparse->n_blocks++] = static_cast<int32_t>(n);
+                        if (Lk - n * kTileRows >= kTileRows) ++sel.n_full;
+                    }
+                    sel.n_sel = static_cast<int32_t>(sparse->n_blocks - sel.off);
+                    sel.pad = 0;
+                    blocks = sel.n_sel;
+                }
+                for (int64_t m = 0; m < nq; m += 2) {
+                    const WorkItem w{b, offsets[b], Lk, pack_item(h, static_cast<int>(m), m + 1 < nq ? 1 : 0)};
+                    gen.push_back(w);
+                    cost.push_back(sparse ? (m + 1 < nq ? 2 : 1) * blocks + 1
+                                          : item_cost(w, Lq, broadcast_q, causal, is_bwd));
+                }
+            }
         } else {
             for (int h = 0; h < H; ++h)
-                for (int64_t n = 0; n < nkv; ++n) gen.push_back({b, offsets[b], Lk, pack_item(h, static_cast<int>(n), 0)});
+                for (int64_t n = 0; n < nkv; ++n) {
+                    if (sparse && !sparse->mask[(bstart + n) * H + h]) {
+                        const int64_t row0 = offsets[b] + n * kTileRows;
+                        sparse->zero[sparse->n_zero++] = {static_cast<int32_t>(row0),
+                                                          static_cast<int32_t>(std::min<int64_t>(kTileRows, offsets[b + 1] - row0)),
+                                                          h, 0};
+                        continue;
+                    }
+                    const WorkItem w{b, offsets[b], Lk, pack_item(h, static_cast<int>(n), 0)};
+                    gen.push_back(w);
+                    cost.push_back(item_cost(w, Lq, broadcast_q, causal, is_bwd));
+                }
         }
+        bstart += nkv;
         if (static_cast<int64_t>(gen.size()) > max_items) return -1;
     }
     const int64_t n = static_cast<int64_t>(gen.size());
@@ -156,12 +199,8 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     // 2. Order: cost-descending, stable (counting sort on the integer cost).
     std::vector<int64_t> order(static_cast<size_t>(n));
     if (policy != kSchedNaive && n > 0) {
-        std::vector<int64_t> cost(static_cast<size_t>(n));
         int64_t cmax = 0;
-        for (int64_t i = 0; i < n; ++i) {
-            cost[i] = item_cost(gen[i], Lq, broadcast_q, causal, is_bwd);
-            cmax = std::max(cmax, cost[i]);
-        }
+        for (int64_t i = 0; i < n; ++i) cmax = std::max(cmax, cost[i]);
         std::vector<int64_t> start(static_cast<size_t>(cmax + 2), 0);
         for (int64_t i = 0; i < n; ++i) ++start[cmax - cost[i] + 1];  // bucket 0 = largest cost
         for (int64_t c = 1; c <= cmax + 1; ++c) start[c] += start[c - 1];
@@ -173,7 +212,8 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     // 3. Deal (see deal()).
     std::vector<int32_t> owner(static_cast<size_t>(n));
     std::vector<int64_t> heap(static_cast<size_t>(P));
-    deal(gen.data(), order.data(), n, Lq, H, broadcast_q, causal, is_bwd, P, policy, owner.data(), heap.data());
+    deal(gen.data(), order.data(), cost.data(), n, Lq, H, broadcast_q, causal, is_bwd, P, policy, owner.data(),
+         heap.data());
     std::fill(cta_start, cta_start + P + 1, 0);
     for (int64_t i = 0; i < n; ++i) ++cta_start[owner[i] + 1];
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
@@ -214,7 +254,7 @@ int64_t build_schedule_noalloc(const int32_t* offsets, int B, int Lq, int H, int
     }
     // Greedy deal (the sort's buckets now serve as the heaps), then CSR
     // placement in deal order.
-    deal(gen, order, n, Lq, H, broadcast_q, causal, is_bwd, P, kSchedLptGreedy, owner, buckets);
+    deal(gen, order, nullptr, n, Lq, H, broadcast_q, causal, is_bwd, P, kSchedLptGreedy, owner, buckets);
     for (int p = 0; p <= P; ++p) cta_start[p] = 0;
     for (int64_t i = 0; i < n; ++i) ++cta_start[owner[i] + 1];
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
@@ -244,4 +284,25 @@ extern "C" long long jfa_host_build_schedule(const int32_t* offsets, int B, int 
                                              int32_t* cta_start, long long max_items) {
     return jfa::build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, policy,
                                static_cast<jfa::WorkItem*>(items), cta_start, max_items);
+}
+
+// Block-sparse schedule (library policy: greedy forward, zigzag backward) with
+// its selection tables; counts[0] = selected-block entries, counts[1] =
+// unselected backward tiles.  Returns the item count or -1.
+extern "C" long long jfa_host_build_schedule_sparse(const int32_t* offsets, int B, int Lq, int H, int broadcast_q,
+                                                    int is_bwd, int P, const uint8_t* mask, void* items,
+                                                    int32_t* cta_start, long long max_items, void* sel,
+                                                    int32_t* blocks, void* zero, long long cap, long long* counts) {
+    jfa::SparseSpec sp;
+    sp.mask = mask;
+    sp.sel = static_cast<jfa::SparseSel*>(sel);
+    sp.blocks = blocks;
+    sp.zero = static_cast<jfa::ZeroTile*>(zero);
+    sp.cap = cap;
+    const long long n = jfa::build_schedule(offsets, B, Lq, H, broadcast_q, 0, is_bwd, P,
+                                            is_bwd ? jfa::kSchedLptZigzag : jfa::kSchedLptGreedy,
+                                            static_cast<jfa::WorkItem*>(items), cta_start, max_items, &sp);
+    counts[0] = sp.n_blocks;
+    counts[1] = sp.n_zero;
+    return n;
 }

@@ -62,12 +62,48 @@ bool head_partition(int broadcast_q, int H, int P);
 // Upper bound on the number of items either pass produces.
 int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q);
 
+// Block-sparse selection (the pages' block-sparse variant only adds
+// iteration over selected key blocks: TLX porta l'attenzione jagged su
+// Blackwell oltre FA4 con un terzo del codice, section "The turning point").
+// Keys come in blocks of 128 counted from each sequence's start; block n of
+// sequence b is selected for head h iff mask[(block_start[b] + n) * H + h]
+// != 0, block_start[b] = sum over b' < b of ceil(len_b' / 128).
+struct SparseSel {     // forward, one per (b, h) at index b * H + h
+    int32_t off;       // first entry of the pair's selected blocks in the block list
+    int32_t n_sel;     // selected blocks (ascending block indices)
+    int32_t n_full;    // of those, blocks with 128 keys (all but a ragged last block)
+    int32_t pad;
+};
+struct ZeroTile {      // backward: an unselected key tile, whose dK and dV rows are zero
+    int32_t row0;      // first packed row
+    int32_t rows;      // rows in the tile (<= 128)
+    int32_t h;         // head
+    int32_t pad;
+};
+static_assert(sizeof(SparseSel) == 16 && sizeof(ZeroTile) == 16, "16-byte records");
+struct SparseSpec {
+    const uint8_t* mask;  // host uint8 [NB, H]
+    SparseSel* sel;       // out (forward): B * H records
+    int32_t* blocks;      // out (forward): selected block indices, capacity cap
+    ZeroTile* zero;       // out (backward): capacity cap
+    int64_t cap;          // >= NB * H
+    int64_t n_blocks = 0, n_zero = 0;  // out: entries written
+};
+
+// NB = sum_b ceil(len_b / 128).
+int64_t num_kv_blocks(const int32_t* offsets, int B);
+
 // Build a schedule.  Writes `n` items into `items` (capacity max_items) and
 // the CSR bounds cta_start[0..P] (CTA p owns items [cta_start[p],
-// cta_start[p+1])).  Returns n, or -1 if the capacity is too small.
-// is_bwd selects the backward item decomposition and cost.
+// cta_start[p+1])).  Returns n, or -1 if a capacity is too small.
+// is_bwd selects the backward item decomposition and cost.  With `sparse`
+// (not causal): forward items keep their query tiles and cost the selected
+// blocks only, and sparse->sel / blocks list each pair's selected blocks;
+// backward items exist only for selected key tiles, the others go to
+// sparse->zero.
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
-                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items);
+                       int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items,
+                       SparseSpec* sparse = nullptr);
 
 // Allocation-free twin of build_schedule with kSchedLptGreedy (same items,
 // order and deal) for callers that cannot allocate: every array comes from

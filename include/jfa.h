@@ -110,6 +110,44 @@ jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o, c
                    size_t workspace_bytes, void *stream);
 
 /*
+ * Block-sparse variant: attention restricted to selected blocks of keys.
+ * The pages' block-sparse kernel only adds iteration over selected blocks
+ * and leaves the rest unchanged (TLX porta l'attenzione jagged su Blackwell
+ * oltre FA4 con un terzo del codice, section "The turning point").  Keys
+ * come in blocks of 128 counted from each sequence's start (the last block of
+ * a sequence may be shorter); a selection applies to a (sequence, head) pair
+ * as a whole, i.e. to every query row of that sequence and head:
+ *
+ *   kv_block_mask  HOST uint8 [NB, H], row-major, NB = jfa_num_kv_blocks():
+ *                  entry (block_start[b] + n) * H + h != 0 selects key
+ *                  block n of sequence b for head h, where block_start[b] =
+ *                  sum over b' < b of ceil(len_b' / 128).  Read during the
+ *                  call only (the selection is turned into the tile schedule
+ *                  on the host); the caller keeps ownership.
+ *
+ * Keys of unselected blocks are treated like keys outside the sequence: they
+ * get no weight, and their dK and dV rows are written as zeros.  A query row
+ * whose (sequence, head) selects no block gets O = 0, LSE = -inf and adds
+ * nothing to dQ.  Work scales with the selected blocks.  Not defined with
+ * causal masking (there is no causal argument).  All other arguments,
+ * layouts, the workspace (jfa_workspace_bytes() covers it) and the error
+ * behaviour are those of jfa_fwd / jfa_bwd; a NULL mask returns
+ * JFA_ERR_INVALID_ARG.
+ */
+jfa_status jfa_fwd_block_sparse(const void *q, const void *k, const void *v, const int32_t *offsets_dev,
+                                const int32_t *offsets_host, const uint8_t *kv_block_mask, int B, int Lq, int H,
+                                int D, int broadcast_q, float scale, void *o, float *lse, void *workspace,
+                                size_t workspace_bytes, void *stream);
+jfa_status jfa_bwd_block_sparse(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                                const void *dout, const int32_t *offsets_dev, const int32_t *offsets_host,
+                                const uint8_t *kv_block_mask, int B, int Lq, int H, int D, int broadcast_q,
+                                float scale, float *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* NB = sum over the B sequences of ceil(len_b / 128) (host offsets [B+1]); -1 for bad arguments. */
+int64_t jfa_num_kv_blocks(const int32_t *offsets_host, int B);
+
+/*
  * jfa_device_status -- synchronises `stream`, then reads and clears the
  * status word kernels write into `workspace`.  Returns JFA_OK,
  * JFA_ERR_DEVICE_TIMEOUT, or JFA_ERR_CUDA if the synchronisation failed.
@@ -146,13 +184,14 @@ jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, c
                                   void *stream);
 
 /*
- * Measurement aid (computes nothing).  While enabled, every jfa_fwd and
- * jfa_bwd call also records a pair of CUDA events on its stream around each
+ * Measurement aid (computes nothing).  While enabled, every forward and
+ * backward call also records a pair of CUDA events on its stream around each
  * of the library's kernels.  jfa_profile_read() waits for the recorded
  * events and writes, for kernel kind k < count, the summed milliseconds into
  * ms[k] and the launch count into launches[k] (either pointer may be NULL),
  * then clears the totals.  Kinds: 0 forward kernel, 1 backward Delta
- * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum.  The events
+ * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum, 4 block-sparse
+ * zeroing of unselected dK/dV tiles.  The events
  * are host-owned CUDA events; no device memory is allocated.
  */
 jfa_status jfa_profile_enable(int on);

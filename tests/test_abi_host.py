@@ -119,3 +119,31 @@ def test_product_path_has_no_cpu_fallback():
                 assert "jfa_oracle" not in text, f
     src = open(os.path.join(pkg, "__init__.py")).read()
     assert "raise ImportError" in src
+
+
+def test_block_sparse_argument_errors(jfa):
+    """The block-sparse entries check their mask and share the dense checks (no GPU needed)."""
+    lib = jfa.lib()
+    off = torch.tensor([0, 3, 300], dtype=torch.int32)
+    mask = torch.ones(jfa.num_kv_blocks(off), 2, dtype=torch.uint8)
+    p = ctypes.c_void_p(P16)
+    mp = ctypes.c_void_p(mask.data_ptr())
+
+    def fwd(m=mp, D=64, ws_bytes=1 << 30):
+        return lib.jfa_fwd_block_sparse(p, p, p, None, ctypes.c_void_p(off.data_ptr()), m, 2, 32, 2, D, 1, 0.1, p, p,
+                                        ctypes.c_void_p(WS), ws_bytes, None)
+
+    def bwd(m=mp, D=64):
+        return lib.jfa_bwd_block_sparse(p, p, p, p, p, p, None, ctypes.c_void_p(off.data_ptr()), m, 2, 32, 2, D, 1,
+                                        0.1, p, p, p, ctypes.c_void_p(WS), 1 << 30, None)
+    assert fwd(m=None) == jfa.JFA_ERR_INVALID_ARG
+    assert bwd(m=None) == jfa.JFA_ERR_INVALID_ARG
+    assert fwd(D=96) == jfa.JFA_ERR_UNSUPPORTED
+    assert bwd(D=96) == jfa.JFA_ERR_UNSUPPORTED
+    assert fwd(ws_bytes=64) == jfa.JFA_ERR_WORKSPACE
+
+
+def test_num_kv_blocks(jfa):
+    off = torch.tensor([0, 0, 1, 128, 257, 1000], dtype=torch.int32)
+    assert jfa.num_kv_blocks(off) == 0 + 1 + 1 + 2 + 6
+    assert jfa.lib().jfa_num_kv_blocks(None, 3) == -1
