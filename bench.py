@@ -54,11 +54,12 @@ def workload_desc(name):
             f"{mode}, packed K/V [N,{w.H},{w.D}], bf16, {'causal' if w.causal else 'non-causal'}")
 
 
-def metric_name(name, backward):
+def metric_name(name, backward, sparse=None):
     what = "fwd+bwd" if backward else "fwd"
+    tail = f", block-sparse (selection ratio {sparse})" if sparse is not None else ""
     if name == WORKLOAD:
-        return f"{what} TFLOPS (bf16, 1 GB300) on jagged broadcast-Q"
-    return f"{what} TFLOPS (bf16, 1 GB300) on {name}"
+        return f"{what} TFLOPS (bf16, 1 GB300) on jagged broadcast-Q{tail}"
+    return f"{what} TFLOPS (bf16, 1 GB300) on {name}{tail}"
 
 
 # ----------------------------------------------------------------------------
@@ -93,6 +94,42 @@ def accounting(x):
     return dict(pairs=pairs, flops_fwd=f_fwd, flops_bwd=f_bwd, bytes_fwd=bytes_fwd, bytes_pre=bytes_pre,
                 bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e, bytes_sum=bytes_sum,
                 flops_sum=float(q_rows * e * max(dq_groups - 1, 0)))
+
+
+def selected_keys(offsets, mask):
+    """Block-sparse: keys selected per (sequence, head), int64 [B, H]."""
+    lens = (offsets[1:] - offsets[:-1]).tolist()
+    out = torch.zeros(len(lens), mask.shape[1], dtype=torch.int64)
+    g = 0
+    for b, L in enumerate(lens):
+        n = (L + 127) // 128
+        if n:
+            sizes = torch.tensor([min(128, L - 128 * i) for i in range(n)], dtype=torch.int64)
+            out[b] = (mask[g:g + n].to(torch.int64) * sizes[:, None]).sum(0)
+        g += n
+    return out
+
+
+def accounting_sparse(x, mask):
+    """Useful work of the block-sparse step: only (query, key) pairs of selected blocks count, and
+    only selected K/V rows are read; dK/dV of unselected rows are written as zeros (their own kernel)."""
+    acc = accounting(x)
+    sel = selected_keys(x["offsets"], mask)                      # [B, H]
+    lens = (x["offsets"][1:] - x["offsets"][:-1]).to(torch.int64)
+    rows = torch.full_like(lens, x["Lq"]) if x["broadcast_q"] else lens
+    pairs_total = int((rows[:, None] * sel).sum())                # over heads
+    H, D = x["H"], x["D"]
+    f_fwd = 4.0 * D * pairs_total
+    kv_sel = 2 * D * int(sel.sum())                               # bytes of K (or V) rows read
+    kv_all = 2 * x["N"] * H * D
+    q_rows = x["Lq"] if x["broadcast_q"] else x["N"]
+    o_rows = x["B"] * x["Lq"] if x["broadcast_q"] else x["N"]
+    q_b, o_b, stat_b = 2 * q_rows * H * D, 2 * o_rows * H * D, 4 * o_rows * H
+    acc.update(pairs=pairs_total / H, flops_fwd=f_fwd, flops_bwd=2.5 * f_fwd,
+               bytes_fwd=q_b + 2 * kv_sel + o_b + stat_b,
+               bytes_bwd=q_b + 2 * kv_sel + o_b + 2 * stat_b + 2 * kv_sel + 2 * q_b,
+               bytes_zero=2 * (kv_all - kv_sel), selected_fraction=int(sel.sum()) / max(1, x["N"] * H))
+    return acc
 
 
 def load_peaks():
@@ -230,37 +267,45 @@ def max_over_ranks(world, v: float, device) -> float:
 # ----------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample of the same workload)
 # ----------------------------------------------------------------------------
-def oracle_sample(x, nseq):
+def oracle_sample(x, nseq, mask=None):
     import oracle
     off = x["offsets"][: nseq + 1].clone()
     N = int(off[-1])
     sub = dict(x, B=nseq, offsets=off, N=N, k=x["k"][:N], v=x["v"][:N])
     sub["do"] = x["do"][:nseq] if x["broadcast_q"] else x["do"][:N]
     sub["q"] = x["q"] if x["broadcast_q"] else x["q"][:N]
-    flops = 3.5 * 4.0 * x["D"] * x["H"] * pair_count(off, x["Lq"], x["broadcast_q"], x["causal"])
+    m = None
+    if mask is None:
+        flops = 3.5 * 4.0 * x["D"] * x["H"] * pair_count(off, x["Lq"], x["broadcast_q"], x["causal"])
+    else:
+        m = mask[: jfa_inputs.num_kv_blocks(off)]
+        flops = 3.5 * accounting_sparse(sub, m)["flops_fwd"]
     t0 = time.perf_counter()
-    oracle.fwd(sub["q"], sub["k"], sub["v"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"])
-    oracle.bwd(sub["q"], sub["k"], sub["v"], sub["do"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"])
+    oracle.fwd(sub["q"], sub["k"], sub["v"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"],
+               kv_block_mask=m)
+    oracle.bwd(sub["q"], sub["k"], sub["v"], sub["do"], off, x["Lq"], x["broadcast_q"], x["causal"], x["scale"],
+               kv_block_mask=m)
     return flops, time.perf_counter() - t0
 
 
-def size_oracle_sample(x, budget_s):
+def size_oracle_sample(x, budget_s, mask=None):
     """Number of leading sequences whose oracle fwd+bwd takes about budget_s."""
-    f1, t1 = oracle_sample(x, 2)
+    f1, t1 = oracle_sample(x, 2, mask)
     rate = f1 / max(t1, 1e-6)
-    per_seq = 3.5 * 4.0 * x["D"] * x["H"] * pair_count(x["offsets"], x["Lq"], x["broadcast_q"], x["causal"]) / x["B"]
-    return max(1, min(x["B"], int(budget_s * rate / per_seq)))
+    total = (3.5 * 4.0 * x["D"] * x["H"] * pair_count(x["offsets"], x["Lq"], x["broadcast_q"], x["causal"])
+             if mask is None else 3.5 * accounting_sparse(x, mask)["flops_fwd"])
+    return max(1, min(x["B"], int(budget_s * rate / (total / x["B"]))))
 
 
-def cpu_baseline(x, budget_s=12.0):
+def cpu_baseline(x, budget_s=12.0, mask=None):
     """The oracle as it stands on the host cores: repeated passes over the first n sequences
     until about budget_s seconds of CPU work have been timed."""
     import oracle
-    n = size_oracle_sample(x, budget_s)
+    n = size_oracle_sample(x, budget_s, mask)
     flops = secs = 0.0
     reps = 0
     while secs < budget_s * 0.8 and reps < 8:
-        f, t = oracle_sample(x, n)
+        f, t = oracle_sample(x, n, mask)
         flops, secs, reps = flops + f, secs + t, reps + 1
     return {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
             "sample": f"fp64 oracle fwd+bwd, {reps} pass(es) over the first {n} of {x['B']} sequences of the "
@@ -284,17 +329,19 @@ def run_reference(args, world, rank):
         return 0
     import oracle
     x = jfa_inputs.make(args.workload)
+    mask = (jfa_inputs.kv_block_mask(x["offsets"], x["H"], args.block_sparse, seed=1)
+            if args.block_sparse is not None else None)
     budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    n = size_oracle_sample(x, budget)
+    n = size_oracle_sample(x, budget, mask)
     for _ in range(args.warmup):
-        oracle_sample(x, n)
+        oracle_sample(x, n, mask)
     tot_f, tot_t = 0.0, 0.0
     for _ in range(args.steps):
-        f, t = oracle_sample(x, n)
+        f, t = oracle_sample(x, n, mask)
         tot_f += f
         tot_t += t
     value = tot_f / tot_t / 1e12
-    line = {"impl": "reference", "metric": metric_name(args.workload, True),
+    line = {"impl": "reference", "metric": metric_name(args.workload, True, args.block_sparse),
             "value": value, "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -321,6 +368,9 @@ def main():
                     help="use only the first BATCH sequences (small profiling case; not a bench line)")
     ap.add_argument("--workload", default=WORKLOAD, choices=list(jfa_inputs.WORKLOAD_ORDER),
                     help="synthetic workload (default: the ads fwd+bwd step the headline metric is quoted on)")
+    ap.add_argument("--block-sparse", type=float, default=None, metavar="RATIO",
+                    help="block-sparse variant: each (128-key block, head) selected with this probability "
+                         "(seeded); also times the dense step on the same inputs (not a bench line)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -335,7 +385,13 @@ def main():
     backward = "do" in x
     if args.batch:
         x = first_sequences(x, args.batch)
-    acc = accounting(x)
+    sparse = args.block_sparse is not None
+    mask_h = None
+    if sparse:
+        assert not x["causal"], "the block-sparse variant is not defined with causal masking"
+        assert 0.0 < args.block_sparse <= 1.0
+        mask_h = jfa_inputs.kv_block_mask(x["offsets"], x["H"], args.block_sparse, seed=1)
+    acc = accounting_sparse(x, mask_h) if sparse else accounting(x)
     if not backward:
         acc.update(flops_bwd=0.0, bytes_bwd=0, flops_pre=0.0, bytes_pre=0)
     B, Lq, H, D, N = x["B"], x["Lq"], x["H"], x["D"], x["N"]
@@ -352,12 +408,21 @@ def main():
     ws = jfa.new_workspace(B, N, Lq if bq else 0, H, D, bq, causal, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def dense_step():
         jfa.fwd(q, k, v, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h,
                 workspace=ws, out=o, lse=lse)
         if backward:
             jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=bq, causal=causal, scale=x["scale"],
                     offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    def sparse_step():
+        jfa.fwd_block_sparse(q, k, v, off_d, mask_h, broadcast_q=bq, scale=x["scale"], offsets_host=off_h,
+                             workspace=ws, out=o, lse=lse)
+        if backward:
+            jfa.bwd_block_sparse(q, k, v, o, lse, do, off_d, mask_h, broadcast_q=bq, scale=x["scale"],
+                                 offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    step = sparse_step if sparse else dense_step
 
     for _ in range(args.warmup):
         step()
@@ -397,7 +462,8 @@ def main():
     for name, flops, nbytes in (("fwd", acc["flops_fwd"], acc["bytes_fwd"]),
                                 ("bwd_pre", acc["flops_pre"], acc["bytes_pre"]),
                                 ("bwd", acc["flops_bwd"], acc["bytes_bwd"]),
-                                ("dq_sum", acc["flops_sum"], acc["bytes_sum"])):
+                                ("dq_sum", acc["flops_sum"], acc["bytes_sum"]),
+                                ("zero_tiles", 0.0, acc.get("bytes_zero", 0) if backward else 0)):
         ms, n = prof[name]
         avg = ms / max(n, 1)
         tflops = flops / (avg * 1e-3) / 1e12 if avg > 0 else 0.0
@@ -408,7 +474,8 @@ def main():
         kernels[name] = {"launches": n, "avg_ms": avg, "share": None, "tflops": tflops, "gbs": gbs,
                          "tensor_frac": tflops / peaks["bf16_tflops"], "hbm_frac": gbs / peaks["hbm_gbs"],
                          "model_bound": bound, "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-                         "traffic": traffic.get(name)}
+                         # the committed DRAM counters were taken on the dense kernels
+                         "traffic": None if (sparse and name in ("fwd", "bwd")) else traffic.get(name)}
     total_k = sum(k_["avg_ms"] * k_["launches"] for k_ in kernels.values())
     for k_ in kernels.values():
         k_["share"] = k_["avg_ms"] * k_["launches"] / total_k if total_k else None
@@ -452,13 +519,31 @@ def main():
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev) / args.e2e_steps
     e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
 
+    # Block-sparse: the dense step on the same inputs, timed the same way, for the speedup.
+    sparse_info = None
+    if sparse:
+        for _ in range(3):
+            dense_step()
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nd = min(args.steps, 200)
+        d0.record(stream)
+        for _ in range(nd):
+            dense_step()
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dense_ms = max_over_ranks(world, d0.elapsed_time(d1), dev) / nd
+        sparse_info = {"ratio": args.block_sparse, "selected_fraction": acc["selected_fraction"],
+                       "mask": "jfa_inputs.kv_block_mask(offsets, H, ratio, seed=1): uint8 [NB, H]",
+                       "dense_ms_per_step": dense_ms, "speedup_vs_dense": dense_ms / ms_per_step}
+
     if rank != 0:
         return 0
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(x) if backward else None
+        cpu = cpu_baseline(x, mask=mask_h) if backward else None
     line = {
-        "metric": metric_name(args.workload, backward),
+        "metric": metric_name(args.workload, backward, args.block_sparse),
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
@@ -468,9 +553,11 @@ def main():
                    "l2": (f"no flush: K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) exceed the 129 MB L2"
                           if 4 * N * H * D > 129e6 else
                           f"no flush; K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) fit in the 129 MB L2"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   **({"block_sparse": sparse_info} if sparse else {})},
         "fwd_tflops": kernels["fwd"]["tflops"], "bwd_tflops": acc["flops_bwd"] / (
-            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]) * 1e-3) / 1e12
+            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]
+             + kernels["zero_tiles"]["avg_ms"]) * 1e-3) / 1e12
         if backward else None,
         "tensor_peak_frac": {"fwd": kernels["fwd"]["tensor_frac"], "bwd_kernel": kernels["bwd"]["tensor_frac"],
                              "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
