@@ -408,19 +408,22 @@ def main():
     ws = jfa.new_workspace(B, N, Lq if bq else 0, H, D, bq, causal, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def dense_step():
-        jfa.fwd(q, k, v, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h,
-                workspace=ws, out=o, lse=lse)
-        if backward:
-            jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=bq, causal=causal, scale=x["scale"],
-                    offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+    bufs0 = dict(q=q, k=k, v=v, do=do, off=off_d, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
-    def sparse_step():
-        jfa.fwd_block_sparse(q, k, v, off_d, mask_h, broadcast_q=bq, scale=x["scale"], offsets_host=off_h,
-                             workspace=ws, out=o, lse=lse)
+    def dense_step(b=bufs0):
+        jfa.fwd(b["q"], b["k"], b["v"], b["off"], broadcast_q=bq, causal=causal, scale=x["scale"],
+                offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
         if backward:
-            jfa.bwd_block_sparse(q, k, v, o, lse, do, off_d, mask_h, broadcast_q=bq, scale=x["scale"],
-                                 offsets_host=off_h, workspace=ws, dq=dq, dk=dk, dv=dv)
+            jfa.bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["off"], broadcast_q=bq, causal=causal,
+                    scale=x["scale"], offsets_host=off_h, workspace=ws, dq=b["dq"], dk=b["dk"], dv=b["dv"])
+
+    def sparse_step(b=bufs0):
+        jfa.fwd_block_sparse(b["q"], b["k"], b["v"], b["off"], mask_h, broadcast_q=bq, scale=x["scale"],
+                             offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
+        if backward:
+            jfa.bwd_block_sparse(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["off"], mask_h,
+                                 broadcast_q=bq, scale=x["scale"], offsets_host=off_h, workspace=ws, dq=b["dq"],
+                                 dk=b["dk"], dv=b["dv"])
 
     step = sparse_step if sparse else dense_step
 
@@ -490,29 +493,57 @@ def main():
     roof.update(kernel=f"jfa_{dom_name}_kernel", traffic=dom["traffic"], peak_source=peaks["source"],
                 algorithmic_per_launch=dom["algorithmic_bytes"] if roof["bound"] == "hbm" else dom["algorithmic_flops"])
 
-    # End to end: pinned host inputs -> device, both passes, outputs -> host, per step.
-    ins = [(q, x["q"]), (k, x["k"]), (v, x["v"])] + ([(do, x["do"])] if backward else []) + [(off_d, off_h)]
-    ins = [(dst, src.pin_memory()) for dst, src in ins]
-    outs = [o, lse] + ([dq, dk, dv] if backward else [])
-    outs = [(src, torch.empty(src.shape, dtype=src.dtype).pin_memory()) for src in outs]
-    h2d = sum(h.numel() * h.element_size() for _, h in ins)
-    d2h = sum(h.numel() * h.element_size() for _, h in outs)
+    # End to end: every step copies its inputs from pinned host memory to the device, runs both
+    # passes through the library's API and copies all of its outputs (O, LSE, dQ, dK, dV) back to
+    # pinned host memory.  Steps are pipelined the way a streaming caller would: two sets of device
+    # buffers, the input copy of step i+1 on one stream and the output copy of step i-1 on another
+    # while step i computes, with events ordering every reuse of a buffer.
+    in_names = ["q", "k", "v"] + (["do"] if backward else [])
+    out_names = ["o", "lse"] + (["dq", "dk", "dv"] if backward else [])
+    host_in = {n_: x[n_].pin_memory() for n_ in in_names}
+    host_in["off"] = off_h.pin_memory()
+    sets = [bufs0, {n_: torch.empty_like(t_) for n_, t_ in bufs0.items() if t_ is not None}]
+    host_out = [{n_: torch.empty(bufs0[n_].shape, dtype=bufs0[n_].dtype).pin_memory() for n_ in out_names}
+                for _ in range(2)]
+    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+    d2h = sum(h.numel() * h.element_size() for h in host_out[0].values())
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev(), ev()]      # inputs of set j landed
+    comp_done = [ev(), ev()]    # step on set j finished (its inputs free, its outputs ready)
+    out_done = [ev(), ev()]     # outputs of set j copied out (set j's output buffers free)
+    started = [False, False]
 
-    def e2e_step():
-        for dst, h in ins:
-            dst.copy_(h, non_blocking=True)
-        step()
-        for src, h in outs:
-            h.copy_(src, non_blocking=True)
+    def e2e_steps(n_steps):
+        for i in range(n_steps):
+            j = i % 2
+            b = sets[j]
+            with torch.cuda.stream(s_in):
+                if started[j]:
+                    s_in.wait_event(comp_done[j])
+                for n_ in list(in_names) + ["off"]:
+                    b[n_].copy_(host_in[n_], non_blocking=True)
+                in_done[j].record(s_in)
+            stream.wait_event(in_done[j])
+            if started[j]:
+                stream.wait_event(out_done[j])
+            step(b)
+            comp_done[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[j])
+                for n_ in out_names:
+                    host_out[j][n_].copy_(b[n_], non_blocking=True)
+                out_done[j].record(s_out)
+            started[j] = True
 
-    for _ in range(3):
-        e2e_step()
+    e2e_steps(3)
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    s_in.wait_stream(stream)
+    e2e_steps(args.e2e_steps)
+    stream.wait_stream(s_out)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -565,7 +596,8 @@ def main():
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "pipeline": "double-buffered: H2D of step i+1 and D2H of step i-1 overlap step i (3 streams)"},
         "gpu_launches": int(sum(k_["launches"] for k_ in kernels.values())),
         "clocks": clocks,
     }
