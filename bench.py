@@ -368,6 +368,9 @@ def main():
                     help="use only the first BATCH sequences (small profiling case; not a bench line)")
     ap.add_argument("--workload", default=WORKLOAD, choices=list(jfa_inputs.WORKLOAD_ORDER),
                     help="synthetic workload (default: the ads fwd+bwd step the headline metric is quoted on)")
+    ap.add_argument("--lengths", default=None, metavar="SPEC",
+                    help="explicit sequence lengths instead of the workload's recipe, e.g. 131072,512x31 "
+                         "(Lq, H, D and mode stay the workload's; a skew case, not a bench line)")
     ap.add_argument("--block-sparse", type=float, default=None, metavar="RATIO",
                     help="block-sparse variant: each (128-key block, head) selected with this probability "
                          "(seeded); also times the dense step on the same inputs (not a bench line)")
@@ -382,6 +385,15 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     x = jfa_inputs.make(args.workload)
+    if args.lengths:
+        w = jfa_inputs.WORKLOADS[args.workload]
+        lens = []
+        for part in args.lengths.split(","):
+            n, _, rep_ = part.partition("x")
+            lens += [int(n)] * (int(rep_) if rep_ else 1)
+        x = jfa_inputs.custom(len(lens), w.Lq, w.H, w.D, lens, w.broadcast_q, w.causal, seed=1,
+                              backward=w.backward)
+        x["workload"] = f"{args.workload} with lengths {args.lengths}"
     backward = "do" in x
     if args.batch:
         x = first_sequences(x, args.batch)
@@ -578,8 +590,9 @@ def main():
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload) if not args.batch
-                   else f"first {B} sequences of: " + workload_desc(args.workload),
+        "config": {"workload": (workload_desc(args.workload) if not args.batch
+                                else f"first {B} sequences of: " + workload_desc(args.workload))
+                   + (f"; sequence lengths replaced by {args.lengths}" if args.lengths else ""),
                    "B": B, "Lq": Lq, "H": H, "D": D, "N": N, "pairs": acc["pairs"],
                    "l2": (f"no flush: K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) exceed the 129 MB L2"
                           if 4 * N * H * D > 129e6 else

@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
             L.jfa_selftest_mma.restype = ci
             L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
             ll = ctypes.c_longlong
+            if hasattr(L, "jfa_host_build_schedule_split"):
+                L.jfa_host_build_schedule_split.argtypes = [vp, ci, ci, ci, ci, vp, vp, ll, vp, ctypes.POINTER(ll)]
+                L.jfa_host_build_schedule_split.restype = ll
             if hasattr(L, "jfa_host_build_schedule_sparse"):
                 L.jfa_host_build_schedule_sparse.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ll, vp, vp, vp,
                                                              ll, ctypes.POINTER(ll)]
@@ -266,7 +269,7 @@ def profile_enable(on: bool = True) -> None:
     _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
 
 
-PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles")
+PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles", "fwd_merge")
 
 
 def profile_read() -> dict:
@@ -306,6 +309,27 @@ def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
     return items[:n].clone(), starts
+
+
+def host_schedule_split(offsets_host, Lq: int, H: int, P: int):
+    """The broadcast-Q forward schedule with split-KV (no GPU): (items [n,4], cta_start [P+1],
+    groups [n_groups,4] = (b, first slot, chunks, h | tile << 8), slot count)."""
+    off = offsets_host.to(torch.int32).contiguous()
+    B = off.numel() - 1
+    N = int(off[-1]) if B > 0 else 0
+    cap = H * (N // 128 + B) + H * B * ((max(Lq, 0) + 255) // 256) + 1
+    items = torch.zeros((cap, 4), dtype=torch.int32)
+    starts = torch.zeros(P + 1, dtype=torch.int32)
+    groups = torch.zeros((SPLIT_MAX_SLOTS, 4), dtype=torch.int32)
+    counts = (ctypes.c_longlong * 2)()
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    n = lib().jfa_host_build_schedule_split(vp(off), B, Lq, H, P, vp(items), vp(starts), cap, vp(groups), counts)
+    if n < 0:
+        raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule_split")
+    return items[:n].clone(), starts, groups[:counts[0]].clone(), int(counts[1])
+
+
+SPLIT_MAX_SLOTS = 512  # split-KV partial slots per call (the library's workspace bound)
 
 
 def host_schedule_sparse(offsets_host, kv_block_mask, Lq: int, H: int, broadcast_q: bool, is_bwd: bool, P: int):

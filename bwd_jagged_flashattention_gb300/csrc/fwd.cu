@@ -114,6 +114,7 @@ struct FwdBars {
 struct FwdItem {
     int b, h, kv_start, Lk, m0, nq, q_row0, q_rows;
     int Lk_trim;  // keys the ragged-tail trim sees (no trim under a block-sparse selection)
+    int slot;     // split-KV chunk: its partial (O, LSE) slot; -1 for a whole item
     int sel_off;  // block-sparse: the item's first entry in the selected-block list
     int nblk[2], nfull[2], nb;
 };
@@ -135,6 +136,7 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
     int nkv = (it.Lk + 127) / 128, full = it.Lk / 128;
     it.Lk_trim = it.Lk;
     it.sel_off = 0;
+    it.slot = w.b < 0 ? -w.b - 1 : -1;  // a split-KV chunk (its keys are kv_start .. + kv_len)
     if (kSparse) {  // block-sparse (never causal): visit only the selected blocks, in ascending order
         const int4 s = __ldg(reinterpret_cast<const int4*>(p.sel) + static_cast<int64_t>(it.b) * p.H + it.h);
         it.sel_off = s.x;
@@ -427,9 +429,12 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         }
     }
 done:
-    // All issued MMAs must finish before TMEM is released.
-    mma_commit(&bars.mma_done);
-    mbar_wait_drain(&bars.mma_done, 0);
+    // All issued MMAs must finish before TMEM is released.  A CTA that never
+    // took a K/V tile (no items, or only empty ones) issued none.
+    if (ring > 0) {
+        mma_commit(&bars.mma_done);
+        mbar_wait_drain(&bars.mma_done, 0);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -623,6 +628,20 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             tc_fence_before();
             mbar_arrive(&bars.o_empty[t]);  // TMEM O is free: the next item's PV may start
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            if (!kSparse && it.slot >= 0) {  // split-KV chunk: fp32 O and LSE of its keys for the merge pass
+                if (valid) {
+                    const int64_t prow = static_cast<int64_t>(it.slot) * 128 + row;
+                    p.lse_part[prow] = l > 0.0f ? (m_use + lg2_approx(l)) * kLn2 : -INFINITY;
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+                    for (int c = 0; c < D / 4; ++c) {
+                        const uint32_t* f = &orr[c / 8][(c % 8) * 4];
+                        dst[c] = make_float4(__uint_as_float(f[0]) * inv, __uint_as_float(f[1]) * inv,
+                                             __uint_as_float(f[2]) * inv, __uint_as_float(f[3]) * inv);
+                    }
+                }
+                continue;
+            }
             if (valid) p.lse[lse_idx] = l > 0.0f ? (m_use + lg2_approx(l)) * kLn2 : -INFINITY;
             uint8_t* stage = smem + L::kStageOff + t * L::kStageBytes;
             const int64_t row0 = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + 128 * (it.m0 + t)
@@ -758,6 +777,82 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
+// Split-KV merge (see scheduler.h): LSE = ln sum_c exp(LSE_c) and
+// O = sum_c exp(LSE_c - LSE) O_c for every split query tile, written as bf16
+// to the broadcast O [B, Lq, H, D] with LSE [B, H, Lq].  One CTA per (split
+// tile, 32-row block, 32-column slice); lane = row, and the 8 warps share the
+// chunks (warp w takes c = w, w + 8, ...), their partial maxima, sums and
+// weighted rows combined through shared memory.
+template <int D>
+__global__ void __launch_bounds__(256) jfa_fwd_merge_kernel(const SplitGroup* groups, const float* o_part,
+                                                            const float* lse_part, uint16_t* o, float* lse, int Lq,
+                                                            int H) {
+    constexpr int kSlices = D / 32;
+    __shared__ float red_m[8][32], red_s[8][32];
+    __shared__ float red_o[8][32][33];
+    const int gi = blockIdx.x / (4 * kSlices), rb = (blockIdx.x / kSlices) % 4, cs = blockIdx.x % kSlices;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+    const int4 g = __ldg(reinterpret_cast<const int4*>(groups) + gi);  // b, slot0, chunks, h | tile << 8
+    const int h = g.w & 0xFF, tile = static_cast<int>(static_cast<uint32_t>(g.w) >> 8);
+    const int row = rb * 32 + lane;
+    const float* lp = lse_part + static_cast<int64_t>(g.y) * 128 + row;
+    float mx = -INFINITY;
+    for (int c = warp; c < g.z; c += 8) mx = fmaxf(mx, lp[c * 128]);
+    red_m[warp][lane] = mx;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) M = fmaxf(M, red_m[w][lane]);
+    float sum = 0.0f;
+    if (M != -INFINITY)
+        for (int c = warp; c < g.z; c += 8) sum += expf(lp[c * 128] - M);
+    red_s[warp][lane] = sum;
+    __syncthreads();
+    float S = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) S += red_s[w][lane];
+    const float L = M == -INFINITY ? -INFINITY : M + logf(S);
+    float acc[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+    if (L != -INFINITY) {
+#pragma unroll 2
+        for (int c = warp; c < g.z; c += 8) {
+            const float wt = expf(lp[c * 128] - L);
+            const float4* src = reinterpret_cast<const float4*>(
+                o_part + (static_cast<int64_t>(g.y + c) * 128 + row) * D + cs * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 v = src[e];
+                acc[4 * e] += wt * v.x;
+                acc[4 * e + 1] += wt * v.y;
+                acc[4 * e + 2] += wt * v.z;
+                acc[4 * e + 3] += wt * v.w;
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) red_o[warp][lane][e] = acc[e];
+    __syncthreads();
+    // Thread t: row t % 32 of the block, columns 4 * (t / 32) .. + 3 of the slice.
+    const int r = threadIdx.x % 32, e0 = 4 * (threadIdx.x / 32);
+    const int q = tile * 128 + rb * 32 + r;
+    if (q < Lq) {
+        float out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += red_o[w][r][e0 + k];
+            out[k] = v;
+        }
+        const int64_t orow = (static_cast<int64_t>(g.x) * Lq + q) * H + h;
+        *reinterpret_cast<uint2*>(o + orow * D + cs * 32 + e0) =
+            make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
+    }
+    if (cs == 0 && warp == 0 && tile * 128 + row < Lq) lse[(static_cast<int64_t>(g.x) * H + h) * Lq + tile * 128 + row] = L;
+}
+
 template <int D, bool kSparse>
 cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     using L = FwdLayout<D>;
@@ -779,6 +874,17 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
 }
 
 }  // namespace
+
+cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, const float* o_part,
+                             const float* lse_part, uint16_t* o, float* lse, int Lq, int H, cudaStream_t s) {
+    if (n_groups <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(n_groups) * 4 * (D / 32);
+    if (D == 128)
+        jfa_fwd_merge_kernel<128><<<grid, 256, 0, s>>>(groups, o_part, lse_part, o, lse, Lq, H);
+    else
+        jfa_fwd_merge_kernel<64><<<grid, 256, 0, s>>>(groups, o_part, lse_part, o, lse, Lq, H);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;

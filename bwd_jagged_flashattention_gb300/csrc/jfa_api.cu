@@ -29,6 +29,12 @@ constexpr size_t kStatusBytes = 256;
 constexpr int kDqGroups = JFA_DQ_GROUPS;
 constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
 
+// Split-KV of long broadcast-Q forward items (scheduler.h); 0 turns it off
+// (for measuring what it gains).
+#ifndef JFA_FWD_SPLIT_KV
+#define JFA_FWD_SPLIT_KV 1
+#endif
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // A schedule region holds the CTA bounds and the items, then (block-sparse
@@ -37,6 +43,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WsLayout {
     size_t fwd_off, bwd_off, fwd_region, bwd_region, delta_off, delta_bytes, dqp_off, dqp_bytes, total;
     size_t sel_off, blocks_off, zero_off;  // offsets inside a region
+    size_t split_off;                      // forward region: split-KV groups (broadcast Q)
+    size_t opart_off, lpart_off;           // split-KV partial O / LSE (broadcast Q; 0 bytes otherwise)
     int64_t max_items, sel_cap;            // sel_cap >= NB * H (NB = key blocks over all sequences)
 };
 
@@ -47,7 +55,8 @@ bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout
     w->sel_off = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
     w->blocks_off = w->sel_off + align_up(static_cast<size_t>(B) * H * sizeof(SparseSel), 256);
     w->zero_off = w->sel_off;
-    w->fwd_region = w->blocks_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(int32_t), 256);
+    w->split_off = w->blocks_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(int32_t), 256);
+    w->fwd_region = w->split_off + (broadcast_q ? align_up(kMaxSplitSlots * sizeof(SplitGroup), 256) : 0);
     w->bwd_region = w->zero_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(ZeroTile), 256);
     w->fwd_off = kStatusBytes;
     w->bwd_off = w->fwd_off + w->fwd_region;
@@ -58,7 +67,9 @@ bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout
     w->dqp_bytes = (broadcast_q && kDqGroups > 1)
                        ? align_up(static_cast<size_t>(kDqGroups) * Lq * H * D * sizeof(float), 256)
                        : 0;
-    w->total = w->dqp_off + w->dqp_bytes;
+    w->opart_off = w->dqp_off + w->dqp_bytes;
+    w->lpart_off = w->opart_off + (broadcast_q ? align_up(static_cast<size_t>(kMaxSplitSlots) * 128 * D * 4, 256) : 0);
+    w->total = w->lpart_off + (broadcast_q ? align_up(static_cast<size_t>(kMaxSplitSlots) * 128 * 4, 256) : 0);
     return true;
 }
 
@@ -90,7 +101,7 @@ DeviceStage& device_stage(int dev) {
 // unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
 int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
                        const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
-                       int64_t* n_zero, jfa_status* st) {
+                       int64_t* n_zero, int64_t* n_split_groups, jfa_status* st) {
     const int64_t max_items = w.max_items;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -104,8 +115,9 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         *st = JFA_ERR_CUDA;
         return -1;
     }
-    const size_t need = mask ? (is_bwd ? w.bwd_region : w.fwd_region)
-                             : kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
+    const bool may_split = JFA_FWD_SPLIT_KV && !is_bwd && !mask && broadcast_q && n_split_groups;
+    const size_t need = (mask || may_split) ? (is_bwd ? w.bwd_region : w.fwd_region)
+                                            : kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
     if (slot.cap < need) {
         if (slot.buf) cudaFreeHost(slot.buf);
         slot.buf = nullptr;
@@ -131,9 +143,11 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         sp.zero = reinterpret_cast<ZeroTile*>(buf + w.zero_off);
         sp.cap = w.sel_cap;
     }
+    SplitSpec split;
+    split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
     const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P,
                                      is_bwd ? kSchedLptZigzag : kSchedLptGreedy, items,
-                                     cta_start, max_items, mask ? &sp : nullptr);
+                                     cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
     if (n < 0) {
         *st = JFA_ERR_WORKSPACE;
         return -1;
@@ -151,11 +165,16 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     if (mask && is_bwd)
         ok = ok && (sp.n_zero == 0 || cudaMemcpyAsync(dst + w.zero_off, buf + w.zero_off, sp.n_zero * sizeof(ZeroTile),
                                                       cudaMemcpyHostToDevice, stream) == cudaSuccess);
+    if (may_split)
+        ok = ok && (split.n_groups == 0 ||
+                    cudaMemcpyAsync(dst + w.split_off, buf + w.split_off, split.n_groups * sizeof(SplitGroup),
+                                    cudaMemcpyHostToDevice, stream) == cudaSuccess);
     if (!ok || cudaEventRecord(slot.ev, stream) != cudaSuccess) {
         *st = JFA_ERR_CUDA;
         return -1;
     }
     if (n_zero) *n_zero = mask ? sp.n_zero : 0;
+    if (n_split_groups) *n_split_groups = may_split ? split.n_groups : 0;
     slot.used = true;
     return n;
 }
@@ -257,7 +276,8 @@ int64_t count_items(const Problem& pr, int is_bwd) {
 // ---------------------------------------------------------------------------
 // Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
 // ---------------------------------------------------------------------------
-enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfZero = 4, kProfKinds = 5 };
+enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfZero = 4, kProfMerge = 5,
+                kProfKinds = 6 };
 
 struct Profiler {
     std::mutex mu;
@@ -338,10 +358,13 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     if (o_rows == 0) return JFA_OK;  // nothing to compute
 
     char* ws = static_cast<char*>(workspace);
-    const int64_t n_items = count_items(pr, 0);
+    // Broadcast Q (split-KV possible): every SM, since splitting can make
+    // more items than the batch has; CTAs left without items exit at once.
+    const int64_t n_items = pr.broadcast_q && !mask ? (int64_t{1} << 30) : count_items(pr, 0);
     const int P = ctas_for(n_items);
+    int64_t n_groups = 0;
     const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w, mask,
-                                     ws + w.fwd_off, s, nullptr, &st);
+                                     ws + w.fwd_off, s, nullptr, &n_groups, &st);
     if (n < 0) return st;
     if (n == 0) return JFA_OK;
 
@@ -363,8 +386,18 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
     p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
-    return timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) == cudaSuccess ? JFA_OK
-                                                                                                : JFA_ERR_CUDA;
+    if (n_groups > 0) {  // split-KV chunks write partials; the merge pass writes their O / LSE
+        p.o_part = reinterpret_cast<float*>(ws + w.opart_off);
+        p.lse_part = reinterpret_cast<float*>(ws + w.lpart_off);
+    }
+    if (timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
+    if (n_groups > 0 && timed_launch(kProfMerge, s, [&] {
+                            return launch_fwd_merge(D, reinterpret_cast<const SplitGroup*>(ws + w.fwd_off + w.split_off),
+                                                    n_groups, p.o_part, p.lse_part, static_cast<uint16_t*>(o), lse,
+                                                    pr.Lq, H, s);
+                        }) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    return JFA_OK;
 }
 
 extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
@@ -441,7 +474,7 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     const int P = ctas_for(n_items);
     int64_t n_zero = 0;
     const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w, mask,
-                                     ws + w.bwd_off, s, &n_zero, &st);
+                                     ws + w.bwd_off, s, &n_zero, nullptr, &st);
     if (n < 0) return st;
     if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
                           return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),

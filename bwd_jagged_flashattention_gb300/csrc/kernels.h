@@ -21,6 +21,8 @@ struct FwdParams {
     float scale_log2;          // softmax scale * log2(e)
     const SparseSel* sel = nullptr;      // block-sparse: selection per (b, h) at b * H + h; null = dense
     const int32_t* sel_blocks = nullptr; // block-sparse: the selected block indices the records point into
+    float* o_part = nullptr;             // split-KV chunks: fp32 O [slot][128][D] (null: no split items)
+    float* lse_part = nullptr;           // split-KV chunks: fp32 LSE [slot][128]
 };
 
 struct BwdParams {
@@ -69,6 +71,9 @@ struct BwdMaps {
 };
 
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s);
+// Split-KV merge of n_groups split query tiles into the broadcast O / LSE.
+cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, const float* o_part,
+                             const float* lse_part, uint16_t* o, float* lse, int Lq, int H, cudaStream_t s);
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
 cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s);

@@ -134,11 +134,59 @@ void group_by_q(WorkItem* items, const int32_t* cta_start, int P, int is_bwd) {
     }
 }
 
+// Split-KV (see scheduler.h): replace every broadcast-Q forward item whose
+// cost exceeds the average per-CTA load by single-tile key chunks of about
+// half that load (at least kMinSplitBlocks blocks), within the slot and item
+// capacities; items are taken in generation order, so the result depends
+// only on the offsets.
+void split_long_items(std::vector<WorkItem>& gen, std::vector<int64_t>& cost, int P, int64_t max_items,
+                      SplitSpec* split) {
+    int64_t total = 0;
+    for (int64_t c : cost) total += c;
+    const int64_t avg = total / P;
+    const int64_t chunk = std::max<int64_t>(kMinSplitBlocks, avg / 2);
+    std::vector<WorkItem> out_items;
+    std::vector<int64_t> out_cost;
+    int64_t budget = max_items - static_cast<int64_t>(gen.size());  // extra items the capacity allows
+    for (size_t i = 0; i < gen.size(); ++i) {
+        const WorkItem& w = gen[i];
+        const int64_t nkv = ceil_div(w.kv_len, kTileRows);
+        const int tile = static_cast<int>((w.packed >> 8) & 0x7FFFFFu);
+        const int tiles = 1 + static_cast<int>(w.packed >> 31);
+        const int64_t chunks = ceil_div(nkv, chunk);
+        if (cost[i] <= avg || chunks < 2 || split->n_slots + tiles * chunks > kMaxSplitSlots ||
+            tiles * chunks - 1 > budget) {
+            out_items.push_back(w);
+            out_cost.push_back(cost[i]);
+            continue;
+        }
+        budget -= tiles * chunks - 1;
+        const int h = static_cast<int>(w.packed & 0xFFu);
+        for (int t = 0; t < tiles; ++t) {
+            SplitGroup& g = split->groups[split->n_groups++];
+            g.b = w.b;
+            g.slot0 = static_cast<int32_t>(split->n_slots);
+            g.n = static_cast<int32_t>(chunks);
+            g.packed = static_cast<uint32_t>(h) | (static_cast<uint32_t>(tile + t) << 8);
+            for (int64_t c = 0; c < chunks; ++c) {
+                const int64_t j0 = c * chunk, j1 = std::min(nkv, j0 + chunk);
+                const int64_t k0 = j0 * kTileRows, k1 = std::min<int64_t>(w.kv_len, j1 * kTileRows);
+                const int32_t slot = static_cast<int32_t>(split->n_slots++);
+                out_items.push_back({-(slot + 1), static_cast<int32_t>(w.kv_start + k0), static_cast<int32_t>(k1 - k0),
+                                     pack_item(h, tile + t, 0)});
+                out_cost.push_back((j1 - j0) + 1);
+            }
+        }
+    }
+    gen.swap(out_items);
+    cost.swap(out_cost);
+}
+
 }  // namespace
 
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
                        int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items,
-                       SparseSpec* sparse) {
+                       SparseSpec* sparse, SplitSpec* split) {
     if (P <= 0 || P > kMaxCtas) return -1;
     if (sparse && causal) return -1;
     // 1. Generate items in (b, h, tile) order, with their costs.
@@ -194,6 +242,9 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         bstart += nkv;
         if (static_cast<int64_t>(gen.size()) > max_items) return -1;
     }
+    if (split) split->n_groups = split->n_slots = 0;
+    if (split && !is_bwd && broadcast_q && !sparse && policy != kSchedNaive && !gen.empty())
+        split_long_items(gen, cost, P, max_items, split);
     const int64_t n = static_cast<int64_t>(gen.size());
 
     // 2. Order: cost-descending, stable (counting sort on the integer cost).
@@ -304,5 +355,20 @@ extern "C" long long jfa_host_build_schedule_sparse(const int32_t* offsets, int 
                                             static_cast<jfa::WorkItem*>(items), cta_start, max_items, &sp);
     counts[0] = sp.n_blocks;
     counts[1] = sp.n_zero;
+    return n;
+}
+
+// Broadcast-Q forward schedule with split-KV (the library's greedy deal);
+// counts[0] = split groups, counts[1] = partial slots.  Returns the item
+// count or -1.
+extern "C" long long jfa_host_build_schedule_split(const int32_t* offsets, int B, int Lq, int H, int P, void* items,
+                                                   int32_t* cta_start, long long max_items, void* groups,
+                                                   long long* counts) {
+    jfa::SplitSpec sp;
+    sp.groups = static_cast<jfa::SplitGroup*>(groups);
+    const long long n = jfa::build_schedule(offsets, B, Lq, H, 1, 0, 0, P, jfa::kSchedLptGreedy,
+                                            static_cast<jfa::WorkItem*>(items), cta_start, max_items, nullptr, &sp);
+    counts[0] = sp.n_groups;
+    counts[1] = sp.n_slots;
     return n;
 }

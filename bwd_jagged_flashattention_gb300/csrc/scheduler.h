@@ -93,6 +93,29 @@ struct SparseSpec {
 // NB = sum_b ceil(len_b / 128).
 int64_t num_kv_blocks(const int32_t* offsets, int B);
 
+// Split-KV for the broadcast-Q forward (load balance under length skew): a
+// query tile of one (sequence, head) whose key loop alone costs more than an
+// average CTA's share of the work is cut into key chunks, each a work item of
+// its own that writes its O (normalised by its own row sums) and its LSE in
+// fp32 to a slot; a merge pass combines each split tile's chunks:
+//     LSE = ln sum_c exp(LSE_c),   O = sum_c exp(LSE_c - LSE) O_c.
+// A chunk item is encoded like a shorter sequence: kv_start / kv_len cover
+// the chunk's keys, the packed field holds (h, query tile, one tile), and
+// b = -(slot + 1) marks it.
+constexpr int kMaxSplitSlots = 512;   // partial (O, LSE) slots in a workspace
+constexpr int kMinSplitBlocks = 4;    // key blocks per chunk, at least
+struct SplitGroup {                   // one split query tile; its chunks own slots [slot0, slot0 + n)
+    int32_t b;
+    int32_t slot0;
+    int32_t n;
+    uint32_t packed;                  // h | query tile << 8
+};
+static_assert(sizeof(SplitGroup) == 16, "16-byte record");
+struct SplitSpec {
+    SplitGroup* groups;               // out: capacity kMaxSplitSlots
+    int64_t n_groups = 0, n_slots = 0;
+};
+
 // Build a schedule.  Writes `n` items into `items` (capacity max_items) and
 // the CSR bounds cta_start[0..P] (CTA p owns items [cta_start[p],
 // cta_start[p+1])).  Returns n, or -1 if a capacity is too small.
@@ -101,9 +124,11 @@ int64_t num_kv_blocks(const int32_t* offsets, int B);
 // blocks only, and sparse->sel / blocks list each pair's selected blocks;
 // backward items exist only for selected key tiles, the others go to
 // sparse->zero.
+// With `split` (broadcast-Q forward without a block-sparse selection):
+// split-KV as above.
 int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd,
                        int P, int policy, WorkItem* items, int32_t* cta_start, int64_t max_items,
-                       SparseSpec* sparse = nullptr);
+                       SparseSpec* sparse = nullptr, SplitSpec* split = nullptr);
 
 // Allocation-free twin of build_schedule with kSchedLptGreedy (same items,
 // order and deal) for callers that cannot allocate: every array comes from

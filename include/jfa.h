@@ -91,6 +91,12 @@ size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D, int broad
  *   o, lse       device outputs (layouts above).
  *   workspace    device scratch of at least jfa_workspace_bytes() bytes.
  *   stream       cudaStream_t (NULL = legacy default stream).
+ * Load balance: the host deals (sequence, head, query-tile) items to one
+ * persistent CTA per SM, longest first.  In broadcast mode a query tile
+ * whose key loop alone costs more than an average CTA's share is split into
+ * key chunks (split-KV); each chunk writes an fp32 partial O and LSE into
+ * the workspace (at most 512 chunks per call) and a merge kernel combines
+ * them (LSE = ln sum_c exp(LSE_c), O = sum_c exp(LSE_c - LSE) O_c).
  */
 jfa_status jfa_fwd(const void *q, const void *k, const void *v, const int32_t *offsets_dev,
                    const int32_t *offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
@@ -191,7 +197,7 @@ jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, c
  * ms[k] and the launch count into launches[k] (either pointer may be NULL),
  * then clears the totals.  Kinds: 0 forward kernel, 1 backward Delta
  * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum, 4 block-sparse
- * zeroing of unselected dK/dV tiles.  The events
+ * zeroing of unselected dK/dV tiles, 5 split-KV merge.  The events
  * are host-owned CUDA events; no device memory is allocated.
  */
 jfa_status jfa_profile_enable(int on);
