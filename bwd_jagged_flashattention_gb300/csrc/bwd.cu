@@ -43,6 +43,13 @@ namespace {
 
 // Tuning knob (compile-time): L2 prefetch of the next item's tiles (measured
 // slower on the ads workload, so off by default).
+// Compute / dQ warpgroups -> MMA hand-offs (p_full, ds_full, dq_empty):
+// 1 = one arrival per warp (lane 0, after the warp's fences and a
+// __syncwarp), 0 = one per thread.  Measured on the ads step: no gain
+// (385.3 vs 382.9 us).
+#ifndef JFA_BWD_WARP_ARRIVE
+#define JFA_BWD_WARP_ARRIVE 0
+#endif
 #ifndef JFA_BWD_PREFETCH
 #define JFA_BWD_PREFETCH 0
 #endif
@@ -674,6 +681,21 @@ __device__ __forceinline__ void bwd_compute_ds(const float* delta, uint32_t s_ad
     }
 }
 
+// Hand-off to the MMA thread after a warpgroup's tcgen05 / shared-memory
+// writes (already fenced for the async proxy where needed): every thread
+// fences, then every thread arrives or, with JFA_BWD_WARP_ARRIVE, lane 0 of
+// each warp once the warp has synchronised.
+constexpr uint32_t kArrivePerWarp = JFA_BWD_WARP_ARRIVE ? 1 : 32;  // arrivals per warp
+__device__ __forceinline__ void handoff_arrive(uint64_t* bar) {
+    tc_fence_before();
+    if (JFA_BWD_WARP_ARRIVE) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    } else {
+        mbar_arrive(bar);
+    }
+}
+
 template <int D>
 __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_t* smem, BwdBars& bars,
                                  uint32_t tmem, int ib, int ie, const AbortState& ab) {
@@ -713,8 +735,7 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                     bwd_compute_p_cols<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, 2 * wg, pkeep);
             }
             if (threadIdx.x == 0) JFA_TRACE_EVENT(32, 0, i, 0);
-            tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            handoff_arrive(&bars.p_full);
             if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
             if (threadIdx.x == 0) JFA_TRACE_EVENT(33, 0, i, 0);
             if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
@@ -737,8 +758,7 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
             }
             fence_proxy_async_smem();
             if (threadIdx.x == 0) JFA_TRACE_EVENT(35, 0, i, 0);
-            tc_fence_before();
-            mbar_arrive(&bars.ds_full);
+            handoff_arrive(&bars.ds_full);
             ++q_cnt;
             ++tile_cnt;
         }
@@ -853,8 +873,7 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_ld32(dq_addr + c * 32, v[c]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
+            handoff_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
             if (issuer) JFA_TRACE_EVENT(42, 4, i, 0);
 #pragma unroll
             for (int sl = 0; sl < D / 16; ++sl) {
@@ -984,11 +1003,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars.do_empty, 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
-        mbar_init(&bars.p_full, 128 * kCW);
-        mbar_init(&bars.ds_full, 128 * kCW);
+        mbar_init(&bars.p_full, 4 * kCW * kArrivePerWarp);
+        mbar_init(&bars.ds_full, 4 * kCW * kArrivePerWarp);
         mbar_init(&bars.ds_empty, 1);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_empty, 128);
+        mbar_init(&bars.dq_empty, 4 * kArrivePerWarp);
         mbar_init(&bars.dkv_full, 1);
         mbar_init(&bars.dv_empty, 128);
         mbar_init(&bars.dk_empty, 128);

@@ -41,6 +41,12 @@ namespace {
 #ifndef JFA_FWD_SLOTS
 #define JFA_FWD_SLOTS 4
 #endif
+// Softmax -> MMA hand-offs (p_full, o_empty): 1 = one arrival per warp
+// (lane 0, after the warp's tcgen05 fences and a __syncwarp), 0 = one per
+// thread.  Measured on the ads step: no gain (137.8 vs 137.2 us).
+#ifndef JFA_FWD_WARP_ARRIVE
+#define JFA_FWD_WARP_ARRIVE 0
+#endif
 #ifndef JFA_FWD_PREFETCH
 #define JFA_FWD_PREFETCH 0
 #endif
@@ -194,6 +200,21 @@ __device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const Fwd
         nx = decode_fwd<kSparse>(p.items[k], p);
     }
     return nx.h == it.h && nx.m0 == it.m0 && nx.nq == it.nq;
+}
+
+// Hand-off from a softmax warpgroup to the MMA thread after its tcgen05
+// stores or loads: every thread fences, then every thread arrives (count
+// 128) or, with JFA_FWD_WARP_ARRIVE, lane 0 of each warp once the warp has
+// synchronised (count 4).
+constexpr uint32_t kHandoffCount = JFA_FWD_WARP_ARRIVE ? 4 : 128;
+__device__ __forceinline__ void handoff_arrive(uint64_t* bar) {
+    tc_fence_before();
+    if (JFA_FWD_WARP_ARRIVE) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    } else {
+        mbar_arrive(bar);
+    }
 }
 
 // Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
@@ -591,8 +612,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             tc_fence_after();
             softmax_block<D, kSparse, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 0);
-            tc_fence_before();
-            mbar_arrive(&bars.p_full[t]);
+            handoff_arrive(&bars.p_full[t]);
         }
         for (; j < nblk; ++j) {  // tail: ragged end and/or causal diagonal
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
@@ -609,8 +629,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             else
                 softmax_block<D, kSparse, true, 1>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
-            tc_fence_before();
-            mbar_arrive(&bars.p_full[t]);
+            handoff_arrive(&bars.p_full[t]);
         }
         // Epilogue: O / l to bf16, LSE = ln(sum exp) of the scaled scores.
         // O leaves TMEM first (freeing it for the next item's PV), then goes
@@ -625,8 +644,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
 #pragma unroll
             for (int oc = 0; oc < D / 32; ++oc) tmem_ld32(o_addr + oc * 32, orr[oc]);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bars.o_empty[t]);  // TMEM O is free: the next item's PV may start
+            handoff_arrive(&bars.o_empty[t]);  // TMEM O is free: the next item's PV may start
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
             if (!kSparse && it.slot >= 0) {  // split-KV chunk: fp32 O and LSE of its keys for the merge pass
                 if (valid) {
@@ -737,9 +755,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars.s_full[t], 1);
-            mbar_init(&bars.p_full[t], 128);
+            mbar_init(&bars.p_full[t], kHandoffCount);
             mbar_init(&bars.o_full[t], 1);
-            mbar_init(&bars.o_empty[t], 128);
+            mbar_init(&bars.o_empty[t], kHandoffCount);
         }
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
