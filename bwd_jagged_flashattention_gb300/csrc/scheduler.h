@@ -94,8 +94,8 @@ struct SparseSpec {
 int64_t num_kv_blocks(const int32_t* offsets, int B);
 
 // Split-KV for the broadcast-Q forward (load balance under length skew): a
-// query tile of one (sequence, head) whose key loop alone costs more than an
-// average CTA's share of the work is cut into key chunks, each a work item of
+// query tile of one (sequence, head) whose key loop alone costs more than
+// 1.5x an average CTA's share of the work is cut into key chunks, each a work item of
 // its own that writes its O (normalised by its own row sums) and its LSE in
 // fp32 to a slot; a merge pass combines each split tile's chunks:
 //     LSE = ln sum_c exp(LSE_c),   O = sum_c exp(LSE_c - LSE) O_c.

@@ -93,7 +93,7 @@ size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D, int broad
  *   stream       cudaStream_t (NULL = legacy default stream).
  * Load balance: the host deals (sequence, head, query-tile) items to one
  * persistent CTA per SM, longest first.  In broadcast mode a query tile
- * whose key loop alone costs more than an average CTA's share is split into
+ * whose key loop alone costs more than 1.5x an average CTA's share is split into
  * key chunks (split-KV); each chunk writes an fp32 partial O and LSE into
  * the workspace (at most 512 chunks per call) and a merge kernel combines
  * them (LSE = ln sum_c exp(LSE_c), O = sum_c exp(LSE_c - LSE) O_c).
