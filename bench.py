@@ -560,6 +560,18 @@ def main():
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev) / args.e2e_steps
+    # The pipelined steps computed what a plain step computes: the last one's copied-back
+    # outputs against a fresh step on the first buffer set (dQ sums with atomics: tolerance).
+    last = host_out[(args.e2e_steps - 1) % 2]
+    step()
+    torch.cuda.synchronize()
+    for n_ in out_names:
+        ref = bufs0[n_].cpu()
+        if n_ == "dq":
+            err = (last[n_].double() - ref.double()).norm() / max(ref.double().norm(), 1e-30)
+            assert err <= 1e-4, f"e2e pipeline: dq differs from a plain step (rel {err})"
+        else:
+            assert torch.equal(last[n_], ref), f"e2e pipeline: {n_} differs from a plain step"
     e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
 
     # Block-sparse: the dense step on the same inputs, timed the same way, for the speedup.
