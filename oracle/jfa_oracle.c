@@ -329,3 +329,256 @@ void jfa_oracle_bwd(const void *q, const void *k, const void *v, const void *dou
     jfa_oracle_bwd_block_sparse(q, k, v, dout, in_bf16, offsets, B, Lq, H, D, broadcast_q, causal, scale, NULL,
                                 dq, dk, dv);
 }
+
+/*
+ * ===========================================================================
+ * MXFP8 variant (the *_mxfp8 entry points below).
+ *
+ * The pages say only that an MXFP8 version of the kernel runs its matmuls in
+ * microscaling precision, quantizes P to FP8 on the fly and keeps the scale
+ * factors in tensor memory (TLX porta l'attenzione jagged su Blackwell oltre
+ * FA4 con un terzo del codice, section "The turning point").  Readings taken:
+ *
+ *   - MXFP8 is the OCP microscaling format: E4M3 elements (1 sign bit, 4
+ *     exponent bits with bias 7, 3 mantissa bits; exponent field 0 encodes
+ *     subnormals m * 2^-9; S.1111.111 is NaN; no infinities; largest finite
+ *     magnitude 448), one E8M0 scale 2^(code - 127) per block of 32
+ *     consecutive elements along the contraction dimension.  The block scale
+ *     is 2^X with X = floor(log2(amax)) - 8, 8 being the exponent of E4M3's
+ *     top binade, so the block's largest magnitude lands in [256, 512);
+ *     elements round to nearest (ties to even mantissa) and magnitudes above
+ *     448 saturate to 448.  An all-zero block, or one holding no element,
+ *     gets code 0.
+ *   - The product in MXFP8 is P V; Q K^T stays bf16.
+ *   - V comes quantized.  Blocks of 32 keys are counted from each sequence's
+ *     start, per head and per column d; the scales are stored per 128-key
+ *     block as v_scale[((block_start[b] + n) * H + h) * D + d][c] for chunk c
+ *     (keys 128 n + 32 c .. + 31 of sequence b), with block_start as in the
+ *     block-sparse variant.
+ *   - P is quantized in the log2 domain: with x_ij = scale * s_ij * log2(e),
+ *     the 32-key chunk c of row i (chunks counted from the sequence start)
+ *     has X = floor(max_{j in c} x_ij) - 8, and
+ *         pq_ij = 2^X * E4M3(2^(x_ij - X)).
+ *     This is the MX rule applied to the weights 2^x_ij; because X is an
+ *     integer it does not depend on where the running maximum of an online
+ *     softmax stood, so a kernel that keeps that maximum at an integer
+ *     reaches the same pq.
+ *   - O_i = sum_j pq_ij v_j / sum_j 2^x_ij: the normaliser is the row sum of
+ *     the unquantized weights, and LSE is the one of the bf16 forward.
+ *
+ * Slack (optional output of jfa_oracle_fwd_mxfp8): a kernel computes x_ij in
+ * fp32, so where the oracle's fp64 x_ij sits within 1e-4 of a decision
+ * boundary (a chunk maximum near an integer, or 2^(x - X) near the midpoint
+ * of two E4M3 values) the kernel may legitimately take the other side.  For
+ * every output element the slack is sum_j |pq'_ij - pq_ij| |v_jd| / sum_j
+ * 2^x_ij over the keys whose decision is that close, pq' the other side's
+ * value.  It is zero almost everywhere.
+ * ===========================================================================
+ */
+
+double jfa_oracle_e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return s ? -mag : mag;
+}
+
+/* Nearest E4M3 code to a finite x (ties to the even mantissa, magnitudes of
+ * 448 and above give 448); the sign of x is kept, also when it rounds to 0. */
+uint8_t jfa_oracle_e4m3_encode(double x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    int ex;
+    frexp(a, &ex); /* a in [2^(ex-1), 2^ex) */
+    /* spacing of E4M3 values around a: 2^-9 below 2^-6, else 2^(ex-1-3) */
+    const int q = a < ldexp(1.0, -6) ? -9 : ex - 4;
+    const double r = ldexp(nearbyint(ldexp(a, -q)), q); /* default rounding: to nearest, ties to even */
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -6)) return sign | (uint8_t)ldexp(r, 9); /* subnormal: m * 2^-9 */
+    int e2;
+    const double f = frexp(r, &e2); /* r = 2f * 2^(e2-1), 2f in [1, 2) */
+    return sign | (uint8_t)((e2 - 1 + 7) << 3) | (uint8_t)((2.0 * f - 1.0) * 8.0);
+}
+
+void jfa_oracle_e4m3_encode_array(const double *x, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = jfa_oracle_e4m3_encode(x[i]);
+}
+
+void jfa_oracle_e4m3_value_array(const uint8_t *c, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = jfa_oracle_e4m3_value(c[i]);
+}
+
+/* Shared exponent X of an MX block with largest magnitude amax (see above),
+ * within the E8M0 code range; -127 (code 0) for an all-zero block. */
+int jfa_oracle_mx_exponent(double amax) {
+    if (!(amax > 0.0)) return -127;
+    int ex;
+    frexp(amax, &ex); /* floor(log2(amax)) = ex - 1 */
+    int X = ex - 1 - 8;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    return X;
+}
+
+/* block_start[b] for b = 0..B (always computed; the caller frees it). */
+static int64_t *all_block_starts(const int32_t *offsets, int B) {
+    int64_t *bs = (int64_t *)malloc(sizeof(int64_t) * ((size_t)B + 1));
+    bs[0] = 0;
+    for (int b = 0; b < B; ++b) bs[b + 1] = bs[b] + (offsets[b + 1] - offsets[b] + 127) / 128;
+    return bs;
+}
+
+void jfa_oracle_quantize_v_mxfp8(const uint16_t *v, const int32_t *offsets, int B, int H, int D, uint8_t *v8,
+                                 uint8_t *v_scale) {
+    int64_t *bstart = all_block_starts(offsets, B);
+    for (int b = 0; b < B; ++b) {
+        const int Lk = offsets[b + 1] - offsets[b];
+        for (int n = 0; 128 * n < Lk; ++n)
+            for (int h = 0; h < H; ++h)
+                for (int d = 0; d < D; ++d)
+                    for (int c = 0; c < 4; ++c) {
+                        const int j0 = 128 * n + 32 * c, j1 = j0 + 32 < Lk ? j0 + 32 : Lk;
+                        double amax = 0.0;
+                        for (int j = j0; j < j1; ++j) {
+                            const double a = fabs(widen_bf16(v[(((int64_t)offsets[b] + j) * H + h) * D + d]));
+                            if (a > amax) amax = a;
+                        }
+                        const int X = j0 < j1 ? jfa_oracle_mx_exponent(amax) : -127;
+                        for (int j = j0; j < j1; ++j) {
+                            const int64_t e = (((int64_t)offsets[b] + j) * H + h) * D + d;
+                            v8[e] = jfa_oracle_e4m3_encode(ldexp(widen_bf16(v[e]), -X));
+                        }
+                        v_scale[(((bstart[b] + n) * H + h) * (int64_t)D + d) * 4 + c] = (uint8_t)(X + 127);
+                    }
+    }
+    free(bstart);
+}
+
+/* Distance from a decision boundary within which the slack counts the other
+ * side (in log2 units for a chunk maximum, relative for a rounding input). */
+static const double kMxEpsFloor = 1e-4, kMxEpsRound = 1e-4;
+static const double kLog2e = 1.4426950408889634074;
+
+/* Quantized weights of one row.  x[0..n) are log2-domain logits (-inf for
+ * hidden keys); chunks of 32 start at index 0.  pq[j] = 2^X E4M3(2^(x_j - X))
+ * with X = floor(max of x over the chunk) - 8, 0 for hidden keys.  With
+ * slack != NULL, slack[j] = |pq'_j - pq_j| for keys whose rounding or chunk
+ * exponent lies within the boundary distance above (the largest such change),
+ * else 0. */
+void jfa_oracle_mx_quantize_p(const double *x, int n, double *pq, double *slack) {
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int c1 = c0 + 32 < n ? c0 + 32 : n;
+        double mx = -INFINITY;
+        for (int j = c0; j < c1; ++j)
+            if (x[j] > mx) mx = x[j];
+        if (mx == -INFINITY) {
+            for (int j = c0; j < c1; ++j) {
+                pq[j] = 0.0;
+                if (slack) slack[j] = 0.0;
+            }
+            continue;
+        }
+        const double f = floor(mx);
+        const int X = (int)f - 8;
+        int X_alt = X;
+        if (mx - f < kMxEpsFloor) X_alt = X - 1;
+        else if (f + 1.0 - mx < kMxEpsFloor) X_alt = X + 1;
+        for (int j = c0; j < c1; ++j) {
+            if (x[j] == -INFINITY) {
+                pq[j] = 0.0;
+                if (slack) slack[j] = 0.0;
+                continue;
+            }
+            const double y = exp2(x[j] - X);
+            const double val = ldexp(jfa_oracle_e4m3_value(jfa_oracle_e4m3_encode(y)), X);
+            pq[j] = val;
+            if (!slack) continue;
+            double sl = 0.0;
+            for (int k = -1; k <= 1; k += 2)
+                sl = fmax(sl, fabs(ldexp(jfa_oracle_e4m3_value(jfa_oracle_e4m3_encode(y * (1.0 + k * kMxEpsRound))), X) - val));
+            if (X_alt != X) {
+                const double ya = exp2(x[j] - X_alt);
+                for (int k = -1; k <= 1; ++k)
+                    sl = fmax(sl, fabs(ldexp(jfa_oracle_e4m3_value(jfa_oracle_e4m3_encode(ya * (1.0 + k * kMxEpsRound))),
+                                             X_alt) - val));
+            }
+            slack[j] = sl;
+        }
+    }
+}
+
+void jfa_oracle_fwd_mxfp8(const void *q, const void *k, const uint8_t *v8, const uint8_t *v_scale, int in_bf16,
+                          const int32_t *offsets, int B, int Lq, int H, int D, int broadcast_q, int causal,
+                          double scale, double *o, double *lse, double *o_slack) {
+    int64_t *bstart = all_block_starts(offsets, B);
+    const int N = B > 0 ? offsets[B] : 0;
+    const int64_t pairs = (int64_t)B * H;
+#pragma omp parallel
+    {
+        double *qi = (double *)malloc(sizeof(double) * D);
+        double *kmat = NULL, *vmat = NULL, *s = NULL, *x = NULL, *pq = NULL, *sl = NULL;
+        int cap = 0;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < pairs; ++bh) {
+            const int b = (int)(bh / H), h = (int)(bh % H);
+            const int Lk = offsets[b + 1] - offsets[b];
+            const int Lqb = broadcast_q ? Lq : Lk;
+            if (Lk > cap) {
+                cap = Lk;
+                kmat = (double *)realloc(kmat, sizeof(double) * (size_t)cap * D);
+                vmat = (double *)realloc(vmat, sizeof(double) * (size_t)cap * D);
+                s = (double *)realloc(s, sizeof(double) * (size_t)cap);
+                x = (double *)realloc(x, sizeof(double) * (size_t)cap);
+                pq = (double *)realloc(pq, sizeof(double) * (size_t)cap);
+                sl = (double *)realloc(sl, sizeof(double) * (size_t)cap);
+            }
+            for (int j = 0; j < Lk; ++j) {
+                const int64_t row = (int64_t)offsets[b] + j;
+                load_row(kmat + (int64_t)j * D, k, row, h, H, D, in_bf16);
+                for (int d = 0; d < D; ++d) {
+                    const uint8_t code =
+                        v_scale[(((bstart[b] + j / 128) * H + h) * (int64_t)D + d) * 4 + (j % 128) / 32];
+                    vmat[(int64_t)j * D + d] = ldexp(jfa_oracle_e4m3_value(v8[(row * H + h) * D + d]), code - 127);
+                }
+            }
+            for (int i = 0; i < Lqb; ++i) {
+                load_row(qi, q, q_row(offsets, b, i, broadcast_q), h, H, D, in_bf16);
+                scores(s, qi, kmat, Lk, D, i, causal, scale, NULL, 0);
+                const double L = log_sum_exp(s, Lk);
+                if (lse) lse[lse_index(offsets, b, h, i, Lq, H, N, broadcast_q)] = L;
+                const int64_t orow = (o_row(offsets, b, i, Lq, broadcast_q) * H + h) * (int64_t)D;
+                if (o) memset(o + orow, 0, sizeof(double) * D);
+                if (o_slack) memset(o_slack + orow, 0, sizeof(double) * D);
+                if (L == -INFINITY || (!o && !o_slack)) continue;
+                /* log2-domain logits, shifted by an integer so that 2^x stays in range */
+                double R = -INFINITY;
+                for (int j = 0; j < Lk; ++j) {
+                    x[j] = s[j] * kLog2e;
+                    if (x[j] > R) R = x[j];
+                }
+                R = floor(R);
+                double den = 0.0;
+                for (int j = 0; j < Lk; ++j) {
+                    x[j] -= R;
+                    den += exp2(x[j]);
+                }
+                jfa_oracle_mx_quantize_p(x, Lk, pq, o_slack ? sl : NULL);
+                for (int j = 0; j < Lk; ++j)
+                    for (int d = 0; d < D; ++d) {
+                        const double vv = vmat[(int64_t)j * D + d];
+                        if (o) o[orow + d] += pq[j] * vv / den;
+                        if (o_slack) o_slack[orow + d] += sl[j] * fabs(vv) / den;
+                    }
+            }
+        }
+        free(qi);
+        free(kmat);
+        free(vmat);
+        free(s);
+        free(x);
+        free(pq);
+        free(sl);
+    }
+    free(bstart);
+}
