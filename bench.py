@@ -356,6 +356,141 @@ def run_reference(args, world, rank):
 # ----------------------------------------------------------------------------
 # The GPU arm
 # ----------------------------------------------------------------------------
+def run_mxfp8(args, world, rank):
+    """The MXFP8 forward (P V in block-scaled E4M3, Q K^T bf16) on the workload's forward, V quantized once
+    before timing (the forward's input, resident like the bf16 forward's bf16 V); the bf16 forward on the same
+    inputs and the quantizer are timed beside it.  Not the headline line."""
+    import bwd_jagged_flashattention_gb300 as jfa
+    import oracle
+    jfa.lib()
+    dev = torch.device("cuda", 0 if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    x = jfa_inputs.make(args.workload, backward=False)
+    if args.batch:
+        x = first_sequences(x, args.batch)
+    acc = accounting(x)
+    B, Lq, H, D, N = x["B"], x["Lq"], x["H"], x["D"], x["N"]
+    bq, causal = x["broadcast_q"], x["causal"]
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    off_h, off_d = x["offsets"], x["offsets"].to(dev)
+    o = torch.empty((B, Lq, H, D) if bq else (N, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Lq) if bq else (H, N), dtype=torch.float32, device=dev)
+    ws = jfa.new_workspace(B, N, Lq if bq else 0, H, D, bq, causal, dev)
+    v8, vs = jfa.quantize_v_mxfp8(v, off_d, offsets_host=off_h, workspace=ws)
+    stream = torch.cuda.current_stream(dev)
+
+    def mx_step(q_=q, k_=k, v8_=v8, vs_=vs, off_=off_d, o_=o, lse_=lse):
+        jfa.fwd_mxfp8(q_, k_, v8_, vs_, off_, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h,
+                      workspace=ws, out=o_, lse=lse_)
+
+    def bf16_step():
+        jfa.fwd(q, k, v, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h, workspace=ws,
+                out=o, lse=lse)
+
+    def quant_step():
+        jfa.quantize_v_mxfp8(v, off_d, offsets_host=off_h, workspace=ws, v8=v8, v_scale=vs)
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        jfa.profile_enable(True)
+        jfa.profile_read()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        prof = jfa.profile_read()
+        jfa.profile_enable(False)
+        return max_over_ranks(world, a.elapsed_time(b), dev) / n, prof
+
+    sampler = ClockSampler(gpu_smi_id(dev))
+    sampler.start()
+    sampler.mark(0)
+    ms, prof = timed(mx_step, args.steps)
+    sampler.mark(1)
+    clocks = sampler.stop()
+    assert jfa.device_status(ws) == 0, "kernel status word reports a timeout"
+    bf16_ms, bf16_prof = timed(bf16_step, min(args.steps, 200))
+    quant_ms, quant_prof = timed(quant_step, min(args.steps, 200))
+    value = world * acc["flops_fwd"] / (ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    # half the FLOPs (Q K^T) run at the bf16 rate, half (P V) at the E4M3 rate, twice the bf16 one
+    # (2.25 vs 4.5 PFLOP/s dense nominal): the mix's peak is 4/3 of the bf16 peak.
+    peak_mix = peaks["bf16_tflops"] * 4.0 / 3.0
+    fwd_ms, nf = prof["fwd"]
+    fwd_avg = fwd_ms / max(nf, 1)
+    v_bytes = N * H * D + N * H * D // 32
+    bytes_fwd = acc["bytes_fwd"] - 2 * N * H * D + v_bytes
+    achieved = acc["flops_fwd"] / (fwd_avg * 1e-3) / 1e12
+    traffic = load_traffic().get("fwd_mxfp8")
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak_mix, "unit": "TFLOP/s", "frac": achieved / peak_mix,
+            "traffic": traffic, "kernel": "jfa_fwd_kernel<D, dense, mxfp8>", "peak_source": peaks["source"],
+            "peak_note": "4/3 x bf16 peak: half the FLOPs bf16 (Q K^T), half E4M3 at twice the rate (P V)",
+            "algorithmic_per_launch": acc["flops_fwd"], "algorithmic_bytes_per_launch": bytes_fwd}
+    # End to end: inputs (Q, K, MXFP8 V and its scales, offsets) from pinned host memory, the forward, the
+    # outputs (O, LSE) back to pinned host memory, every step.
+    host_in = {"q": x["q"].pin_memory(), "k": x["k"].pin_memory(), "v8": v8.cpu().pin_memory(),
+               "vs": vs.cpu().pin_memory(), "off": off_h.pin_memory()}
+    dev_in = {n_: torch.empty_like(t_, device=dev) for n_, t_ in host_in.items()}
+    host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
+    h2d = sum(t_.numel() * t_.element_size() for t_ in host_in.values())
+    d2h = sum(t_.numel() * t_.element_size() for t_ in host_out.values())
+
+    def e2e_step():
+        for n_, t_ in host_in.items():
+            dev_in[n_].copy_(t_, non_blocking=True)
+        mx_step(dev_in["q"], dev_in["k"], dev_in["v8"], dev_in["vs"], dev_in["off"])
+        host_out["o"].copy_(o, non_blocking=True)
+        host_out["lse"].copy_(lse, non_blocking=True)
+
+    e2e_ms, _ = timed(e2e_step, args.e2e_steps)
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        nseq, t_cpu = 1, 0.0
+        while True:  # grow the sample until the oracle takes a few seconds
+            sub = first_sequences(x, nseq)
+            r8, rs = oracle.quantize_v_mxfp8(sub["v"], sub["offsets"])
+            t0 = time.perf_counter()
+            oracle.fwd_mxfp8(sub["q"], sub["k"], r8, rs, sub["offsets"], Lq, bq, causal, x["scale"])
+            t_cpu = time.perf_counter() - t0
+            if t_cpu > 3.0 or nseq >= B:
+                break
+            nseq = min(B, nseq * 4)
+        cpu = {"value": accounting(sub)["flops_fwd"] / t_cpu / 1e12, "unit": "TFLOPS",
+               "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"oracle fwd_mxfp8 on the first {nseq} sequences ({t_cpu:.1f} s)"}
+    line = {
+        "metric": f"fwd TFLOPS (MXFP8 P V, bf16 Q K^T, 1 GB300) on {args.workload}",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (P V, E8M0 scales) + bf16 (Q K^T)", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload) + "; forward only, V in MXFP8",
+                   "B": B, "Lq": Lq, "H": H, "D": D, "N": N, "pairs": acc["pairs"],
+                   "l2": "no flush: Q, K, V inputs exceed the 129 MB L2" if 3 * N * H * D > 129e6 else "no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "bf16_fwd": {"ms_per_step": bf16_ms, "tflops": world * acc["flops_fwd"] / (bf16_ms * 1e-3) / 1e12,
+                     "speedup_of_mxfp8": bf16_ms / ms},
+        "quantize_v": {"ms": quant_prof["quant_v"][0] / max(quant_prof["quant_v"][1], 1),
+                       "algorithmic_bytes": 2 * N * H * D + v_bytes},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * acc["flops_fwd"] / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(prof["fwd"][1] + prof["fwd_merge"][1]),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -374,10 +509,16 @@ def main():
     ap.add_argument("--block-sparse", type=float, default=None, metavar="RATIO",
                     help="block-sparse variant: each (128-key block, head) selected with this probability "
                          "(seeded); also times the dense step on the same inputs (not a bench line)")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="MXFP8 variant of the forward (P V in E4M3 with E8M0 scales), forward only, with the bf16 "
+                         "forward timed beside it (not the headline line)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.mxfp8:
+        assert args.warmup >= 3, "at least 3 warm-up steps"
+        return run_mxfp8(args, world, rank)
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     import bwd_jagged_flashattention_gb300 as jfa

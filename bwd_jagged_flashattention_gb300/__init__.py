@@ -29,7 +29,8 @@ JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUD
 # Every symbol include/jfa.h and include/jfa_selftest.h declare.
 EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
             "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma", "jfa_fwd_static_scratch",
-            "jfa_fwd_block_sparse", "jfa_bwd_block_sparse", "jfa_num_kv_blocks")
+            "jfa_fwd_block_sparse", "jfa_bwd_block_sparse", "jfa_num_kv_blocks", "jfa_fwd_mxfp8",
+            "jfa_quantize_v_mxfp8")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,11 @@ def lib() -> ctypes.CDLL:
                 L.jfa_bwd_block_sparse.restype = ci
                 L.jfa_num_kv_blocks.argtypes = [vp, ci]
                 L.jfa_num_kv_blocks.restype = ctypes.c_int64
+            if hasattr(L, "jfa_fwd_mxfp8"):  # (absent only from builds that predate it)
+                L.jfa_fwd_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp, sz, vp]
+                L.jfa_fwd_mxfp8.restype = ci
+                L.jfa_quantize_v_mxfp8.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp, vp, sz, vp]
+                L.jfa_quantize_v_mxfp8.restype = ci
             L.jfa_device_status.argtypes = [vp, vp]
             L.jfa_device_status.restype = ci
             L.jfa_status_string.argtypes = [ci]
@@ -259,6 +265,52 @@ def bwd_block_sparse(q, k, v, o, lse, do, offsets, kv_block_mask, broadcast_q: b
     return dq, dk, dv
 
 
+def quantize_v_mxfp8(v, offsets, offsets_host=None, workspace=None, v8=None, v_scale=None):
+    """MXFP8 V for fwd_mxfp8: E4M3 codes (uint8 [N,H,D]) and E8M0 scales (uint8 [NB,H,D,4]) of bf16 v."""
+    assert v.is_cuda and v.dtype == torch.bfloat16 and offsets is not None and offsets.is_cuda
+    N, H, D = v.shape
+    offsets_host = _host_offsets(offsets, offsets_host)
+    B = offsets_host.numel() - 1
+    nb = num_kv_blocks(offsets_host)
+    v8 = torch.empty((N, H, D), dtype=torch.uint8, device=v.device) if v8 is None else v8
+    v_scale = torch.empty((nb, H, D, 4), dtype=torch.uint8, device=v.device) if v_scale is None else v_scale
+    if workspace is None:
+        workspace = torch.empty(256 + 4 * (B + 1), dtype=torch.uint8, device=v.device)
+    st = lib().jfa_quantize_v_mxfp8(_ptr(v.contiguous()), _ptr(offsets), ctypes.c_void_p(offsets_host.data_ptr()),
+                                    B, H, D, _ptr(v8), _ptr(v_scale), _ptr(workspace), workspace.numel(),
+                                    _stream(v.device))
+    _check(st, "jfa_quantize_v_mxfp8")
+    return v8, v_scale
+
+
+def fwd_mxfp8(q, k, v8, v_scale, offsets, broadcast_q: bool = True, causal: bool = False,
+              scale: float | None = None, offsets_host=None, workspace=None, out=None, lse=None):
+    """MXFP8 forward: O (bf16) and LSE (fp32) with P V in MXFP8; v8 / v_scale from quantize_v_mxfp8."""
+    assert q.is_cuda and q.dtype == torch.bfloat16 and k.dtype == torch.bfloat16 and v8.dtype == torch.uint8
+    H, D = k.shape[1], k.shape[2]
+    offsets_host = _host_offsets(offsets, offsets_host)
+    B = offsets_host.numel() - 1
+    N = int(offsets_host[-1]) if B > 0 else 0
+    nb = num_kv_blocks(offsets_host)
+    if tuple(v8.shape) != (N, H, D) or tuple(v_scale.shape) != (nb, H, D, 4) or v_scale.dtype != torch.uint8:
+        raise ValueError(f"v8 must be uint8 [{N}, {H}, {D}] and v_scale uint8 [{nb}, {H}, {D}, 4]")
+    Lq = q.shape[0] if broadcast_q else 0
+    out = torch.empty((B, Lq, H, D) if broadcast_q else (N, H, D), dtype=torch.bfloat16,
+                      device=q.device) if out is None else out
+    lse = torch.empty((B, H, Lq) if broadcast_q else (H, N), dtype=torch.float32,
+                      device=q.device) if lse is None else lse
+    if workspace is None:
+        workspace = new_workspace(B, N, Lq, H, D, broadcast_q, causal, q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    offsets_dev = offsets if (offsets is not None and offsets.is_cuda) else None
+    st = lib().jfa_fwd_mxfp8(_ptr(q.contiguous()), _ptr(k.contiguous()), _ptr(v8.contiguous()),
+                             _ptr(v_scale.contiguous()), _ptr(offsets_dev), ctypes.c_void_p(offsets_host.data_ptr()),
+                             B, Lq, H, D, int(broadcast_q), int(causal), sc, _ptr(out), _ptr(lse), _ptr(workspace),
+                             workspace.numel(), _stream(q.device))
+    _check(st, "jfa_fwd_mxfp8")
+    return out, lse
+
+
 def device_status(workspace, device=None) -> int:
     """Synchronises the current stream and returns (and clears) the kernels' status word."""
     device = workspace.device if device is None else device
@@ -269,7 +321,7 @@ def profile_enable(on: bool = True) -> None:
     _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
 
 
-PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles", "fwd_merge")
+PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles", "fwd_merge", "quant_v")
 
 
 def profile_read() -> dict:

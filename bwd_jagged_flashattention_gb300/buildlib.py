@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "libjfa.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["jfa_api.cu", "fwd.cu", "bwd.cu", "host_util.cu", "selftest.cu", "scheduler.cpp", "noalloc.cu"]
+SOURCES = ["jfa_api.cu", "fwd.cu", "bwd.cu", "mxfp8.cu", "host_util.cu", "selftest.cu", "scheduler.cpp", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "kernels.h", "scheduler.h", "host_util.h", "trace.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -20,6 +20,18 @@
 // (otherwise the stale max is kept; P stays <= 256, exact after the final
 // division by l).  The KV loop is peeled into an unmasked bulk pass and a
 // masked tail (section "Optimizations layered on top", "Loop peeling").
+//
+// MXFP8 variant (kMx; TLX porta l'attenzione jagged su Blackwell oltre FA4
+// con un terzo del codice, section "The turning point": P quantized to FP8
+// on the fly, scale factors in tensor memory): V arrives as E4M3 with one
+// E8M0 scale per 32 keys and column, and the PV product is block-scaled
+// E4M3 (tcgen05 kind::mxf8f6f4).  The softmax keeps the running max at an
+// integer (log2 domain), gives every 32-key chunk of its row the exponent
+// X = floor(chunk max) - 8, writes P / 2^X as E4M3 over the first 32
+// columns of S and the four chunk exponents next to it (column 32 + warp),
+// plus its lane quarter's copy of the block's V scales (columns 64..).
+// Q K^T stays bf16: with S0 | S1 | O0 | O1 filling TMEM at D = 128 there is
+// no column left for its scale factors while both S tiles are live.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -268,6 +280,22 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
         if (kk < ksteps) mma_ts(d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
 }
 
+// TMEM columns (from a tile's S base) of the MXFP8 product's scale factors:
+// P's chunk exponents, then this block's V scales (D / 32 columns).
+constexpr uint32_t kSfaCol = 32, kSfbCol = 64;
+
+// O(tmem) (+)= P(tmem, E4M3) V(smem, E4M3), block-scaled: four K=32 steps,
+// step c using byte c of the scale words (keys 32c .. 32c+31).  V is
+// MN-major with D-byte rows (128-byte swizzle at D=128, 64-byte at D=64);
+// one step covers 32 rows.
+template <int D>
+__device__ __forceinline__ void issue_pv_mx(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        mma_ts_mx(d_tmem, p_tmem + c * 8, v_desc + c * (32 * D / 16), idesc_mxf8_e4m3(128, D, 1, c, c),
+                  p_tmem + kSfaCol, p_tmem + kSfbCol, (acc | c) != 0);
+}
+
 // Keys of KV block j the products cover: 128, or for a ragged last block the
 // remaining keys rounded up to 16 (the MMA's N granularity).
 __device__ __forceinline__ uint32_t block_keys(int Lk, int j) {
@@ -307,7 +335,7 @@ __device__ __forceinline__ void prefetch_next_block(PrefetchCursor& c, const Fwd
 // ---------------------------------------------------------------------------
 // TMA producer (one thread).
 // ---------------------------------------------------------------------------
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kMx>
 __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CUtensorMap* mk,
                              const CUtensorMap* mv, uint8_t* smem, FwdBars& bars, int ib, int ie,
                              const AbortState& ab) {
@@ -342,6 +370,14 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = ring % L::kSlots;
                 if (!mbar_wait(&bars.kv_empty[slot], ((ring / L::kSlots) & 1) ^ 1, ab)) goto done;
+                if (kMx && kv) {  // E4M3 V: one box of 128 rows x D bytes
+                    mbar_arrive_expect_tx(&bars.kv_full[slot], 128 * D);
+                    tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes, mv, &bars.kv_full[slot], it.h * D,
+                                it.kv_start + 128 * j);
+                    JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
+                    ++ring;
+                    continue;
+                }
                 mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
 #pragma unroll
                 for (int s = 0; s < L::kSlabs; ++s)
@@ -366,13 +402,14 @@ done:
 //   S0=Q0K0, S1=Q1K0, then for each block j: O0+=P0Vj, S0=Q0K(j+1),
 //   O1+=P1Vj, S1=Q1K(j+1).
 // ---------------------------------------------------------------------------
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kMx>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
     const uint64_t q_desc = kmajor_desc(smem_u32(smem + L::kQOff));
     const uint64_t k_desc = kmajor_desc(smem_u32(smem + L::kRingOff));
-    const uint64_t v_desc = mnmajor_desc(smem_u32(smem + L::kRingOff));
+    const uint64_t v_desc = kMx ? smem_desc_swz(smem_u32(smem + L::kRingOff), 16384, 8 * D, D == 128 ? 2u : 4u)
+                                : mnmajor_desc(smem_u32(smem + L::kRingOff));
     constexpr uint64_t kTileUnits = L::kTileBytes / 16;  // descriptor step between tiles
     uint32_t ring = 0, q_ph = 0;
     uint32_t p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
@@ -431,8 +468,11 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 p_ph[t] ^= 1;
                 JFA_TRACE_EVENT(15, 9, t, j);
                 tc_fence_after();
-                issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0,
-                            static_cast<int>(block_keys(it.Lk_trim, j) / 16));
+                if (kMx)
+                    issue_pv_mx<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                else
+                    issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0,
+                                static_cast<int>(block_keys(it.Lk_trim, j) / 16));
                 JFA_TRACE_EVENT(16, 9, t, j);
                 if (j == it.nblk[t] - 1) mma_commit(&bars.o_full[t]);
                 if (j + 1 < it.nblk[t]) {
@@ -568,7 +608,115 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
     tmem_st_wait();
 }
 
-template <int D, bool kSparse>
+// MXFP8 block: the same online softmax with an integer running max, then
+// per 32-key chunk c the exponent X_c = floor(max_c(x) - m) - 8 (x the
+// log2-domain logit, m the running max; clamped to E8M0's normal range) and
+// the weights 2^(x - m - X_c) rounded to E4M3 (in [0, 512), saturating at
+// 448).  Relative to the integer m, X_c + m = floor(max_c(x)) - 8 whatever m
+// is, so the quantized weights do not depend on the online schedule.  The row
+// sum takes the unquantized weights, sum_c 2^X_c sum_{j in c} 2^(x_j - m - X_c).
+// vsc: this lane's words of the block's V scales (column 32 w + lane of
+// word w), copied into its lane quarter of the scale columns.
+template <int D, bool kMask>
+__device__ __forceinline__ void softmax_block_mx(const FwdParams& p, const FwdItem& it, int j, int qpos, int wq,
+                                                 uint32_t s_addr, uint32_t o_addr, const uint32_t (&vsc)[D / 32],
+                                                 float& m_use, float& l) {
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
+    tmem_ld_wait();
+    if (kMask) {
+        const int kbase = 128 * j;
+        int nvis = it.Lk - kbase;
+        if (p.causal) nvis = min(nvis, qpos - kbase + 1);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (c * 32 + i >= nvis) sr[c][i] = __float_as_uint(-INFINITY);
+    }
+    float mxc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float a = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
+        float b = fmaxf(__uint_as_float(sr[c][16]), __uint_as_float(sr[c][17]));
+#pragma unroll
+        for (int i = 2; i < 16; i += 2) {
+            a = fmax3(a, __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+            b = fmax3(b, __uint_as_float(sr[c][16 + i]), __uint_as_float(sr[c][17 + i]));
+        }
+        mxc[c] = fmaxf(a, b);
+    }
+    const float mx = fmaxf(fmaxf(mxc[0], mxc[1]), fmaxf(mxc[2], mxc[3]));
+    const float m_new = fmaxf(m_use, mx * p.scale_log2);
+    float corr = 1.0f;
+    bool resc = false;
+    if (j == 0) {
+        m_use = ceilf(m_new);
+    } else if (m_new > m_use + kRescaleLog2) {
+        const float m_int = ceilf(m_new);
+        corr = ex2_approx(m_use - m_int);
+        m_use = m_int;
+        resc = true;
+    }
+    const float base = m_use == -INFINITY ? 0.0f : m_use;
+    uint32_t sfa = 0;
+    float rs = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float xm = fmaf(mxc[c], p.scale_log2, -base);
+        const int e = xm == -INFINITY ? -126 : max(-126, min(127, static_cast<int>(floorf(xm)) - 8));
+        const float cb = base + static_cast<float>(e);
+        float r0 = 0.0f, r1 = 0.0f;
+        uint32_t pk[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            float x0, x1, x2, x3;
+            ffma2(x0, x1, __uint_as_float(sr[c][4 * w]), __uint_as_float(sr[c][4 * w + 1]), p.scale_log2,
+                  p.scale_log2, -cb, -cb);
+            ffma2(x2, x3, __uint_as_float(sr[c][4 * w + 2]), __uint_as_float(sr[c][4 * w + 3]), p.scale_log2,
+                  p.scale_log2, -cb, -cb);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            fadd2(r0, r1, r0, r1, p0, p1);
+            fadd2(r0, r1, r0, r1, p2, p3);
+            pk[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+        }
+        tmem_st8(s_addr + c * 8, pk);
+        rs += (r0 + r1) * exp2i(e);
+        sfa |= static_cast<uint32_t>(e + 127) << (8 * c);
+    }
+    tmem_st1(s_addr + kSfaCol + wq, sfa);
+    if constexpr (D == 128) tmem_st4(s_addr + kSfbCol, vsc);
+    else tmem_st2(s_addr + kSfbCol, vsc);
+    l = l * corr + rs;
+    if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int oc = 0; oc < D / 32; ++oc) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + oc * 32, orr);
+            tmem_ld_wait();
+            uint32_t lo[16], hi[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                lo[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
+                hi[i] = __float_as_uint(__uint_as_float(orr[16 + i]) * corr);
+            }
+            tmem_st16(o_addr + oc * 32, lo);
+            tmem_st16(o_addr + oc * 32 + 16, hi);
+        }
+    }
+    tmem_st_wait();
+}
+
+// This lane's words of the V scales of key block blk (column 32 w + lane).
+template <int D>
+__device__ __forceinline__ void load_vscale(const FwdParams& p, int64_t blk, int h, uint32_t (&v)[D / 32]) {
+    const uint32_t* src = p.v_scale + (blk * p.H + h) * D + (threadIdx.x & 31);
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) v[w] = __ldg(src + 32 * w);
+}
+
+template <int D, bool kSparse, bool kMx>
 __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, uint8_t* smem, FwdBars& bars,
                                  uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = FwdLayout<D>;
@@ -605,22 +753,41 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
         }
         float m_use = -INFINITY, l = 0.0f;
         int j = 0;
+        // MXFP8: this lane's V-scale words, fetched one block ahead
+        uint32_t vsc[D / 32], vsn[D / 32];
+        const int64_t blk0 = kMx ? static_cast<int64_t>(__ldg(p.block_start + it.b)) : 0;
+        if (kMx) load_vscale<D>(p, blk0, it.h, vsn);
         for (; j < nfull; ++j) {  // bulk: every key visible, no mask
+            if (kMx) {
+#pragma unroll
+                for (int w = 0; w < D / 32; ++w) vsc[w] = vsn[w];
+                if (j + 1 < nblk) load_vscale<D>(p, blk0 + j + 1, it.h, vsn);
+            }
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 0);
             tc_fence_after();
-            softmax_block<D, kSparse, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+            if constexpr (kMx)
+                softmax_block_mx<D, false>(p, it, j, qpos, wq, s_addr, o_addr, vsc, m_use, l);
+            else
+                softmax_block<D, kSparse, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 0);
             handoff_arrive(&bars.p_full[t]);
         }
         for (; j < nblk; ++j) {  // tail: ragged end and/or causal diagonal
+            if (kMx) {
+#pragma unroll
+                for (int w = 0; w < D / 32; ++w) vsc[w] = vsn[w];
+                if (j + 1 < nblk) load_vscale<D>(p, blk0 + j + 1, it.h, vsn);
+            }
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
             const int nch = (JFA_FWD_TRIM_TAIL & 2) ? min(4, (it.Lk_trim - 128 * j + 31) / 32) : 4;
-            if (nch == 4)
+            if (kMx)
+                softmax_block_mx<D, true>(p, it, j, qpos, wq, s_addr, o_addr, vsc, m_use, l);
+            else if (nch == 4)
                 softmax_block<D, kSparse, true, 4>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             else if (nch == 3)
                 softmax_block<D, kSparse, true, 3>(p, it, j, qpos, s_addr, o_addr, m_use, l);
@@ -731,7 +898,7 @@ done:
     if (JFA_FWD_EPI_TMA && row == 0) bulk_wait_group<0>();  // every O store has completed
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kMx>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     jfa_fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -775,14 +942,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     if (warp < 8) {
         regs_inc<kSoftmaxRegs>();
-        fwd_softmax_role<D, kSparse>(p, &map_o, smem, bars, tmem, ib, ie, ab);
+        fwd_softmax_role<D, kSparse, kMx>(p, &map_o, smem, bars, tmem, ib, ie, ab);
     } else {
         regs_dec<kAuxRegs>();
         if (warp == kWarpTma) {
-            if (lane == 0) fwd_tma_role<D, kSparse>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
+            if (lane == 0) fwd_tma_role<D, kSparse, kMx>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            if (lane == 0) fwd_mma_role<D, kSparse>(p, smem, bars, tmem, ib, ie, ab);
+            if (lane == 0) fwd_mma_role<D, kSparse, kMx>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }
@@ -871,7 +1038,7 @@ __global__ void __launch_bounds__(256) jfa_fwd_merge_kernel(const SplitGroup* gr
     if (cs == 0 && warp == 0 && tile * 128 + row < Lq) lse[(static_cast<int64_t>(g.x) * H + h) * Lq + tile * 128 + row] = L;
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kMx>
 cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     using L = FwdLayout<D>;
     static bool configured = false;
@@ -879,15 +1046,15 @@ cudaError_t launch_fwd_d(const FwdParams& p, const FwdMaps& m, int grid, cudaStr
         // The register split above is only safe if the kernel launches with
         // exactly kLaunchRegs registers per thread; refuse to launch otherwise.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_fwd_kernel<D, kSparse>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_fwd_kernel<D, kSparse, kMx>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(jfa_fwd_kernel<D, kSparse, kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::kDynSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_fwd_kernel<D, kSparse><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v, m.o);
+    jfa_fwd_kernel<D, kSparse, kMx><<<grid, kFwdThreads, L::kDynSmem, s>>>(p, m.q, m.k, m.v, m.o);
     return cudaGetLastError();
 }
 
@@ -906,8 +1073,11 @@ cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, 
 
 cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    if (p.sel) return D == 128 ? launch_fwd_d<128, true>(p, m, grid, s) : launch_fwd_d<64, true>(p, m, grid, s);
-    return D == 128 ? launch_fwd_d<128, false>(p, m, grid, s) : launch_fwd_d<64, false>(p, m, grid, s);
+    if (p.sel)
+        return D == 128 ? launch_fwd_d<128, true, false>(p, m, grid, s) : launch_fwd_d<64, true, false>(p, m, grid, s);
+    if (p.v_scale)
+        return D == 128 ? launch_fwd_d<128, false, true>(p, m, grid, s) : launch_fwd_d<64, false, true>(p, m, grid, s);
+    return D == 128 ? launch_fwd_d<128, false, false>(p, m, grid, s) : launch_fwd_d<64, false, false>(p, m, grid, s);
 }
 
 }  // namespace jfa

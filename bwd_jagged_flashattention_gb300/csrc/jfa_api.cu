@@ -51,7 +51,7 @@ struct WsLayout {
 bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout* w) {
     if (B < 0 || N < 0 || H <= 0) return false;
     w->max_items = max_work_items(B, N, Lq, H, broadcast_q);
-    w->sel_cap = (N / kTileRows + B) * H;
+    w->sel_cap = (N / kTileRows + B) * H + 1;  // (+1: also holds block_start[0..B] of the MXFP8 calls)
     w->sel_off = align_up(kCtaStartBytes + static_cast<size_t>(w->max_items) * sizeof(WorkItem), 256);
     w->blocks_off = w->sel_off + align_up(static_cast<size_t>(B) * H * sizeof(SparseSel), 256);
     w->zero_off = w->sel_off;
@@ -95,6 +95,32 @@ DeviceStage& device_stage(int dev) {
     return stages[dev & 63];
 }
 
+// Runs fill(buf) on a pinned slot of at least `need` bytes; fill writes the
+// slot and enqueues the copies that read it on `stream`.  The slot's event is
+// recorded after them, so the slot is reused only once they have executed.
+template <typename F>
+jfa_status with_stage(size_t need, cudaStream_t stream, F&& fill) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JFA_ERR_CUDA;
+    DeviceStage& ds = device_stage(dev);
+    std::lock_guard<std::mutex> lock(ds.mu);
+    StageSlot& slot = ds.slots[ds.next++ % 4];
+    if (slot.used && cudaEventSynchronize(slot.ev) != cudaSuccess) return JFA_ERR_CUDA;
+    if (slot.cap < need) {
+        if (slot.buf) cudaFreeHost(slot.buf);
+        slot.buf = nullptr;
+        slot.cap = 0;
+        if (cudaHostAlloc(&slot.buf, need, cudaHostAllocDefault) != cudaSuccess) return JFA_ERR_CUDA;
+        slot.cap = need;
+    }
+    if (!slot.ev && cudaEventCreateWithFlags(&slot.ev, cudaEventDisableTiming) != cudaSuccess) return JFA_ERR_CUDA;
+    const jfa_status st = fill(static_cast<char*>(slot.buf));
+    if (st != JFA_OK) return st;
+    if (cudaEventRecord(slot.ev, stream) != cudaSuccess) return JFA_ERR_CUDA;
+    slot.used = true;
+    return JFA_OK;
+}
+
 // Builds the schedule into a pinned slot laid out like the workspace region
 // (WsLayout) and enqueues its copy into ws_region.  With a block mask
 // (block-sparse) the selection tables follow; *n_zero receives the number of
@@ -103,80 +129,69 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
                        const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
                        int64_t* n_zero, int64_t* n_split_groups, jfa_status* st) {
     const int64_t max_items = w.max_items;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        *st = JFA_ERR_CUDA;
-        return -1;
-    }
-    DeviceStage& ds = device_stage(dev);
-    std::lock_guard<std::mutex> lock(ds.mu);
-    StageSlot& slot = ds.slots[ds.next++ % 4];
-    if (slot.used && cudaEventSynchronize(slot.ev) != cudaSuccess) {
-        *st = JFA_ERR_CUDA;
-        return -1;
-    }
     const bool may_split = JFA_FWD_SPLIT_KV && !is_bwd && !mask && broadcast_q && n_split_groups;
     const size_t need = (mask || may_split) ? (is_bwd ? w.bwd_region : w.fwd_region)
                                             : kCtaStartBytes + static_cast<size_t>(max_items) * sizeof(WorkItem);
-    if (slot.cap < need) {
-        if (slot.buf) cudaFreeHost(slot.buf);
-        slot.buf = nullptr;
-        slot.cap = 0;
-        if (cudaHostAlloc(&slot.buf, need, cudaHostAllocDefault) != cudaSuccess) {
-            *st = JFA_ERR_CUDA;
-            return -1;
-        }
-        slot.cap = need;
-    }
-    if (!slot.ev && cudaEventCreateWithFlags(&slot.ev, cudaEventDisableTiming) != cudaSuccess) {
-        *st = JFA_ERR_CUDA;
-        return -1;
-    }
-    char* buf = static_cast<char*>(slot.buf);
-    int32_t* cta_start = reinterpret_cast<int32_t*>(buf);
-    WorkItem* items = reinterpret_cast<WorkItem*>(buf + kCtaStartBytes);
+    int64_t n = -1;
     SparseSpec sp;
-    if (mask) {
-        sp.mask = mask;
-        sp.sel = reinterpret_cast<SparseSel*>(buf + w.sel_off);
-        sp.blocks = reinterpret_cast<int32_t*>(buf + w.blocks_off);
-        sp.zero = reinterpret_cast<ZeroTile*>(buf + w.zero_off);
-        sp.cap = w.sel_cap;
-    }
     SplitSpec split;
-    split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
-    const int64_t n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P,
-                                     is_bwd ? kSchedLptZigzag : kSchedLptGreedy, items,
-                                     cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
-    if (n < 0) {
-        *st = JFA_ERR_WORKSPACE;
-        return -1;
-    }
-    char* dst = static_cast<char*>(ws_region);
-    const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
-    bool ok = cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
-    if (mask && !is_bwd) {
-        ok = ok && cudaMemcpyAsync(dst + w.sel_off, buf + w.sel_off, static_cast<size_t>(B) * H * sizeof(SparseSel),
-                                   cudaMemcpyHostToDevice, stream) == cudaSuccess;
-        ok = ok && (sp.n_blocks == 0 ||
-                    cudaMemcpyAsync(dst + w.blocks_off, buf + w.blocks_off, sp.n_blocks * sizeof(int32_t),
-                                    cudaMemcpyHostToDevice, stream) == cudaSuccess);
-    }
-    if (mask && is_bwd)
-        ok = ok && (sp.n_zero == 0 || cudaMemcpyAsync(dst + w.zero_off, buf + w.zero_off, sp.n_zero * sizeof(ZeroTile),
-                                                      cudaMemcpyHostToDevice, stream) == cudaSuccess);
-    if (may_split)
-        ok = ok && (split.n_groups == 0 ||
-                    cudaMemcpyAsync(dst + w.split_off, buf + w.split_off, split.n_groups * sizeof(SplitGroup),
-                                    cudaMemcpyHostToDevice, stream) == cudaSuccess);
-    if (!ok || cudaEventRecord(slot.ev, stream) != cudaSuccess) {
-        *st = JFA_ERR_CUDA;
-        return -1;
-    }
+    *st = with_stage(need, stream, [&](char* buf) -> jfa_status {
+        int32_t* cta_start = reinterpret_cast<int32_t*>(buf);
+        WorkItem* items = reinterpret_cast<WorkItem*>(buf + kCtaStartBytes);
+        if (mask) {
+            sp.mask = mask;
+            sp.sel = reinterpret_cast<SparseSel*>(buf + w.sel_off);
+            sp.blocks = reinterpret_cast<int32_t*>(buf + w.blocks_off);
+            sp.zero = reinterpret_cast<ZeroTile*>(buf + w.zero_off);
+            sp.cap = w.sel_cap;
+        }
+        split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
+        n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, is_bwd ? kSchedLptZigzag : kSchedLptGreedy,
+                           items, cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
+        if (n < 0) return JFA_ERR_WORKSPACE;
+        char* dst = static_cast<char*>(ws_region);
+        const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
+        bool ok = cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+        if (mask && !is_bwd) {
+            ok = ok && cudaMemcpyAsync(dst + w.sel_off, buf + w.sel_off, static_cast<size_t>(B) * H * sizeof(SparseSel),
+                                       cudaMemcpyHostToDevice, stream) == cudaSuccess;
+            ok = ok && (sp.n_blocks == 0 ||
+                        cudaMemcpyAsync(dst + w.blocks_off, buf + w.blocks_off, sp.n_blocks * sizeof(int32_t),
+                                        cudaMemcpyHostToDevice, stream) == cudaSuccess);
+        }
+        if (mask && is_bwd)
+            ok = ok && (sp.n_zero == 0 ||
+                        cudaMemcpyAsync(dst + w.zero_off, buf + w.zero_off, sp.n_zero * sizeof(ZeroTile),
+                                        cudaMemcpyHostToDevice, stream) == cudaSuccess);
+        if (may_split)
+            ok = ok && (split.n_groups == 0 ||
+                        cudaMemcpyAsync(dst + w.split_off, buf + w.split_off, split.n_groups * sizeof(SplitGroup),
+                                        cudaMemcpyHostToDevice, stream) == cudaSuccess);
+        return ok ? JFA_OK : JFA_ERR_CUDA;
+    });
+    if (*st != JFA_OK) return -1;
     if (n_zero) *n_zero = mask ? sp.n_zero : 0;
     if (n_split_groups) *n_split_groups = may_split ? split.n_groups : 0;
-    slot.used = true;
     return n;
+}
+
+// First 128-key block of every sequence (block_start[b], b = 0..B; the last
+// entry is the total NB) into dst (device, B + 1 int32).  Returns NB in *nb.
+jfa_status stage_block_starts(const int32_t* offsets, int B, void* dst, cudaStream_t stream, int64_t* nb) {
+    return with_stage(sizeof(int32_t) * (static_cast<size_t>(B) + 1), stream, [&](char* buf) -> jfa_status {
+        int32_t* bs = reinterpret_cast<int32_t*>(buf);
+        int64_t acc = 0;
+        for (int b = 0; b < B; ++b) {
+            bs[b] = static_cast<int32_t>(acc);
+            acc += (static_cast<int64_t>(offsets[b + 1]) - offsets[b] + 127) / 128;
+        }
+        bs[B] = static_cast<int32_t>(acc);
+        *nb = acc;
+        return cudaMemcpyAsync(dst, buf, sizeof(int32_t) * (static_cast<size_t>(B) + 1), cudaMemcpyHostToDevice,
+                               stream) == cudaSuccess
+                   ? JFA_OK
+                   : JFA_ERR_CUDA;
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -243,6 +258,16 @@ bool map_rows_bf16(CUtensorMap* m, const void* base, int64_t rows, int H, int D,
                              CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// A 2D [rows, H*D] E4M3 (byte) view with D x 128 boxes: one box is a whole
+// 128-row tile of one head (128-byte swizzle at D=128, 64-byte at D=64).
+bool map_rows_e4m3(CUtensorMap* m, const void* base, int64_t rows, int H, int D, const void* fallback) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(H) * D, static_cast<uint64_t>(rows > 0 ? rows : 1)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(H) * D};
+    const uint32_t box[2] = {static_cast<uint32_t>(D), 128};
+    return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, rows > 0 ? base : fallback, dims, strides, box,
+                             D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 // A 2D [rows, H*D] fp32 view with 16x128 boxes and 64-byte swizzle (dQ reduce-add).
 bool map_rows_f32(CUtensorMap* m, const void* base, int64_t rows, int H, int D, const void* fallback) {
     const uint64_t dims[2] = {static_cast<uint64_t>(H) * D, static_cast<uint64_t>(rows > 0 ? rows : 1)};
@@ -277,7 +302,7 @@ int64_t count_items(const Problem& pr, int is_bwd) {
 // Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
 // ---------------------------------------------------------------------------
 enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfZero = 4, kProfMerge = 5,
-                kProfKinds = 6 };
+                kProfQuant = 6, kProfKinds = 7 };
 
 struct Profiler {
     std::mutex mu;
@@ -339,11 +364,12 @@ extern "C" size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D
 
 extern "C" int jfa_num_ctas(void) { return ctas_for(1 << 30); }
 
-// Forward for jfa_fwd (mask == NULL) and jfa_fwd_block_sparse.
+// Forward for jfa_fwd (mask == NULL, v_scale == NULL), jfa_fwd_block_sparse
+// (mask) and jfa_fwd_mxfp8 (v_scale: v holds E4M3 codes).
 static jfa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
-                           const int32_t* offsets_host, const uint8_t* mask, int B, int Lq, int H, int D,
-                           int broadcast_q, int causal, float scale, void* o, float* lse, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           const int32_t* offsets_host, const uint8_t* mask, bool mx, const void* v_scale, int B,
+                           int Lq, int H, int D, int broadcast_q, int causal, float scale, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Problem pr;
     jfa_status st = check_common(B, Lq, H, D, broadcast_q, causal, scale, offsets_dev, offsets_host, s, &pr);
@@ -352,25 +378,36 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     if ((st = check_workspace(pr, workspace, workspace_bytes, &w)) != JFA_OK) return st;
     const int64_t q_rows = pr.broadcast_q ? pr.Lq : pr.N;
     const int64_t o_rows = pr.broadcast_q ? static_cast<int64_t>(pr.B) * pr.Lq : pr.N;
-    if ((q_rows > 0 && !q) || (pr.N > 0 && (!k || !v)) || (o_rows > 0 && (!o || !lse))) return JFA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    if ((q_rows > 0 && !q) || (pr.N > 0 && (!k || !v || (mx && !v_scale))) || (o_rows > 0 && (!o || !lse)))
+        return JFA_ERR_INVALID_ARG;
+    if (pr.N == 0) v_scale = nullptr;  // no key: nothing is quantized (the bf16 kernel writes the empty rows)
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(v_scale, 16))
         return JFA_ERR_UNSUPPORTED;
     if (o_rows == 0) return JFA_OK;  // nothing to compute
 
     char* ws = static_cast<char*>(workspace);
     // Broadcast Q (split-KV possible): every SM, since splitting can make
     // more items than the batch has; CTAs left without items exit at once.
-    const int64_t n_items = pr.broadcast_q && !mask ? (int64_t{1} << 30) : count_items(pr, 0);
+    // The MXFP8 forward does not split (its items look up their sequence's
+    // V scales by sequence index, which a split chunk does not carry).
+    const bool may_split = pr.broadcast_q && !mask && !v_scale;
+    const int64_t n_items = may_split ? (int64_t{1} << 30) : count_items(pr, 0);
     const int P = ctas_for(n_items);
     int64_t n_groups = 0;
     const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w, mask,
-                                     ws + w.fwd_off, s, nullptr, &n_groups, &st);
+                                     ws + w.fwd_off, s, nullptr, may_split ? &n_groups : nullptr, &st);
     if (n < 0) return st;
     if (n == 0) return JFA_OK;
+    int64_t n_blocks = 0;
+    if (v_scale && (st = stage_block_starts(pr.off, pr.B, ws + w.fwd_off + w.blocks_off, s, &n_blocks)) != JFA_OK)
+        return st;
 
     FwdMaps maps;
+    const bool v_ok = v_scale ? map_rows_e4m3(&maps.v, v, pr.N, H, D, workspace)
+                              : map_rows_bf16(&maps.v, v, pr.N, H, D, workspace);
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
-        !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.o, o, o_rows, H, D, workspace))
+        !v_ok || !map_rows_bf16(&maps.o, o, o_rows, H, D, workspace))
         return JFA_ERR_CUDA;
     FwdParams p;
     p.cta_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off);
@@ -386,6 +423,10 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
     p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
+    if (v_scale) {
+        p.v_scale = static_cast<const uint32_t*>(v_scale);
+        p.block_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off);
+    }
     if (n_groups > 0) {  // split-KV chunks write partials; the merge pass writes their O / LSE
         p.o_part = reinterpret_cast<float*>(ws + w.opart_off);
         p.lse_part = reinterpret_cast<float*>(ws + w.lpart_off);
@@ -404,8 +445,8 @@ extern "C" jfa_status jfa_fwd(const void* q, const void* k, const void* v, const
                               const int32_t* offsets_host, int B, int Lq, int H, int D, int broadcast_q, int causal,
                               float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
                               void* stream) {
-    return fwd_impl(q, k, v, offsets_dev, offsets_host, nullptr, B, Lq, H, D, broadcast_q, causal, scale, o, lse,
-                    workspace, workspace_bytes, stream);
+    return fwd_impl(q, k, v, offsets_dev, offsets_host, nullptr, false, nullptr, B, Lq, H, D, broadcast_q, causal,
+                    scale, o, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" jfa_status jfa_fwd_block_sparse(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
@@ -413,8 +454,40 @@ extern "C" jfa_status jfa_fwd_block_sparse(const void* q, const void* k, const v
                                            int H, int D, int broadcast_q, float scale, void* o, float* lse,
                                            void* workspace, size_t workspace_bytes, void* stream) {
     if (!kv_block_mask) return JFA_ERR_INVALID_ARG;
-    return fwd_impl(q, k, v, offsets_dev, offsets_host, kv_block_mask, B, Lq, H, D, broadcast_q, 0, scale, o, lse,
-                    workspace, workspace_bytes, stream);
+    return fwd_impl(q, k, v, offsets_dev, offsets_host, kv_block_mask, false, nullptr, B, Lq, H, D, broadcast_q, 0,
+                    scale, o, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" jfa_status jfa_fwd_mxfp8(const void* q, const void* k, const void* v8, const void* v_scale,
+                                    const int32_t* offsets_dev, const int32_t* offsets_host, int B, int Lq, int H,
+                                    int D, int broadcast_q, int causal, float scale, void* o, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(q, k, v8, offsets_dev, offsets_host, nullptr, true, v_scale, B, Lq, H, D, broadcast_q, causal,
+                    scale, o, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" jfa_status jfa_quantize_v_mxfp8(const void* v, const int32_t* offsets_dev, const int32_t* offsets_host,
+                                           int B, int H, int D, void* v8, void* v_scale, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Problem pr;
+    jfa_status st = check_common(B, 0, H, D, 0, 0, 1.0f, offsets_dev, offsets_host, s, &pr);
+    if (st != JFA_OK) return st;
+    if (!offsets_dev) return JFA_ERR_INVALID_ARG;
+    const size_t need = kStatusBytes + sizeof(int32_t) * (static_cast<size_t>(B) + 1);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return JFA_ERR_WORKSPACE;
+    if (pr.N > 0 && (!v || !v8 || !v_scale)) return JFA_ERR_INVALID_ARG;
+    if (!aligned(v, 16) || !aligned(v8, 16) || !aligned(v_scale, 16)) return JFA_ERR_UNSUPPORTED;
+    if (pr.N == 0) return JFA_OK;
+    int32_t* bs = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kStatusBytes);
+    int64_t n_blocks = 0;
+    if ((st = stage_block_starts(pr.off, pr.B, bs, s, &n_blocks)) != JFA_OK) return st;
+    if (timed_launch(kProfQuant, s, [&] {
+            return launch_quant_v_mxfp8(static_cast<const uint16_t*>(v), offsets_dev, bs, pr.B, n_blocks, H, D,
+                                        static_cast<uint8_t*>(v8), static_cast<uint32_t*>(v_scale), s);
+        }) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    return JFA_OK;
 }
 
 // Backward for jfa_bwd (mask == NULL) and jfa_bwd_block_sparse.

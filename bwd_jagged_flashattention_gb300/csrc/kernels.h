@@ -23,6 +23,11 @@ struct FwdParams {
     const int32_t* sel_blocks = nullptr; // block-sparse: the selected block indices the records point into
     float* o_part = nullptr;             // split-KV chunks: fp32 O [slot][128][D] (null: no split items)
     float* lse_part = nullptr;           // split-KV chunks: fp32 LSE [slot][128]
+    // MXFP8 P V (null: bf16 V): E8M0 scales of V, one 32-bit word (the four
+    // 32-key chunks of a 128-key block) per (block, head, column) at
+    // (block_start[b] + n) * H * D + h * D + d; block_start[b] = first block of sequence b.
+    const uint32_t* v_scale = nullptr;
+    const int32_t* block_start = nullptr;
 };
 
 struct BwdParams {
@@ -77,6 +82,11 @@ cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, 
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
 cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s);
+// MXFP8 quantization of bf16 V [N,H,D] into E4M3 codes (same layout) and
+// E8M0 scales [NB,H,D,4]: one CTA per 128-key block (NB blocks in total;
+// block_start has B + 1 entries).
+cudaError_t launch_quant_v_mxfp8(const uint16_t* v, const int32_t* offsets, const int32_t* block_start, int B,
+                                 int64_t n_blocks, int H, int D, uint8_t* v8, uint32_t* v_scale, cudaStream_t s);
 // Block-sparse backward: zero the dK and dV rows of the n unselected key tiles.
 cudaError_t launch_zero_tiles(const ZeroTile* tiles, int64_t n, uint16_t* dk, uint16_t* dv, int H, int D,
                               cudaStream_t s);

@@ -278,6 +278,42 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// The same descriptor with a chosen swizzle mode (2 = 128-byte, 4 = 64-byte).
+__device__ __forceinline__ uint64_t smem_desc_swz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                  uint32_t swizzle) {
+    return (smem_desc(saddr, lbo_bytes, sbo_bytes) & ~(7ull << 61)) | (static_cast<uint64_t>(swizzle & 7u) << 61);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: E4M3 A and B,
+// fp32 accumulator, UE8M0 scale factors (one per 32 elements of K).  sf_a /
+// sf_b pick the byte of the scale words that the instruction's 32-element
+// slice of K uses; b_mn selects an MN-major B.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int b_mn, int sf_a, int sf_b) {
+    return (static_cast<uint32_t>(sf_b) << 4)        // B scale-factor byte
+           | (0u << 7)                               // A: E4M3
+           | (0u << 10)                              // B: E4M3
+           | (static_cast<uint32_t>(b_mn) << 16)     // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+           | (1u << 23)                              // scale factors: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)   // M / 16
+           | (static_cast<uint32_t>(sf_a) << 29);    // A scale-factor byte
+}
+
+// D(tmem) (+)= (A(tmem) x 2^sfa) (B(smem) x 2^sfb), block-scaled E4M3 with
+// scale factors in TMEM.  Measured layout for M = 128: row m's A scale is in
+// lane m, column sfa + m / 32; column n's B scale in column sfb + n / 32 of
+// lane 32 * (m / 32) + n % 32 (so every 32-lane quarter holds its own copy).
+__device__ __forceinline__ void mma_ts_mx(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // D(tmem) (+)= A(smem) * B(smem)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -342,6 +378,26 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, const uint32_t (&r)[2]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(r[0]), "r"(r[1]) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -446,6 +502,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_as_float(packed << 16); }
+
+// Two fp32 values to E4M3 (nearest, ties to even; magnitudes beyond 448
+// saturate to 448): lo in bits 0-7, hi in bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^e for an integer e in [-126, 127], exactly.
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
 
 }  // namespace jfa

@@ -150,6 +150,50 @@ jfa_status jfa_bwd_block_sparse(const void *q, const void *k, const void *v, con
                                 float scale, float *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/*
+ * MXFP8 variant of the forward.  The pages' MXFP8 kernel runs its matmuls in
+ * microscaling precision, quantizing P to FP8 on the fly and keeping the
+ * scale factors in tensor memory (TLX porta l'attenzione jagged su Blackwell
+ * oltre FA4 con un terzo del codice, section "The turning point").  Here the
+ * P V product is MXFP8 (E4M3 elements, one E8M0 scale 2^(code - 127) per 32
+ * elements along the keys); Q K^T stays bf16.
+ *
+ *   v8       device uint8 [N, H, D]: V as E4M3 codes (1 sign, 4 exponent
+ *            bits with bias 7, 3 mantissa bits; S.1111.111 is NaN).
+ *   v_scale  device uint8 [NB, H, D, 4], NB = jfa_num_kv_blocks(), 16-byte
+ *            aligned: byte [block_start[b] + n][h][d][c] is the scale code of
+ *            keys 128 n + 32 c .. + 31 of sequence b in column d (block_start
+ *            as for the block-sparse mask).  jfa_quantize_v_mxfp8 writes both.
+ *
+ * P is quantized per row and 32-key chunk c (counted from the sequence
+ * start): with x = scale * s * log2(e), X_c = floor(max_c x) - 8 and the
+ * weight 2^x becomes 2^X_c * E4M3(2^(x - X_c)) (nearest, ties to even,
+ * saturating at 448).  O = sum_j pq_j v_j / sum_j 2^(x_j): the normaliser is
+ * the row sum of the unquantized weights, and LSE is the bf16 forward's.
+ * Split-KV is not used.  All other arguments, layouts, the workspace and the
+ * errors are those of jfa_fwd; a NULL v_scale with N > 0 returns
+ * JFA_ERR_INVALID_ARG.
+ */
+jfa_status jfa_fwd_mxfp8(const void *q, const void *k, const void *v8, const void *v_scale,
+                         const int32_t *offsets_dev, const int32_t *offsets_host, int B, int Lq, int H, int D,
+                         int broadcast_q, int causal, float scale, void *o, float *lse, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/*
+ * jfa_quantize_v_mxfp8 -- MXFP8 V for jfa_fwd_mxfp8 from bf16 v [N, H, D].
+ * Per sequence b, 128-key block n, head h, column d and 32-key chunk c:
+ * X = floor(log2(max |v|)) - 8 over the chunk's keys (clamped to [-127, 127];
+ * -127 for an all-zero chunk), v8 = E4M3(v / 2^X) for those keys, and scale
+ * code X + 127; chunks past the sequence end get code 0.  Exact: the codes
+ * do not depend on rounding order.  offsets_dev is required (the kernel reads
+ * it); offsets_host as for jfa_fwd.  workspace: 256-byte aligned, at least
+ * 256 + 4 (B + 1) bytes (any jfa_workspace_bytes() workspace of the same B
+ * qualifies).  v, v8 and v_scale must be 16-byte aligned.
+ */
+jfa_status jfa_quantize_v_mxfp8(const void *v, const int32_t *offsets_dev, const int32_t *offsets_host, int B,
+                                int H, int D, void *v8, void *v_scale, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
 /* NB = sum over the B sequences of ceil(len_b / 128) (host offsets [B+1]); -1 for bad arguments. */
 int64_t jfa_num_kv_blocks(const int32_t *offsets_host, int B);
 
@@ -197,7 +241,8 @@ jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, c
  * ms[k] and the launch count into launches[k] (either pointer may be NULL),
  * then clears the totals.  Kinds: 0 forward kernel, 1 backward Delta
  * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum, 4 block-sparse
- * zeroing of unselected dK/dV tiles, 5 split-KV merge.  The events
+ * zeroing of unselected dK/dV tiles, 5 split-KV merge, 6 MXFP8 quantization
+ * of V.  The events
  * are host-owned CUDA events; no device memory is allocated.
  */
 jfa_status jfa_profile_enable(int on);

@@ -23,7 +23,7 @@ def _declared_functions():
     for h in ("jfa.h", "jfa_selftest.h"):
         text = open(os.path.join(ROOT, "include", h)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"\b(jfa_[a-z_]+)\s*\(", text):
+        for m in re.finditer(r"\b(jfa_[a-z0-9_]+)\s*\(", text):
             names.add(m.group(1))
     return names
 
@@ -147,3 +147,28 @@ def test_num_kv_blocks(jfa):
     off = torch.tensor([0, 0, 1, 128, 257, 1000], dtype=torch.int32)
     assert jfa.num_kv_blocks(off) == 0 + 1 + 1 + 2 + 6
     assert jfa.lib().jfa_num_kv_blocks(None, 3) == -1
+
+
+def test_mxfp8_argument_errors(jfa):
+    """The MXFP8 entries check their scale pointer, alignment and workspace before any launch (no GPU needed)."""
+    lib = jfa.lib()
+    off = torch.tensor([0, 3, 300], dtype=torch.int32)
+    p = ctypes.c_void_p(P16)
+    offp = ctypes.c_void_p(off.data_ptr())
+
+    def fwd(vs=p, D=64, ws_bytes=1 << 30, causal=0):
+        return lib.jfa_fwd_mxfp8(p, p, p, vs, None, offp, 2, 32, 2, D, 1, causal, 0.1, p, p, ctypes.c_void_p(WS),
+                                 ws_bytes, None)
+
+    def quant(v=p, D=64, dev=p, ws_bytes=1 << 20, vs=p):
+        return lib.jfa_quantize_v_mxfp8(v, dev, offp, 2, 2, D, p, vs, ctypes.c_void_p(WS), ws_bytes, None)
+    assert fwd(vs=None) == jfa.JFA_ERR_INVALID_ARG
+    assert fwd(vs=ctypes.c_void_p(P16 + 4)) == jfa.JFA_ERR_UNSUPPORTED  # scales must be 16-byte aligned
+    assert fwd(D=96) == jfa.JFA_ERR_UNSUPPORTED
+    assert fwd(causal=1) == jfa.JFA_ERR_UNSUPPORTED                      # causal with broadcast Q
+    assert fwd(ws_bytes=64) == jfa.JFA_ERR_WORKSPACE
+    assert quant(D=96) == jfa.JFA_ERR_UNSUPPORTED
+    assert quant(dev=None) == jfa.JFA_ERR_INVALID_ARG                    # the kernel reads device offsets
+    assert quant(v=None) == jfa.JFA_ERR_INVALID_ARG
+    assert quant(vs=ctypes.c_void_p(P16 + 8)) == jfa.JFA_ERR_UNSUPPORTED
+    assert quant(ws_bytes=256) == jfa.JFA_ERR_WORKSPACE                  # needs 256 + 4 (B + 1) bytes
