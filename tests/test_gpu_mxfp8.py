@@ -166,3 +166,29 @@ def test_mxfp8_empty_batch_and_sequences():
     o, lse = jfa.fwd_mxfp8(y["q"], y["k"], v8, vs, y["offsets_dev"], broadcast_q=True, scale=x["scale"],
                            offsets_host=x["offsets"])
     assert torch.all(o.cpu() == 0) and torch.all(torch.isinf(lse.cpu()))
+
+
+def test_mxfp8_dense_llm_sampled():
+    """The dense-LLM workload (jagged causal self-attention, 32 sequences of 512..8192 keys, H=16, D=128) at full
+    size: the whole batch is quantized and run on the GPU; the shortest sequence is checked on every head and
+    the longest on one head against the oracle run on just those rows, with their quantized V bit-exact."""
+    x = jfa_inputs.make("dense_llm", backward=False)
+    v8, vs = _gpu_quant(x)
+    o, lse = _gpu_fwd(x, v8, vs)
+    v8, vs = v8.cpu(), vs.cpu()
+    off = x["offsets"].tolist()
+    lens = [off[b + 1] - off[b] for b in range(x["B"])]
+    blk = [0]
+    for L in lens:
+        blk.append(blk[-1] + (L + 127) // 128)
+    order = sorted(range(x["B"]), key=lambda b: lens[b])
+    for b, h0, h1 in ((order[0], 0, x["H"]), (order[-1], 0, 1)):
+        rows = slice(off[b], off[b + 1])
+        sub = dict(x, B=1, N=lens[b], offsets=torch.tensor([0, lens[b]], dtype=torch.int32),
+                   q=x["q"][rows, h0:h1].contiguous(), k=x["k"][rows, h0:h1].contiguous(),
+                   v=x["v"][rows, h0:h1].contiguous())
+        r8, rs = oracle.quantize_v_mxfp8(sub["v"], sub["offsets"])
+        assert torch.equal(v8[rows, h0:h1], r8) and torch.equal(vs[blk[b]:blk[b + 1], h0:h1], rs)
+        o_ref, lse_ref, slack = oracle._default().fwd_mxfp8(sub["q"], sub["k"], r8, rs, sub["offsets"], 0, False,
+                                                            True, x["scale"], want_slack=True)
+        check_mx(o[rows, h0:h1], lse[h0:h1, rows], o_ref, lse_ref, slack, f"dense-LLM sequence {b} heads {h0}:{h1}")
