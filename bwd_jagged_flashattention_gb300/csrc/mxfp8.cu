@@ -35,16 +35,21 @@ __device__ __forceinline__ float exp2_neg(int X) {
     return X <= 126 ? __int_as_float((127 - X) << 23) : __int_as_float(1 << 22);
 }
 
-// One CTA per 128-key block nb.  Thread i takes column pairs (h, d, d + 1),
-// d even, i, i + 256, ...; for each chunk it reads the chunk's keys (a warp
-// reads 32 consecutive pairs = 128 bytes of one row), finds both columns'
-// maxima, then writes the codes (2 bytes per key) and, at the end, both
-// columns' four scale bytes as one 8-byte store.
-__global__ void __launch_bounds__(256) jfa_quant_v_mxfp8_kernel(const uint16_t* __restrict__ v,
-                                                                const int32_t* __restrict__ offsets,
-                                                                const int32_t* __restrict__ block_start, int B,
-                                                                int H, int D, uint8_t* __restrict__ v8,
-                                                                uint32_t* __restrict__ v_scale) {
+// One CTA per 128-key block nb.  Work unit = (32-key chunk c, 8 adjacent
+// columns of one head): its thread reads the chunk's rows as 16-byte vectors
+// (a warp covers 512 contiguous bytes of a row), takes the 8 column maxima,
+// then reads the rows again (now from L1) to write 8 codes per row as one
+// 8-byte store.  The scale bytes meet in shared memory ([column][chunk], the
+// output layout) and leave as 16-byte words.
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads) jfa_quant_v_mxfp8_kernel(const uint16_t* __restrict__ v,
+                                                                          const int32_t* __restrict__ offsets,
+                                                                          const int32_t* __restrict__ block_start,
+                                                                          int B, int H, int D,
+                                                                          uint8_t* __restrict__ v8,
+                                                                          uint32_t* __restrict__ v_scale) {
+    extern __shared__ uint32_t sc_words[];  // [H * D] scale words of this block
     const int64_t nb = blockIdx.x;
     // The sequence holding block nb: the largest b with block_start[b] <= nb
     // (block_start[0] = 0 <= nb < block_start[B]; empty sequences repeat a
@@ -59,39 +64,63 @@ __global__ void __launch_bounds__(256) jfa_quant_v_mxfp8_kernel(const uint16_t* 
     const int n = static_cast<int>(nb - block_start[b]);
     const int64_t row0 = static_cast<int64_t>(offsets[b]) + 128 * n;
     const int nk = min(128, offsets[b + 1] - offsets[b] - 128 * n);
-    const int pairs = H * D / 2;
-    for (int cp = threadIdx.x; cp < pairs; cp += blockDim.x) {
-        const int h = cp / (D / 2), d = 2 * (cp % (D / 2));
-        const int64_t col = static_cast<int64_t>(h) * D + d;
-        const int64_t stride = static_cast<int64_t>(H) * D;
-        uint32_t sc0 = 0, sc1 = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            const int k0 = 32 * c, cnt = min(32, nk - k0);
-            if (cnt <= 0) break;  // no key left: the remaining scale bytes stay 0
-            uint32_t w[32];
-            float a0 = 0.0f, a1 = 0.0f;
+    const int64_t stride = static_cast<int64_t>(H) * D;  // elements per key row
+    const int groups = H * D / 8;                         // 8-column groups per row
+    uint8_t* sc = reinterpret_cast<uint8_t*>(sc_words);
+    for (int u = threadIdx.x; u < 4 * groups; u += blockDim.x) {
+        const int c = u / groups, g = u % groups;
+        const int col = 8 * g;  // h * D + d, d a multiple of 8 (never crosses a head)
+        const int k0 = 32 * c, cnt = min(32, nk - k0);
+        uint32_t code[8];
+        if (cnt <= 0) {  // no key in this chunk: scale code 0
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                w[k] = 0;
-                if (k < cnt) {
-                    w[k] = __ldg(reinterpret_cast<const uint32_t*>(v + (row0 + k0 + k) * stride + col));
-                    a0 = fmaxf(a0, fabsf(bf16lo_to_f32(w[k])));
-                    a1 = fmaxf(a1, fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+            for (int e = 0; e < 8; ++e) code[e] = 0;
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(v + (row0 + k0) * stride + col);
+            const int64_t rstep = stride / 8;  // uint4 per row
+            float amax[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax[e] = 0.0f;
+#pragma unroll 8
+            for (int k = 0; k < cnt; ++k) {
+                const uint4 w = __ldg(src + k * rstep);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    amax[2 * q] = fmaxf(amax[2 * q], fabsf(bf16lo_to_f32(ww[q])));
+                    amax[2 * q + 1] = fmaxf(amax[2 * q + 1], fabsf(__uint_as_float(ww[q] & 0xFFFF0000u)));
                 }
             }
-            const int X0 = mx_exponent(a0), X1 = mx_exponent(a1);
-            const float s0 = exp2_neg(X0), s1 = exp2_neg(X1);
+            float s[8];
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (k < cnt)
-                    *reinterpret_cast<uint16_t*>(v8 + (row0 + k0 + k) * stride + col) = static_cast<uint16_t>(
-                        cvt_e4m3x2(bf16lo_to_f32(w[k]) * s0, __uint_as_float(w[k] & 0xFFFF0000u) * s1));
-            sc0 |= static_cast<uint32_t>(X0 + 127) << (8 * c);
-            sc1 |= static_cast<uint32_t>(X1 + 127) << (8 * c);
+            for (int e = 0; e < 8; ++e) {
+                const int X = mx_exponent(amax[e]);
+                code[e] = static_cast<uint32_t>(X + 127);
+                s[e] = exp2_neg(X);
+            }
+            uint2* dst = reinterpret_cast<uint2*>(v8 + (row0 + k0) * stride + col);
+            const int64_t dstep = stride / 8;  // uint2 per row
+#pragma unroll 8
+            for (int k = 0; k < cnt; ++k) {
+                const uint4 w = __ldg(src + k * rstep);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                uint32_t pk[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    pk[q] = cvt_e4m3x2(bf16lo_to_f32(ww[2 * q]) * s[4 * q],
+                                       __uint_as_float(ww[2 * q] & 0xFFFF0000u) * s[4 * q + 1]) |
+                            (cvt_e4m3x2(bf16lo_to_f32(ww[2 * q + 1]) * s[4 * q + 2],
+                                        __uint_as_float(ww[2 * q + 1] & 0xFFFF0000u) * s[4 * q + 3])
+                             << 16);
+                dst[k * dstep] = make_uint2(pk[0], pk[1]);
+            }
         }
-        *reinterpret_cast<uint2*>(v_scale + (nb * H + h) * D + d) = make_uint2(sc0, sc1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[(col + e) * 4 + c] = static_cast<uint8_t>(code[e]);
     }
+    __syncthreads();
+    uint4* out = reinterpret_cast<uint4*>(v_scale + nb * stride);
+    for (int i = threadIdx.x; i < H * D / 4; i += blockDim.x) out[i] = reinterpret_cast<const uint4*>(sc_words)[i];
 }
 
 }  // namespace
@@ -100,8 +129,13 @@ cudaError_t launch_quant_v_mxfp8(const uint16_t* v, const int32_t* offsets, cons
                                  int64_t n_blocks, int H, int D, uint8_t* v8, uint32_t* v_scale, cudaStream_t s) {
     if (n_blocks <= 0) return cudaSuccess;
     if (n_blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    jfa_quant_v_mxfp8_kernel<<<static_cast<unsigned>(n_blocks), 256, 0, s>>>(v, offsets, block_start, B, H, D, v8,
-                                                                            v_scale);
+    const size_t smem = static_cast<size_t>(H) * D * 4;  // at most 255 x 128 x 4 = 130,560 bytes
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(jfa_quant_v_mxfp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    jfa_quant_v_mxfp8_kernel<<<static_cast<unsigned>(n_blocks), kQuantThreads, smem, s>>>(v, offsets, block_start, B,
+                                                                                        H, D, v8, v_scale);
     return cudaGetLastError();
 }
 
