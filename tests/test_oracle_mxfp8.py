@@ -16,6 +16,9 @@ independently of the oracle's own arithmetic:
   in E4M3's top binade [256, 512) -- checked as a property, X found by search.
 - V quantization and P quantization against brute force built from the two
   checks above (sequence-relative chunks of 32, scale code X + 127).
+- The quantized P equals what an online softmax with an integer running
+  maximum produces block by block (the schedule a kernel runs), whatever
+  the order in which the maximum grows.
 - The MXFP8 forward equals the plain attention oracle where quantization is
   lossless (V exactly representable, every weight 1.5 * 2^k), has the bf16
   forward's LSE, and matches a brute-force restatement on small random cases.
@@ -281,8 +284,54 @@ def pin_lse_is_the_bf16_forwards(orc):
     assert torch.equal(lse, lse_ref)
 
 
+def online_quantize_p(orc, x, threshold=8.0):
+    """The schedule a kernel runs: 128-key blocks in order, a running maximum kept at an integer m (the
+    ceiling of the first block's maximum, raised to the ceiling of a new maximum only when that exceeds m by
+    more than `threshold`), and per 32-key chunk the exponent e = floor(chunk max - m) - 8 applied to
+    2^(x - m); returns the absolute weights 2^(m + e) E4M3(2^(x - m - e)) for every key."""
+    x = torch.as_tensor(x, dtype=torch.float64)
+    out = torch.zeros_like(x)
+    m = None
+    for j0 in range(0, x.numel(), 128):
+        blk = x[j0:j0 + 128]
+        fin = torch.isfinite(blk)
+        if fin.any():
+            bm = blk[fin].max().item()
+            if m is None:
+                m = math.ceil(bm)
+            elif bm > m + threshold:
+                m = math.ceil(bm)
+        if m is None:
+            continue
+        for c0 in range(0, blk.numel(), 32):
+            ch = blk[c0:c0 + 32]
+            cf = torch.isfinite(ch)
+            if not cf.any():
+                continue
+            e = math.floor(ch[cf].max().item() - m) - 8
+            y = torch.where(cf, torch.exp2(ch - m - e), torch.zeros_like(ch))
+            out[j0 + c0:j0 + c0 + 32] = orc.e4m3_value(orc.e4m3_encode(y)) * 2.0 ** (m + e)
+    return out
+
+
+def pin_online_schedule_invariance(orc):
+    """The oracle's quantized P (one exponent per chunk from floor(chunk max) - 8) is what an online softmax
+    with an integer running max produces, whatever the order in which the maximum grows: rows whose maxima
+    rise over the blocks (so the running max is stale or raised), fall, or jump by more than 8."""
+    g = torch.Generator().manual_seed(14)
+    for trial in range(12):
+        n = int(torch.randint(1, 700, (1,), generator=g))
+        ramp = torch.linspace(0, float(torch.empty(1).uniform_(-30, 30, generator=g)), n, dtype=torch.float64)
+        x = torch.empty(n, dtype=torch.float64).uniform_(-12, 4, generator=g) + ramp
+        x[torch.rand(n, generator=g) < 0.1] = -math.inf
+        want = orc.mx_quantize_p(x)
+        got = online_quantize_p(orc, x)
+        assert torch.allclose(got, want, rtol=1e-12, atol=0), trial
+
+
 PINS = [pin_e4m3_landmarks, pin_e4m3_round_trip, pin_e4m3_nearest_even, pin_mx_exponent, pin_quantize_v,
-        pin_quantize_p, pin_fwd_lossless, pin_fwd_brute_force, pin_lse_is_the_bf16_forwards]
+        pin_quantize_p, pin_online_schedule_invariance, pin_fwd_lossless, pin_fwd_brute_force,
+        pin_lse_is_the_bf16_forwards]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
