@@ -55,6 +55,9 @@
  * -inf, no weight in O, zero dK and dV; a row with no visible key is an
  * empty row (O = 0, LSE = -inf, no gradient).
  *
+ * MXFP8 variant (the *_mxfp8 functions and the E4M3 / E8M0 helpers): see
+ * the section at the end of this file, which states its readings.
+ *
  * Inputs are either fp64 or bf16 bit patterns (uint16) that are widened
  * exactly to fp64 before any arithmetic.  All arithmetic is fp64.  Outputs
  * are fp64; an output pointer may be NULL, in which case that output is
