@@ -2,7 +2,7 @@
 """Benchmark: Jagged Flash Attention forward + backward on one GB300.
 
 One step = one pass of the whole hot path over one batch: the host tile
-schedule, the forward kernel (O, LSE), the backward pre-pass (Delta) and the
+schedules, the forward kernel (O, LSE), the backward pre-pass (Delta) and the
 backward kernel (dQ summed over the batch, dK, dV), all through the C ABI.
 
 Workload (BASELINE metric's configuration): jagged broadcast-Q attention in
@@ -89,11 +89,8 @@ def accounting(x):
     bytes_fwd = q_b + 2 * kv_b + o_b + stat_b                       # Q, K, V in; O, LSE out
     bytes_pre = 2 * o_b + stat_b                                     # O, dO in; Delta out
     bytes_bwd = q_b + 2 * kv_b + o_b + 2 * stat_b + 2 * kv_b + 2 * q_b  # Q,K,V,dO,LSE,Delta in; dK,dV,dQ(fp32) out
-    dq_groups = 0  # partial dQ buffers are off by default in the library (JFA_DQ_GROUPS = 1)
-    bytes_sum = 4 * q_rows * e * (dq_groups + 1) if dq_groups else 0      # G partial dQ in, dQ out
     return dict(pairs=pairs, flops_fwd=f_fwd, flops_bwd=f_bwd, bytes_fwd=bytes_fwd, bytes_pre=bytes_pre,
-                bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e, bytes_sum=bytes_sum,
-                flops_sum=float(q_rows * e * max(dq_groups - 1, 0)))
+                bytes_bwd=bytes_bwd, flops_pre=2.0 * o_rows * e)
 
 
 def selected_keys(offsets, mask):
@@ -563,63 +560,132 @@ def main():
 
     bufs0 = dict(q=q, k=k, v=v, do=do, off=off_d, o=o, lse=lse, dq=dq, dk=dk, dv=dv)
 
-    def dense_step(b=bufs0):
-        jfa.fwd(b["q"], b["k"], b["v"], b["off"], broadcast_q=bq, causal=causal, scale=x["scale"],
-                offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
-        if backward:
-            jfa.bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["off"], broadcast_q=bq, causal=causal,
-                    scale=x["scale"], offsets_host=off_h, workspace=ws, dq=b["dq"], dk=b["dk"], dv=b["dv"])
+    def fwd_pass(b=bufs0):
+        if sparse:
+            jfa.fwd_block_sparse(b["q"], b["k"], b["v"], b["off"], mask_h, broadcast_q=bq, scale=x["scale"],
+                                 offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
+        else:
+            jfa.fwd(b["q"], b["k"], b["v"], b["off"], broadcast_q=bq, causal=causal, scale=x["scale"],
+                    offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
 
-    def sparse_step(b=bufs0):
-        jfa.fwd_block_sparse(b["q"], b["k"], b["v"], b["off"], mask_h, broadcast_q=bq, scale=x["scale"],
-                             offsets_host=off_h, workspace=ws, out=b["o"], lse=b["lse"])
-        if backward:
+    def bwd_pass(b=bufs0):
+        if not backward:
+            return
+        if sparse:
             jfa.bwd_block_sparse(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["off"], mask_h,
                                  broadcast_q=bq, scale=x["scale"], offsets_host=off_h, workspace=ws, dq=b["dq"],
                                  dk=b["dk"], dv=b["dv"])
+        else:
+            jfa.bwd(b["q"], b["k"], b["v"], b["o"], b["lse"], b["do"], b["off"], broadcast_q=bq, causal=causal,
+                    scale=x["scale"], offsets_host=off_h, workspace=ws, dq=b["dq"], dk=b["dk"], dv=b["dv"])
 
-    step = sparse_step if sparse else dense_step
+    def step(b=bufs0):
+        fwd_pass(b)
+        bwd_pass(b)
+
+    def dense_step():
+        jfa.fwd(q, k, v, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h, workspace=ws,
+                out=o, lse=lse)
+        if backward:
+            jfa.bwd(q, k, v, o, lse, do, off_d, broadcast_q=bq, causal=causal, scale=x["scale"], offsets_host=off_h,
+                    workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    def timed_steps(n):
+        """n steps with events around each pass on the launching stream: (total ms, fwd-pass ms list,
+        bwd-pass ms list, host seconds spent issuing the steps)."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_start.record(stream)
+        h0 = time.perf_counter()
+        for i in range(n):
+            evs[i][0].record(stream)
+            fwd_pass()
+            evs[i][1].record(stream)
+            bwd_pass()
+            evs[i][2].record(stream)
+        host_s = time.perf_counter() - h0
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        return (e_start.elapsed_time(e_end), [e[0].elapsed_time(e[1]) for e in evs],
+                [e[1].elapsed_time(e[2]) for e in evs] if backward else [], host_s)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert jfa.device_status(ws) == 0, "kernel status word reports a timeout"
 
+    # The headline region runs without the library's per-kernel events (an event between the
+    # Delta pre-pass and the backward kernel would keep the latter from starting early); the
+    # per-kernel durations come from a second region of the same K steps with them on.
     sampler = ClockSampler(gpu_smi_id(dev))
     sampler.start()
     for _ in range(3):
         step()
-    jfa.profile_enable(True)
-    jfa.profile_read()
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler.mark(0)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    total_ms, fwd_ms_list, bwd_ms_list, host_s = timed_steps(args.steps)
     sampler.mark(1)
     barrier(world)
+    clocks = sampler.stop()
+    jfa.profile_enable(True)
+    jfa.profile_read()
+    prof_total_ms, _, _, _ = timed_steps(args.steps)
     prof = jfa.profile_read()
     jfa.profile_enable(False)
-    clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(world, ev0.elapsed_time(ev1), dev)
+    elapsed_ms = max_over_ranks(world, total_ms, dev)
     ms_per_step = elapsed_ms / args.steps
     step_flops = acc["flops_fwd"] + acc["flops_bwd"]
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
     assert jfa.device_status(ws) == 0, "kernel status word reports a timeout"
+    fwd_pass_ms = statistics.mean(fwd_ms_list)
+    bwd_pass_ms = statistics.mean(bwd_ms_list) if backward else None
+
+    # Host-side cost of the schedules the calls above built (the pages call it negligible): the
+    # forward and backward tile schedules, built alone on the host.
+    P_ctas = jfa.num_ctas()
+    host_sched = {}
+    for name_, fn_ in (("fwd", lambda: jfa.host_schedule(off_h, Lq if bq else 0, H, bq, causal, False, P_ctas,
+                                                          policy=jfa.SCHED_GREEDY)),
+                       ("bwd", lambda: jfa.host_schedule(off_h, Lq if bq else 0, H, bq, causal, True, P_ctas,
+                                                          policy=jfa.SCHED_ZIGZAG))):
+        ts = []
+        for _ in range(7):
+            t0 = time.perf_counter()
+            fn_()
+            ts.append(time.perf_counter() - t0)
+        host_sched[name_ + "_ms"] = 1e3 * statistics.median(ts)
+    host_sched["host_issue_ms_per_step"] = 1e3 * host_s / args.steps
+    host_sched["note"] = ("schedules built alone on the host (median of 7); host_issue_ms_per_step = host time to "
+                          "issue one whole step (argument checks, schedules, copies, launches), overlapped with "
+                          "the GPU's work")
+
+    # Deal-policy ablation (the pages' longest-first sort + zigzag recovered ~20% of the forward):
+    # the same step with each way of dealing the sorted items to the CTAs.
+    ablation = None
+    if not args.batch and world == 1:
+        ablation = {}
+        n_ab = max(20, min(args.steps, 100))
+        for pol_name, pol in (("lpt_greedy", jfa.SCHED_GREEDY), ("lpt_zigzag", jfa.SCHED_ZIGZAG),
+                              ("naive_round_robin", jfa.SCHED_NAIVE)):
+            jfa.set_schedule_policy(pol, pol)
+            for _ in range(3):
+                step()
+            _, f_l, b_l, _ = timed_steps(n_ab)
+            ablation[pol_name] = {"fwd_ms": statistics.mean(f_l), "bwd_ms": statistics.mean(b_l) if backward else None}
+        jfa.set_schedule_policy()  # the library's defaults: greedy forward, zigzag backward
+        ablation["note"] = (f"{n_ab} steps per policy, same inputs; the library deals the forward lpt_greedy and "
+                            f"the backward lpt_zigzag")
 
     # Per-kernel live timing -> rooflines.
     peaks = load_peaks()
     traffic = load_traffic()
     kernels = {}
     for name, flops, nbytes in (("fwd", acc["flops_fwd"], acc["bytes_fwd"]),
-                                ("bwd_pre", acc["flops_pre"], acc["bytes_pre"]),
+                                ("bwd_pre", acc["flops_pre"] if backward else 0.0, acc["bytes_pre"] if backward else 0),
                                 ("bwd", acc["flops_bwd"], acc["bytes_bwd"]),
-                                ("dq_sum", acc["flops_sum"], acc["bytes_sum"]),
-                                ("zero_tiles", 0.0, acc.get("bytes_zero", 0) if backward else 0)):
+                                ("zero_tiles", 0.0, acc.get("bytes_zero", 0) if backward else 0),
+                                ("fwd_merge", 0.0, 0)):
         ms, n = prof[name]
         avg = ms / max(n, 1)
         tflops = flops / (avg * 1e-3) / 1e12 if avg > 0 else 0.0
@@ -645,6 +711,36 @@ def main():
                 "frac": dom["gbs"] / peaks["hbm_gbs"]}
     roof.update(kernel=f"jfa_{dom_name}_kernel", traffic=dom["traffic"], peak_source=peaks["source"],
                 algorithmic_per_launch=dom["algorithmic_bytes"] if roof["bound"] == "hbm" else dom["algorithmic_flops"])
+
+    # Host link rates (pinned memory, 256 MiB copies), each direction alone and both at once: the
+    # rates the end-to-end line's copies should be read against.
+    link = None
+    if world == 1:
+        nb_ = 256 << 20
+        hbuf, hbuf2 = torch.empty(nb_, dtype=torch.uint8).pin_memory(), torch.empty(nb_, dtype=torch.uint8).pin_memory()
+        dbuf, dbuf2 = torch.empty(nb_, dtype=torch.uint8, device=dev), torch.empty(nb_, dtype=torch.uint8, device=dev)
+        s2 = torch.cuda.Stream(dev)
+
+        def copy_rate(h2d_, d2h_):
+            dbuf.copy_(hbuf, non_blocking=True)
+            torch.cuda.synchronize()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            s2.wait_stream(stream)
+            for _ in range(3):
+                if h2d_:
+                    dbuf.copy_(hbuf, non_blocking=True)
+                if d2h_:
+                    with torch.cuda.stream(s2):
+                        hbuf2.copy_(dbuf2, non_blocking=True)
+            stream.wait_stream(s2)
+            eb.record(stream)
+            torch.cuda.synchronize()
+            return 3 * nb_ * (int(h2d_) + int(d2h_)) / (ea.elapsed_time(eb) * 1e-3) / 1e9
+
+        link = {"h2d_gbs": copy_rate(True, False), "d2h_gbs": copy_rate(False, True),
+                "both_gbs": copy_rate(True, True), "how": "3 x 256 MiB pinned copies per direction, CUDA events"}
+        del hbuf, hbuf2, dbuf, dbuf2
 
     # End to end: every step copies its inputs from pinned host memory to the device, runs both
     # passes through the library's API and copies all of its outputs (O, LSE, dQ, dK, dV) back to
@@ -752,19 +848,33 @@ def main():
                           f"no flush; K+V inputs (~{4 * N * H * D / 1e6:.0f} MB) fit in the 129 MB L2"),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    **({"block_sparse": sparse_info} if sparse else {})},
-        "fwd_tflops": kernels["fwd"]["tflops"], "bwd_tflops": acc["flops_bwd"] / (
-            (kernels["bwd"]["avg_ms"] + kernels["bwd_pre"]["avg_ms"] + kernels["dq_sum"]["avg_ms"]
-             + kernels["zero_tiles"]["avg_ms"]) * 1e-3) / 1e12
-        if backward else None,
-        "tensor_peak_frac": {"fwd": kernels["fwd"]["tensor_frac"], "bwd_kernel": kernels["bwd"]["tensor_frac"],
+        # Each pass timed on the launching stream from its first to its last operation: the forward
+        # pass is its kernel (and a split-KV merge when one runs); the backward pass is the dQ memset,
+        # the Delta pre-pass and the backward kernel.
+        "fwd_ms": fwd_pass_ms, "bwd_ms": bwd_pass_ms,
+        "fwd_tflops": acc["flops_fwd"] / (fwd_pass_ms * 1e-3) / 1e12,
+        "bwd_tflops": acc["flops_bwd"] / (bwd_pass_ms * 1e-3) / 1e12 if backward else None,
+        "tensor_peak_frac": {"fwd": acc["flops_fwd"] / (fwd_pass_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                             "bwd": (acc["flops_bwd"] / (bwd_pass_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]
+                                     if backward else None),
+                             "fwd_kernel": kernels["fwd"]["tensor_frac"],
+                             "bwd_kernel": kernels["bwd"]["tensor_frac"] if backward else None,
                              "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"]},
         "roofline": roof,
         "kernels": kernels,
+        "host_schedule": host_sched,
+        "schedule_ablation": ablation,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
-                "pipeline": "double-buffered: H2D of step i+1 and D2H of step i-1 overlap step i (3 streams)"},
+                "pipeline": "double-buffered: H2D of step i+1 and D2H of step i-1 overlap step i (3 streams)",
+                "host_link": link,
+                "link_floor_ms": (max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
+                                      (h2d + d2h) / (link["both_gbs"] * 1e9)) * 1e3 if link else None)},
         "gpu_launches": int(sum(k_["launches"] for k_ in kernels.values())),
+        "kernel_timing": (f"per-kernel CUDA events on the launching stream over a second region of {args.steps} "
+                          f"steps right after the headline one ({prof_total_ms / args.steps:.4f} ms per step "
+                          f"with the events on)"),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

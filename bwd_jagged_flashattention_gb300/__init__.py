@@ -29,6 +29,7 @@ JFA_OK, JFA_ERR_INVALID_ARG, JFA_ERR_UNSUPPORTED, JFA_ERR_WORKSPACE, JFA_ERR_CUD
 # Every symbol include/jfa.h and include/jfa_selftest.h declare.
 EXPORTED = ("jfa_workspace_bytes", "jfa_fwd", "jfa_bwd", "jfa_device_status", "jfa_status_string",
             "jfa_num_ctas", "jfa_profile_enable", "jfa_profile_read", "jfa_selftest_mma", "jfa_fwd_static_scratch",
+            "jfa_static_scratch_status", "jfa_set_schedule_policy", "jfa_set_wait_limit", "jfa_selftest_timeout",
             "jfa_fwd_block_sparse", "jfa_bwd_block_sparse", "jfa_num_kv_blocks", "jfa_fwd_mxfp8",
             "jfa_quantize_v_mxfp8")
 
@@ -82,6 +83,12 @@ def lib() -> ctypes.CDLL:
             L.jfa_device_status.restype = ci
             L.jfa_status_string.argtypes = [ci]
             L.jfa_status_string.restype = ctypes.c_char_p
+            L.jfa_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+            L.jfa_set_wait_limit.restype = ci
+            L.jfa_selftest_timeout.argtypes = [ctypes.c_ulonglong, vp, vp, vp]
+            L.jfa_selftest_timeout.restype = ci
+            L.jfa_set_schedule_policy.argtypes = [ci, ci]
+            L.jfa_set_schedule_policy.restype = ci
             L.jfa_num_ctas.argtypes = []
             L.jfa_num_ctas.restype = ci
             L.jfa_profile_enable.argtypes = [ci]
@@ -321,7 +328,7 @@ def profile_enable(on: bool = True) -> None:
     _check(lib().jfa_profile_enable(int(on)), "jfa_profile_enable")
 
 
-PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "dq_sum", "zero_tiles", "fwd_merge", "quant_v")
+PROFILE_KINDS = ("fwd", "bwd_pre", "bwd", "zero_tiles", "fwd_merge", "quant_v")
 
 
 def profile_read() -> dict:
@@ -361,6 +368,18 @@ def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
     return items[:n].clone(), starts
+
+
+def set_wait_limit(ns: int = 0) -> None:
+    """Limit of one barrier wait inside the kernels, in ns, for later launches (0: the 4 s default)."""
+    _check(lib().jfa_set_wait_limit(int(ns)), "jfa_set_wait_limit")
+
+
+def set_schedule_policy(fwd_policy: int = None, bwd_policy: int = None) -> None:
+    """How later calls deal their sorted items to the CTAs (a measurement aid; defaults: greedy / zigzag)."""
+    _check(lib().jfa_set_schedule_policy(SCHED_GREEDY if fwd_policy is None else int(fwd_policy),
+                                         SCHED_ZIGZAG if bwd_policy is None else int(bwd_policy)),
+           "jfa_set_schedule_policy")
 
 
 def host_schedule_split(offsets_host, Lq: int, H: int, P: int):

@@ -41,52 +41,9 @@
 namespace jfa {
 namespace {
 
-// Tuning knobs (compile-time): K/V ring depth in 128-row tiles at D=128, and
-// how many KV blocks ahead of the ring the L2 prefetch runs (0 = off).
-// O epilogue without a shared-memory stage: each thread stores its own row
-// (frees 32 KB, e.g. for a fifth K/V ring slot).  Ads step: 140.5 us with
-// four slots, 141.6 us with five, vs 138.2 us staged (a fifth slot does not
-// help; three slots cost 23 us).
-#ifndef JFA_FWD_O_ROWSTORE
-#define JFA_FWD_O_ROWSTORE 0
-#endif
-#ifndef JFA_FWD_SLOTS
-#define JFA_FWD_SLOTS 4
-#endif
-// Softmax -> MMA hand-offs (p_full, o_empty): 1 = one arrival per warp
-// (lane 0, after the warp's tcgen05 fences and a __syncwarp), 0 = one per
-// thread.  Measured on the ads step: no gain (137.8 vs 137.2 us).
-#ifndef JFA_FWD_WARP_ARRIVE
-#define JFA_FWD_WARP_ARRIVE 0
-#endif
-#ifndef JFA_FWD_PREFETCH
-#define JFA_FWD_PREFETCH 0
-#endif
-// Exponent pairs (of every 16) computed on the FMA pipe in unmasked blocks.
-// Measured: any share > 0 is slower on GB300 (the passes are latency-bound,
-// not special-function-bound), so the default keeps every exponential on the SFU.
-// Ragged last KV block: cover only the keys up to the sequence end instead
-// of all 128 -- bit 0: in the products (rounded up to 16 keys), bit 1: in the
-// softmax (whole 32-column chunks; needs bit 0).  Measured on the ads step:
-// slower either way (products only 166.6 us, both 174.9 us, off 158.6 us).
-#ifndef JFA_FWD_TRIM_TAIL
-#define JFA_FWD_TRIM_TAIL 0
-#endif
-// O epilogue of whole 128-row tiles through TMA stores (each softmax
-// warpgroup stages a 64-column half in its 16 KB stage, one thread stores it).
-// Measured slower on the ads step (140.9 vs 135.8 us): with one stage per
-// warpgroup the second half waits for the first half's store.
-#ifndef JFA_FWD_EPI_TMA
-#define JFA_FWD_EPI_TMA 0
-#endif
-// Row sums of P: 1 = four paired partial sums (add.f32x2), 0 = eight scalar
-// (ads step: 158.7 vs 164.4 us).
-#ifndef JFA_FWD_PAIRED_SUMS
-#define JFA_FWD_PAIRED_SUMS 1
-#endif
-#ifndef JFA_FWD_POLY_PAIRS
-#define JFA_FWD_POLY_PAIRS 0
-#endif
+// K/V ring depth in 128-row tiles at D = 128 (twice as many at D = 64):
+// three slots cost 23 us on the ads step, a fifth gained nothing.
+constexpr int kRingSlots = 4;
 
 // 384 threads = three warpgroups: two softmax warpgroups and one holding the
 // TMA warp, the MMA warp and two idle warps.  Registers are moved from the
@@ -108,12 +65,12 @@ struct FwdLayout {
     static constexpr int kSlabBytes = 128 * 128;  // 128 rows x 64 bf16 (one swizzle span)
     static constexpr int kSlabs = D / 64;
     static constexpr int kTileBytes = kSlabs * kSlabBytes;
-    static constexpr int kSlots = D == 128 ? JFA_FWD_SLOTS : 2 * JFA_FWD_SLOTS;  // K/V ring tiles
+    static constexpr int kSlots = D == 128 ? kRingSlots : 2 * kRingSlots;  // K/V ring tiles
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = 2 * kTileBytes;
     // Epilogue staging: 128 rows x 64 columns of bf16 (16 KB) per softmax warpgroup.
     static constexpr int kStageOff = (2 + kSlots) * kTileBytes;
-    static constexpr int kStageBytes = JFA_FWD_O_ROWSTORE ? 0 : 16384;
+    static constexpr int kStageBytes = 16384;
     static constexpr int kBytes = kStageOff + 2 * kStageBytes;
     static constexpr int kDynSmem = kBytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
@@ -122,7 +79,7 @@ struct FwdLayout {
 
 struct FwdBars {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[2 * JFA_FWD_SLOTS], kv_empty[2 * JFA_FWD_SLOTS];
+    uint64_t kv_full[2 * kRingSlots], kv_empty[2 * kRingSlots];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -131,7 +88,6 @@ struct FwdBars {
 
 struct FwdItem {
     int b, h, kv_start, Lk, m0, nq, q_row0, q_rows;
-    int Lk_trim;  // keys the ragged-tail trim sees (no trim under a block-sparse selection)
     int slot;     // split-KV chunk: its partial (O, LSE) slot; -1 for a whole item
     int sel_off;  // block-sparse: the item's first entry in the selected-block list
     int nblk[2], nfull[2], nb;
@@ -152,7 +108,6 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
     it.q_row0 = p.broadcast_q ? 0 : w.kv_start;
     it.q_rows = p.broadcast_q ? p.Lq : w.kv_len;
     int nkv = (it.Lk + 127) / 128, full = it.Lk / 128;
-    it.Lk_trim = it.Lk;
     it.sel_off = 0;
     it.slot = w.b < 0 ? -w.b - 1 : -1;  // a split-KV chunk (its keys are kv_start .. + kv_len)
     if (kSparse) {  // block-sparse (never causal): visit only the selected blocks, in ascending order
@@ -160,7 +115,6 @@ __device__ __forceinline__ FwdItem decode_fwd(const WorkItem& w, const FwdParams
         it.sel_off = s.x;
         nkv = s.y;
         full = s.z;  // a ragged last block, when selected, is the last one visited
-        it.Lk_trim = 1 << 30;
     }
     it.nb = 0;
 #pragma unroll
@@ -215,18 +169,11 @@ __device__ __forceinline__ bool next_item_reuses_q(const FwdParams& p, const Fwd
 }
 
 // Hand-off from a softmax warpgroup to the MMA thread after its tcgen05
-// stores or loads: every thread fences, then every thread arrives (count
-// 128) or, with JFA_FWD_WARP_ARRIVE, lane 0 of each warp once the warp has
-// synchronised (count 4).
-constexpr uint32_t kHandoffCount = JFA_FWD_WARP_ARRIVE ? 4 : 128;
+// stores or loads: every thread fences, then arrives (count 128).
+constexpr uint32_t kHandoffCount = 128;
 __device__ __forceinline__ void handoff_arrive(uint64_t* bar) {
     tc_fence_before();
-    if (JFA_FWD_WARP_ARRIVE) {
-        __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    } else {
-        mbar_arrive(bar);
-    }
+    mbar_arrive(bar);
 }
 
 // Barrier over the 128 threads of one softmax warpgroup (ids 1 and 2).
@@ -245,39 +192,25 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t saddr) { return smem_d
 // S(tmem) = Q K^T: both operands K-major in 128-byte-swizzled slabs of 64
 // columns; one K=16 step advances 32 bytes inside a slab.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+__device__ __forceinline__ void issue_qk(uint32_t lead, uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         constexpr uint64_t unit = 16;
         const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) / unit;
-        mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0);
-    }
-}
-
-// The same product for a ragged last KV block: only the first n keys
-// (n a multiple of 16 covering the sequence's remaining keys); the S columns
-// past n keep stale values, which the softmax masks to -inf.
-template <int D>
-__device__ __forceinline__ void issue_qk_n(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc, uint32_t n) {
-    const uint32_t idesc = idesc_bf16_f32(128, 0, 0, 0) | ((n >> 3) << 17);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        constexpr uint64_t unit = 16;
-        const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) / unit;
-        mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0);
+        mma_ss_p(lead, d_tmem, q_desc + off, k_desc + off, idesc, kk > 0);
     }
 }
 
 // O(tmem) (+)= P(tmem, bf16) V: V is MN-major (D contiguous); one K=16 step
 // covers 16 key rows = 2048 bytes; the 64-column slabs are 16 KB apart.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc,
-                                         int ksteps = 8) {
+__device__ __forceinline__ void issue_pv(uint32_t lead, uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                         uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        if (kk < ksteps) mma_ts(d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
+        mma_ts_p(lead, d_tmem, p_tmem + kk * 8, v_desc + kk * (2048 / 16), idesc, (acc | kk) != 0);
 }
 
 // TMEM columns (from a tile's S base) of the MXFP8 product's scale factors:
@@ -289,47 +222,12 @@ constexpr uint32_t kSfaCol = 32, kSfbCol = 64;
 // MN-major with D-byte rows (128-byte swizzle at D=128, 64-byte at D=64);
 // one step covers 32 rows.
 template <int D>
-__device__ __forceinline__ void issue_pv_mx(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc, uint32_t acc) {
+__device__ __forceinline__ void issue_pv_mx(uint32_t lead, uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                            uint32_t acc) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-        mma_ts_mx(d_tmem, p_tmem + c * 8, v_desc + c * (32 * D / 16), idesc_mxf8_e4m3(128, D, 1, c, c),
-                  p_tmem + kSfaCol, p_tmem + kSfbCol, (acc | c) != 0);
-}
-
-// Keys of KV block j the products cover: 128, or for a ragged last block the
-// remaining keys rounded up to 16 (the MMA's N granularity).
-__device__ __forceinline__ uint32_t block_keys(int Lk, int j) {
-    const int nv = Lk - 128 * j;
-    return (!(JFA_FWD_TRIM_TAIL & 1) || nv >= 128) ? 128u : static_cast<uint32_t>((nv + 15) & ~15);
-}
-
-// L2 prefetch runs this many KV blocks ahead of the smem ring, so the ring's
-// TMA loads hit L2 instead of waiting for HBM.
-constexpr int kPrefetchBlocks = JFA_FWD_PREFETCH;
-
-// Walks the same (item, KV block) sequence as the loads, kPrefetchBlocks ahead.
-struct PrefetchCursor {
-    int i, j, nb, h, kv_start;
-};
-
-template <int D, bool kSparse>
-__device__ __forceinline__ void prefetch_next_block(PrefetchCursor& c, const FwdParams& p, int ie,
-                                                    const CUtensorMap* mk, const CUtensorMap* mv) {
-    while (c.i < ie && c.j >= c.nb) {
-        if (++c.i >= ie) return;
-        const FwdItem it = decode_fwd<kSparse>(p.items[c.i], p);
-        c.j = 0;
-        c.nb = it.nb;
-        c.h = it.h;
-        c.kv_start = it.kv_start;
-    }
-    if (kPrefetchBlocks == 0 || c.i >= ie) return;
-#pragma unroll
-    for (int s = 0; s < D / 64; ++s) {
-        tma_prefetch_2d(mk, c.h * D + 64 * s, c.kv_start + 128 * c.j);
-        tma_prefetch_2d(mv, c.h * D + 64 * s, c.kv_start + 128 * c.j);
-    }
-    ++c.j;
+        mma_ts_mx_p(lead, d_tmem, p_tmem + c * 8, v_desc + c * (32 * D / 16), idesc_mxf8_e4m3(128, D, 1, c, c),
+                    p_tmem + kSfaCol, p_tmem + kSfbCol, (acc | c) != 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -345,8 +243,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     prefetch_tensormap(mv);
     uint32_t ring = 0, q_loads = 0;
     QKey qk;
-    PrefetchCursor pf{ib - 1, 0, 0, 0, 0};
-    for (int k = 0; k < kPrefetchBlocks; ++k) prefetch_next_block<D, kSparse>(pf, p, ie, mk, mv);
     WorkItem wn = load_item(p.items, ib, ie);
     for (int i = ib; i < ie; ++i) {
         const WorkItem wc = wn;
@@ -386,7 +282,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                 JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
                 ++ring;
             }
-            prefetch_next_block<D, kSparse>(pf, p, ie, mk, mv);
         }
     }
 done:
@@ -406,6 +301,9 @@ template <int D, bool kSparse, bool kMx>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
+    // The whole warp runs this role (uniform control flow and operands); only
+    // lane 0 issues the products and commits.
+    const uint32_t lead = (threadIdx.x & 31) == 0 ? 1u : 0u;
     const uint64_t q_desc = kmajor_desc(smem_u32(smem + L::kQOff));
     const uint64_t k_desc = kmajor_desc(smem_u32(smem + L::kRingOff));
     const uint64_t v_desc = kMx ? smem_desc_swz(smem_u32(smem + L::kRingOff), 16384, 8 * D, D == 128 ? 2u : 4u)
@@ -420,7 +318,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         wn = wn2;  // item i + 1, loaded an iteration ago
         wn2 = load_item(p.items, i + 2, ie);
         const FwdItem it = decode_fwd<kSparse>(wc, p);
-        JFA_TRACE_EVENT(10, 9, i, it.nb);
+        if (lead) JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {
             if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
@@ -428,32 +326,31 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             qk.set(it);
         }
         const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
-        JFA_TRACE_EVENT(11, 9, i, 0);
+        if (lead) JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
         if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
         ++ring;
-        JFA_TRACE_EVENT(12, 9, 0, 0);
+        if (lead) JFA_TRACE_EVENT(12, 9, 0, 0);
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 2; ++t)
             if (it.nblk[t] > 0) {
-                issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
-                              block_keys(it.Lk_trim, 0));
-                mma_commit(&bars.s_full[t]);
+                issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                mma_commit_p(lead, &bars.s_full[t]);
             }
-        mma_commit(&bars.kv_empty[kslot]);
-        if (it.nb == 1 && release_q) mma_commit(&bars.q_empty);
+        mma_commit_p(lead, &bars.kv_empty[kslot]);
+        if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
             if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
             ++ring;
-            JFA_TRACE_EVENT(13, 9, j, 0);
+            if (lead) JFA_TRACE_EVENT(13, 9, j, 0);
             const bool has_next = j + 1 < it.nb;
             if (has_next) {
                 kslot = ring % L::kSlots;
                 if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
                 ++ring;
-                JFA_TRACE_EVENT(12, 9, j + 1, 0);
+                if (lead) JFA_TRACE_EVENT(12, 9, j + 1, 0);
             }
             tc_fence_after();
 #pragma unroll
@@ -462,30 +359,28 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 if (j == 0) {
                     if (!mbar_wait(&bars.o_empty[t], oe_ph[t], ab)) goto done;
                     oe_ph[t] ^= 1;
-                    JFA_TRACE_EVENT(17, 9, t, j);
+                    if (lead) JFA_TRACE_EVENT(17, 9, t, j);
                 }
                 if (!mbar_wait(&bars.p_full[t], p_ph[t], ab)) goto done;
                 p_ph[t] ^= 1;
-                JFA_TRACE_EVENT(15, 9, t, j);
+                if (lead) JFA_TRACE_EVENT(15, 9, t, j);
                 tc_fence_after();
                 if (kMx)
-                    issue_pv_mx<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                    issue_pv_mx<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
                 else
-                    issue_pv<D>(tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0,
-                                static_cast<int>(block_keys(it.Lk_trim, j) / 16));
-                JFA_TRACE_EVENT(16, 9, t, j);
-                if (j == it.nblk[t] - 1) mma_commit(&bars.o_full[t]);
+                    issue_pv<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                if (lead) JFA_TRACE_EVENT(16, 9, t, j);
+                if (j == it.nblk[t] - 1) mma_commit_p(lead, &bars.o_full[t]);
                 if (j + 1 < it.nblk[t]) {
-                    issue_qk_n<D>(tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits,
-                                  block_keys(it.Lk_trim, j + 1));
-                    JFA_TRACE_EVENT(18, 9, t, j + 1);
-                    mma_commit(&bars.s_full[t]);
+                    issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                    if (lead) JFA_TRACE_EVENT(18, 9, t, j + 1);
+                    mma_commit_p(lead, &bars.s_full[t]);
                 }
             }
-            mma_commit(&bars.kv_empty[vslot]);
+            mma_commit_p(lead, &bars.kv_empty[vslot]);
             if (has_next) {
-                mma_commit(&bars.kv_empty[kslot]);
-                if (j + 2 == it.nb && release_q) mma_commit(&bars.q_empty);
+                mma_commit_p(lead, &bars.kv_empty[kslot]);
+                if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
             }
         }
     }
@@ -493,7 +388,7 @@ done:
     // All issued MMAs must finish before TMEM is released.  A CTA that never
     // took a K/V tile (no items, or only empty ones) issued none.
     if (ring > 0) {
-        mma_commit(&bars.mma_done);
+        mma_commit_p(lead, &bars.mma_done);
         mbar_wait_drain(&bars.mma_done, 0);
     }
 }
@@ -502,19 +397,12 @@ done:
 // Softmax / correction / epilogue (one warpgroup per query tile; thread r
 // owns query row r of the tile = TMEM lane r).
 // ---------------------------------------------------------------------------
-// kChunks: 32-column chunks of S that hold visible keys.  A ragged last
-// block (JFA_FWD_TRIM_TAIL) uses only its first kChunks; the products skip
-// the keys past them too, so those P columns are never read.
-template <int D, bool kSparse, bool kMask, int kChunks = 4>
+template <int D, bool kSparse, bool kMask>
 __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem& it, int j, int qpos,
                                               uint32_t s_addr, uint32_t o_addr, float& m_use, float& l) {
     uint32_t sr[4][32];
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
-#pragma unroll
-    for (int c = kChunks; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sr[c][i] = __float_as_uint(-INFINITY);
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sr[c]);
     tmem_ld_wait();
     if (kMask) {
         // Keys kbase .. kbase + nvis - 1 are visible to this row: the
@@ -553,36 +441,28 @@ __device__ __forceinline__ void softmax_block(const FwdParams& p, const FwdItem&
     }
     const float base = m_use == -INFINITY ? 0.0f : m_use;
     // P = 2^(s * scale_log2 - base): paired FMAs, then the hardware exp2;
-    // the row sum uses 8 partial sums.
+    // the row sum uses four paired (add.f32x2) partial sums (ads step:
+    // 158.7 vs 164.4 us with eight scalar ones).
     float rss[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) rss[a] = 0.0f;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            float x0, x1, p0, p1;
+            float x0, x1;
             ffma2(x0, x1, __uint_as_float(sr[c][2 * e]), __uint_as_float(sr[c][2 * e + 1]), p.scale_log2, p.scale_log2,
                   -base, -base);
-            if (!kMask && poly_pair<JFA_FWD_POLY_PAIRS>(e)) {  // part of the exponentials on the FMA pipe (no -inf here)
-                exp2_fma2(x0, x1, p0, p1);
-            } else {
-                p0 = ex2_approx(x0);
-                p1 = ex2_approx(x1);
-            }
-            if (JFA_FWD_PAIRED_SUMS) {  // 4 paired (add.f32x2) partial sums
-                const int a = (c * 2 + e / 8) & 6;
-                float s0 = a == 0 ? rss[0] : a == 2 ? rss[2] : a == 4 ? rss[4] : rss[6];
-                float s1 = a == 0 ? rss[1] : a == 2 ? rss[3] : a == 4 ? rss[5] : rss[7];
-                fadd2(s0, s1, s0, s1, p0, p1);
-                if (a == 0) { rss[0] = s0; rss[1] = s1; }
-                else if (a == 2) { rss[2] = s0; rss[3] = s1; }
-                else if (a == 4) { rss[4] = s0; rss[5] = s1; }
-                else { rss[6] = s0; rss[7] = s1; }
-            } else {
-                rss[(c * 2 + e / 8)] += p0 + p1;
-            }
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const int a = (c * 2 + e / 8) & 6;
+            float s0 = a == 0 ? rss[0] : a == 2 ? rss[2] : a == 4 ? rss[4] : rss[6];
+            float s1 = a == 0 ? rss[1] : a == 2 ? rss[3] : a == 4 ? rss[5] : rss[7];
+            fadd2(s0, s1, s0, s1, p0, p1);
+            if (a == 0) { rss[0] = s0; rss[1] = s1; }
+            else if (a == 2) { rss[2] = s0; rss[3] = s1; }
+            else if (a == 4) { rss[4] = s0; rss[5] = s1; }
+            else { rss[6] = s0; rss[7] = s1; }
             pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
@@ -784,17 +664,10 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             s_ph ^= 1;
             if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
-            const int nch = (JFA_FWD_TRIM_TAIL & 2) ? min(4, (it.Lk_trim - 128 * j + 31) / 32) : 4;
-            if (kMx)
+            if constexpr (kMx)
                 softmax_block_mx<D, true>(p, it, j, qpos, wq, s_addr, o_addr, vsc, m_use, l);
-            else if (nch == 4)
-                softmax_block<D, kSparse, true, 4>(p, it, j, qpos, s_addr, o_addr, m_use, l);
-            else if (nch == 3)
-                softmax_block<D, kSparse, true, 3>(p, it, j, qpos, s_addr, o_addr, m_use, l);
-            else if (nch == 2)
-                softmax_block<D, kSparse, true, 2>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             else
-                softmax_block<D, kSparse, true, 1>(p, it, j, qpos, s_addr, o_addr, m_use, l);
+                softmax_block<D, kSparse, true>(p, it, j, qpos, s_addr, o_addr, m_use, l);
             if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
             handoff_arrive(&bars.p_full[t]);
         }
@@ -832,34 +705,8 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             const int64_t row0 = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + 128 * (it.m0 + t)
                                                : static_cast<int64_t>(it.q_row0) + 128 * (it.m0 + t);
             const int rows_valid = min(128, it.q_rows - 128 * (it.m0 + t));
-            // Whole tiles leave by TMA stores (one thread issues, the
-            // warpgroup only stages); a ragged tile by coalesced copies.
-            if (JFA_FWD_O_ROWSTORE) {
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o + ((row0 + row) * p.H + it.h) * D);
-#pragma unroll
-                    for (int ch = 0; ch < D / 8; ++ch) {
-                        const uint32_t* f = &orr[ch / 4][(ch % 4) * 8];
-                        dst[ch] = make_uint4(pack_bf16x2(__uint_as_float(f[0]) * inv, __uint_as_float(f[1]) * inv),
-                                             pack_bf16x2(__uint_as_float(f[2]) * inv, __uint_as_float(f[3]) * inv),
-                                             pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv),
-                                             pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv));
-                    }
-                }
-                if (threadIdx.x % 128 == 0) JFA_TRACE_EVENT(24, t, i, 0);
-                continue;
-            }
-            const bool tma_ok = JFA_FWD_EPI_TMA && rows_valid == 128;
-            if (JFA_FWD_EPI_TMA && !tma_ok) {  // the last store has read the stage
-                if (row == 0) bulk_wait_group_read<0>();
-                group_sync(1 + t);
-            }
 #pragma unroll
             for (int half = 0; half < D / 64; ++half) {
-                if (tma_ok) {  // the previous store (last half, or the last item's) has read the stage
-                    if (row == 0) bulk_wait_group_read<0>();
-                    group_sync(1 + t);
-                }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {  // 8 bf16 per 16-byte chunk
                     const uint32_t* f = &orr[half * 2 + ch / 4][(ch % 4) * 8];
@@ -868,15 +715,6 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
                                                pack_bf16x2(__uint_as_float(f[4]) * inv, __uint_as_float(f[5]) * inv),
                                                pack_bf16x2(__uint_as_float(f[6]) * inv, __uint_as_float(f[7]) * inv));
                     *reinterpret_cast<uint4*>(stage + row * 128 + ((ch ^ (row & 7)) * 16)) = u;
-                }
-                if (tma_ok) {
-                    fence_proxy_async_smem();
-                    group_sync(1 + t);
-                    if (row == 0) {
-                        tma_store_2d(map_o, stage, it.h * D + half * 64, static_cast<int>(row0));
-                        bulk_commit_group();
-                    }
-                    continue;
                 }
                 group_sync(1 + t);
                 // 128 rows x 8 chunks: thread k of the warpgroup copies chunks k, k+128, ...
@@ -895,7 +733,7 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
         if (row == 0) JFA_TRACE_EVENT(24, t, i, 0);
     }
 done:
-    if (JFA_FWD_EPI_TMA && row == 0) bulk_wait_group<0>();  // every O store has completed
+    return;
 }
 
 template <int D, bool kSparse, bool kMx>
@@ -909,7 +747,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __shared__ FwdBars bars;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
-    const AbortState ab{&bars.abort_flag, p.status};
+    const AbortState ab{&bars.abort_flag, p.status, p.wait_ns};
 
     JFA_TRACE_INIT();
     if (threadIdx.x == 0) {
@@ -949,7 +787,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) fwd_tma_role<D, kSparse, kMx>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            if (lane == 0) fwd_mma_role<D, kSparse, kMx>(p, smem, bars, tmem, ib, ie, ab);
+            fwd_mma_role<D, kSparse, kMx>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }

@@ -1,6 +1,8 @@
 // host_util.cu -- see host_util.h.
 #include "host_util.h"
 
+#include <atomic>
+
 #include <mutex>
 
 namespace jfa {
@@ -56,5 +58,12 @@ int device_sm_count() {
     }
     return cache[dev];
 }
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 }  // namespace jfa

@@ -19,4 +19,9 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Limit of one barrier wait inside the kernels, in nanoseconds (process-wide;
+// jfa_set_wait_limit sets it, 4 s by default).
+uint64_t wait_limit_ns();
+void set_wait_limit_ns(uint64_t ns);
+
 }  // namespace jfa

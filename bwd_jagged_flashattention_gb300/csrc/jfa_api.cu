@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -19,14 +20,6 @@ namespace {
 
 constexpr size_t kStatusBytes = 256;
 
-// Broadcast-Q dQ is summed over the batch by every CTA.  With G > 1 the
-// reduce-adds go to G partial buffers (CTA index mod G), spreading them over
-// G times more L2 lines, and a final pass adds the partials.  G = 8 measured
-// no faster than G = 1 on the ads workload, so the default is the direct sum.
-#ifndef JFA_DQ_GROUPS
-#define JFA_DQ_GROUPS 1
-#endif
-constexpr int kDqGroups = JFA_DQ_GROUPS;
 constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
 
 // Split-KV of long broadcast-Q forward items (scheduler.h); 0 turns it off
@@ -37,11 +30,14 @@ constexpr size_t kCtaStartBytes = 4096;  // (kMaxCtas + 1) int32, rounded up
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Deal policies of the two passes' schedules (jfa_set_schedule_policy).
+std::atomic<int> g_fwd_policy{kSchedLptGreedy}, g_bwd_policy{kSchedLptZigzag};
+
 // A schedule region holds the CTA bounds and the items, then (block-sparse
 // calls only) the selection tables: forward, one SparseSel per (b, h) and the
 // selected block indices; backward, the unselected tiles (ZeroTile).
 struct WsLayout {
-    size_t fwd_off, bwd_off, fwd_region, bwd_region, delta_off, delta_bytes, dqp_off, dqp_bytes, total;
+    size_t fwd_off, bwd_off, fwd_region, bwd_region, delta_off, delta_bytes, total;
     size_t sel_off, blocks_off, zero_off;  // offsets inside a region
     size_t split_off;                      // forward region: split-KV groups (broadcast Q)
     size_t opart_off, lpart_off;           // split-KV partial O / LSE (broadcast Q; 0 bytes otherwise)
@@ -63,11 +59,7 @@ bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout
     w->delta_off = w->bwd_off + w->bwd_region;
     const int64_t stat_elems = broadcast_q ? static_cast<int64_t>(B) * H * Lq : static_cast<int64_t>(H) * N;
     w->delta_bytes = align_up(static_cast<size_t>(stat_elems) * sizeof(float), 256);
-    w->dqp_off = w->delta_off + w->delta_bytes;
-    w->dqp_bytes = (broadcast_q && kDqGroups > 1)
-                       ? align_up(static_cast<size_t>(kDqGroups) * Lq * H * D * sizeof(float), 256)
-                       : 0;
-    w->opart_off = w->dqp_off + w->dqp_bytes;
+    w->opart_off = w->delta_off + w->delta_bytes;
     w->lpart_off = w->opart_off + (broadcast_q ? align_up(static_cast<size_t>(kMaxSplitSlots) * 128 * D * 4, 256) : 0);
     w->total = w->lpart_off + (broadcast_q ? align_up(static_cast<size_t>(kMaxSplitSlots) * 128 * 4, 256) : 0);
     return true;
@@ -146,7 +138,7 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
             sp.cap = w.sel_cap;
         }
         split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
-        n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, is_bwd ? kSchedLptZigzag : kSchedLptGreedy,
+        n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, is_bwd ? g_bwd_policy.load() : g_fwd_policy.load(),
                            items, cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
         if (n < 0) return JFA_ERR_WORKSPACE;
         char* dst = static_cast<char*>(ws_region);
@@ -301,8 +293,8 @@ int64_t count_items(const Problem& pr, int is_bwd) {
 // ---------------------------------------------------------------------------
 // Optional per-kernel event timing (jfa_profile_enable / jfa_profile_read).
 // ---------------------------------------------------------------------------
-enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfDqSum = 3, kProfZero = 4, kProfMerge = 5,
-                kProfQuant = 6, kProfKinds = 7 };
+enum ProfKind { kProfFwd = 0, kProfPre = 1, kProfBwd = 2, kProfZero = 3, kProfMerge = 4, kProfQuant = 5,
+                kProfKinds = 6 };
 
 struct Profiler {
     std::mutex mu;
@@ -364,6 +356,19 @@ extern "C" size_t jfa_workspace_bytes(int B, int total_len, int Lq, int H, int D
 
 extern "C" int jfa_num_ctas(void) { return ctas_for(1 << 30); }
 
+extern "C" jfa_status jfa_set_wait_limit(unsigned long long ns) {
+    set_wait_limit_ns(ns ? static_cast<uint64_t>(ns) : 4000000000ull);
+    return JFA_OK;
+}
+
+extern "C" jfa_status jfa_set_schedule_policy(int fwd_policy, int bwd_policy) {
+    auto ok = [](int v) { return v == kSchedLptZigzag || v == kSchedNaive || v == kSchedLptGreedy; };
+    if (!ok(fwd_policy) || !ok(bwd_policy)) return JFA_ERR_INVALID_ARG;
+    g_fwd_policy.store(fwd_policy);
+    g_bwd_policy.store(bwd_policy);
+    return JFA_OK;
+}
+
 // Forward for jfa_fwd (mask == NULL, v_scale == NULL), jfa_fwd_block_sparse
 // (mask) and jfa_fwd_mxfp8 (v_scale: v holds E4M3 codes).
 static jfa_status fwd_impl(const void* q, const void* k, const void* v, const int32_t* offsets_dev,
@@ -421,6 +426,7 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.wait_ns = wait_limit_ns();
     p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
     p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
     if (v_scale) {
@@ -513,21 +519,31 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     const size_t elems_kv = static_cast<size_t>(pr.N) * H * D;
     const size_t elems_q = static_cast<size_t>(q_rows) * H * D;
     char* ws = static_cast<char*>(workspace);
-    // Broadcast dQ with work to do accumulates into kDqGroups partial buffers
-    // in the workspace (zeroed here) and is summed into dq at the end; every
-    // other case accumulates into (or just zeroes) dq itself.
-    const bool partial = pr.broadcast_q && kDqGroups > 1 && o_rows > 0 && pr.N > 0;
-    float* dq_target = partial ? reinterpret_cast<float*>(ws + w.dqp_off) : dq;
-    const size_t dq_target_elems = partial ? elems_q * kDqGroups : elems_q;
-    if (q_rows > 0 && cudaMemsetAsync(dq_target, 0, dq_target_elems * sizeof(float), s) != cudaSuccess)
-        return JFA_ERR_CUDA;
-    if (o_rows == 0) {  // no query rows: every key gets a zero gradient
-        if (elems_kv && (cudaMemsetAsync(dk, 0, elems_kv * 2, s) != cudaSuccess ||
-                         cudaMemsetAsync(dv, 0, elems_kv * 2, s) != cudaSuccess))
+    if (o_rows == 0 || pr.N == 0) {
+        if (q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
+        // no query rows: every key gets a zero gradient
+        if (o_rows == 0 && elems_kv && (cudaMemsetAsync(dk, 0, elems_kv * 2, s) != cudaSuccess ||
+                                        cudaMemsetAsync(dv, 0, elems_kv * 2, s) != cudaSuccess))
             return JFA_ERR_CUDA;
         return JFA_OK;
     }
-    if (pr.N == 0) return JFA_OK;
+
+    // Stream order: schedule copy, dQ zeroing, zeroed dK/dV of unselected
+    // tiles (block-sparse), the Delta pre-pass, then the main kernel.
+    const int64_t n_items = count_items(pr, 1);
+    const int P = ctas_for(n_items);
+    int64_t n_zero = 0;
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w, mask,
+                                     ws + w.bwd_off, s, &n_zero, nullptr, &st);
+    if (n < 0) return st;
+    if (q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
+    if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
+                          return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
+                                                   n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
+                                                   D, s);
+                      }) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    if (n == 0) return JFA_OK;
 
     float* delta = reinterpret_cast<float*>(ws + w.delta_off);
     PreParams pp;
@@ -541,30 +557,12 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     pp.N = static_cast<int>(pr.N);
     pp.D = D;
     pp.broadcast_q = pr.broadcast_q;
-    if (timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess) return JFA_ERR_CUDA;
-
-    const int64_t n_items = count_items(pr, 1);
-    const int P = ctas_for(n_items);
-    int64_t n_zero = 0;
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w, mask,
-                                     ws + w.bwd_off, s, &n_zero, nullptr, &st);
-    if (n < 0) return st;
-    if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
-                          return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
-                                                   n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
-                                                   D, s);
-                      }) != cudaSuccess)
-        return JFA_ERR_CUDA;
-    if (n == 0) {
-        if (partial && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
-        return JFA_OK;
-    }
 
     BwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
         !map_rows_bf16(&maps.v, v, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dout, dout, o_rows, H, D, workspace) ||
-        !map_rows_f32(&maps.dq, dq_target, partial ? q_rows * kDqGroups : q_rows, H, D, workspace) ||
-        !map_rows_bf16(&maps.dk, dk, pr.N, H, D, workspace) || !map_rows_bf16(&maps.dv, dv, pr.N, H, D, workspace))
+        !map_rows_f32(&maps.dq, dq, q_rows, H, D, workspace) || !map_rows_bf16(&maps.dk, dk, pr.N, H, D, workspace) ||
+        !map_rows_bf16(&maps.dv, dv, pr.N, H, D, workspace))
         return JFA_ERR_CUDA;
     BwdParams p;
     p.cta_start = reinterpret_cast<const int32_t*>(ws + w.bwd_off);
@@ -579,14 +577,11 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     p.N = static_cast<int>(pr.N);
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
-    p.dq_groups = partial ? kDqGroups : 1;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
+    p.wait_ns = wait_limit_ns();
+    if (timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess) return JFA_ERR_CUDA;
     if (timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
-    if (partial && timed_launch(kProfDqSum, s, [&] {
-                       return launch_dq_sum(dq_target, dq, static_cast<int64_t>(elems_q), kDqGroups, s);
-                   }) != cudaSuccess)
-        return JFA_ERR_CUDA;
     return JFA_OK;
 }
 

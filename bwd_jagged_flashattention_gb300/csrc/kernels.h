@@ -19,6 +19,7 @@ struct FwdParams {
     int Lq, H, N;
     int broadcast_q, causal;
     float scale_log2;          // softmax scale * log2(e)
+    uint64_t wait_ns = 4000000000ull;    // limit of one barrier wait (jfa_set_wait_limit)
     const SparseSel* sel = nullptr;      // block-sparse: selection per (b, h) at b * H + h; null = dense
     const int32_t* sel_blocks = nullptr; // block-sparse: the selected block indices the records point into
     float* o_part = nullptr;             // split-KV chunks: fp32 O [slot][128][D] (null: no split items)
@@ -34,14 +35,14 @@ struct BwdParams {
     const WorkItem* items;
     const int32_t* cta_start;
     const float* lse;          // [B,H,Lq] or [H,N]
-    const float* delta;        // same layout as lse
     uint16_t* dk;              // bf16 [N,H,D]
     uint16_t* dv;              // bf16 [N,H,D]
     uint32_t* status;
     int Lq, H, N;
     int broadcast_q, causal;
-    int dq_groups;             // broadcast: number of partial dQ buffers (rows g*Lq ..)
     float scale, scale_log2;
+    uint64_t wait_ns;          // limit of one barrier wait (jfa_set_wait_limit)
+    const float* delta;        // same layout as lse (the pre-pass writes it)
 };
 
 struct PreParams {
@@ -79,9 +80,9 @@ cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cu
 // Split-KV merge of n_groups split query tiles into the broadcast O / LSE.
 cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, const float* o_part,
                              const float* lse_part, uint16_t* o, float* lse, int Lq, int H, cudaStream_t s);
+// Delta = rowsum(dO * O) in fp32 (LSE layout), before launch_bwd on the same stream.
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
-cudaError_t launch_dq_sum(const float* partial, float* dq, int64_t n, int groups, cudaStream_t s);
 // MXFP8 quantization of bf16 V [N,H,D] into E4M3 codes (same layout) and
 // E8M0 scales [NB,H,D,4]: one CTA per 128-key block (NB blocks in total;
 // block_start has B + 1 entries).

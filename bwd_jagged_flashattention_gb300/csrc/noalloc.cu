@@ -19,7 +19,14 @@
 //
 // Set-up: the first call on each device looks up the array's device address
 // with cudaGetSymbolAddress (a host-side name of a __device__ array is not a
-// device address).  Make that first call before any stream capture.
+// device address) and keeps it for the life of the process.  Make that first
+// call before any stream capture.  The cached address does not survive
+// cudaDeviceReset (the module may load elsewhere afterwards).
+//
+// The tile schedule is copied to the array from a host buffer that every call
+// rewrites, so a call on a stream that is capturing is refused
+// (JFA_ERR_UNSUPPORTED): a recorded copy would read whatever a later call
+// left in that buffer.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -57,6 +64,20 @@ std::mutex g_mu;
 void* g_scratch_addr[64] = {nullptr};
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Device address of g_scratch on the current device, looked up once per
+// device (with that device current) and cached; null on failure.  Callers
+// hold g_mu.
+char* scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!g_scratch_addr[dev]) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess || !addr) return nullptr;
+        g_scratch_addr[dev] = addr;
+    }
+    return static_cast<char*>(g_scratch_addr[dev]);
+}
 
 bool map_rows_bf16(CUtensorMap* m, const void* base, int64_t rows, int H, int D, const void* fallback) {
     const uint64_t dims[2] = {static_cast<uint64_t>(H) * D, static_cast<uint64_t>(rows > 0 ? rows : 1)};
@@ -99,15 +120,12 @@ extern "C" jfa_status jfa_fwd_static_scratch(const void* q, const void* k, const
         return JFA_ERR_UNSUPPORTED;
     if (o_rows == 0 || n_items == 0) return JFA_OK;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return JFA_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return JFA_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return JFA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_scratch) != cudaSuccess || !addr) return JFA_ERR_CUDA;
-        g_scratch_addr[dev] = addr;
-    }
-    char* scratch = static_cast<char*>(g_scratch_addr[dev]);
+    char* scratch = scratch_address();
+    if (!scratch) return JFA_ERR_CUDA;
 
     int P = device_sm_count();
     if (P <= 0) return JFA_ERR_CUDA;
@@ -141,5 +159,17 @@ extern "C" jfa_status jfa_fwd_static_scratch(const void* q, const void* k, const
     p.broadcast_q = broadcast_q ? 1 : 0;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = (scale > 0.0f ? scale : 1.0f / std::sqrt(static_cast<float>(D))) * 1.4426950408889634f;
+    p.wait_ns = wait_limit_ns();
     return launch_fwd(D, p, maps, P, s) == cudaSuccess ? JFA_OK : JFA_ERR_CUDA;
+}
+
+extern "C" jfa_status jfa_static_scratch_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    char* scratch = scratch_address();
+    if (!scratch || cudaStreamSynchronize(s) != cudaSuccess) return JFA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return JFA_ERR_CUDA;
+    if (word != 0 && cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return JFA_ERR_CUDA;
+    return word ? JFA_ERR_DEVICE_TIMEOUT : JFA_OK;
 }

@@ -20,8 +20,9 @@ enum DeviceError : uint32_t {
     kDevTimeout = 1,
 };
 
-// Wait limit: a legitimate wait in these kernels lasts microseconds.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+// Default wait limit: a legitimate wait in these kernels lasts microseconds.
+// The launches carry the limit in effect (jfa_set_wait_limit) in AbortState.
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -31,17 +32,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "elect.sync _|P, %1;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}\n"
-        : "=r"(pred)
-        : "r"(0xffffffffu));
-    return pred != 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -65,24 +55,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-// Suspend-time hint of a barrier wait, in nanoseconds: the waiting thread
-// sleeps in hardware until the phase completes (or the hint elapses) instead
-// of spinning and taking issue slots from the warps that do the work.
-#ifndef JFA_WAIT_HINT_NS
-#define JFA_WAIT_HINT_NS 1000000
-#endif
-
+// One test of a barrier phase (without a suspend-time hint: a hinted wait,
+// which sleeps in hardware until the phase completes, measured 1% slower on
+// the ads backward, 367.5 vs 371.5 us).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
     uint32_t ok;
-#if JFA_WAIT_HINT_NS > 0
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar_addr), "r"(parity), "r"(static_cast<uint32_t>(JFA_WAIT_HINT_NS))
-        : "memory");
-#else
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
         "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
@@ -90,7 +67,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         : "=r"(ok)
         : "r"(bar_addr), "r"(parity)
         : "memory");
-#endif
     return ok != 0;
 }
 
@@ -99,6 +75,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 struct AbortState {
     volatile uint32_t* smem_flag;  // CTA-local flag (shared memory)
     uint32_t* status;              // global status word (may be null)
+    uint64_t limit_ns;             // how long one wait may last
 };
 
 // Bounded wait for the phase with the given parity to complete.
@@ -109,9 +86,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if (JFA_WAIT_HINT_NS > 0 || (it & 63u) == 0) {
+        if ((it & 15u) == 0) {
             if (*ab.smem_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > ab.limit_ns) {
                 *ab.smem_flag = 1u;
                 if (ab.status) atomicOr(ab.status, 1u << kDevTimeout);
                 return false;
@@ -128,7 +105,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(a, parity)) return true;
-        if ((JFA_WAIT_HINT_NS > 0 || (it & 63u) == 0) && global_timer_ns() - t0 > kWaitLimitNs / 4) return false;
+        if ((it & 15u) == 0 && global_timer_ns() - t0 > kDefaultWaitLimitNs / 4) return false;
     }
 }
 
@@ -162,21 +139,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
-        "%5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-// Pull a tile of global memory into L2 ahead of its TMA load (no smem, no barrier).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),
@@ -191,22 +153,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, const vo
         "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
             reinterpret_cast<uint64_t>(m)),
         "r"(smem_u32(src)), "r"(x), "r"(y)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(m)),
-        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(m)),
-        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
 
@@ -336,6 +282,55 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// The same three products issued only by the thread whose `lead` is
+// nonzero (a PTX predicate, no branch): a whole warp can then run the MMA
+// role with warp-uniform control flow and operands, one lane issuing (ads
+// forward 140.0 vs 142.6 us with the role on lane 0 alone).
+__device__ __forceinline__ void mma_ss_p(uint32_t lead, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, l;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 l, %5, 0;\n\t"
+        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(lead)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_p(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, l;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 l, %5, 0;\n\t"
+        "@l tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(lead)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_mx_p(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, l;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 l, %7, 0;\n\t"
+        "@l tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"(lead)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_p(uint32_t lead, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred l;\n\t"
+        "setp.ne.b32 l, %1, 0;\n\t"
+        "@l tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar)),
+        "r"(lead)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05 async ops of
 // this thread have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -357,15 +352,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 
@@ -452,38 +438,6 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, 
         "mov.b64 {%0, %1}, rd;\n\t}\n"
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-// 2^x for a pair of values on the FMA/ALU pipes instead of the special-
-// function unit (which runs at a quarter of the FMA rate).  Our own scheme:
-//   * range reduction: t = x + 1.5*2^23 rounds x to the nearest integer n
-//     (held in t's low mantissa bits); f = x - n lies in [-1/2, 1/2];
-//   * 2^f by a degree-3 polynomial fitted for minimum relative error on
-//     [-1/2, 1/2] (iteratively reweighted least squares on Chebyshev nodes;
-//     max relative error 7.5e-5, far below the bf16 rounding of P);
-//   * 2^n by adding n to the exponent field (t's low bits shifted by 23).
-// x is clamped to >= -125 so results stay normal (callers only use this where
-// no entry is masked to -inf) and must be <= 127.
-constexpr float kExp2C0 = 0.999928057f, kExp2C1 = 0.693260968f, kExp2C2 = 0.242611140f, kExp2C3 = 0.0551716685f;
-__device__ __forceinline__ void exp2_fma2(float x0, float x1, float& y0, float& y1) {
-    x0 = fmaxf(x0, -125.0f);
-    x1 = fmaxf(x1, -125.0f);
-    float t0, t1, n0, n1, f0, f1, p0, p1;
-    fadd2(t0, t1, x0, x1, 12582912.0f, 12582912.0f);
-    fadd2(n0, n1, t0, t1, -12582912.0f, -12582912.0f);
-    fadd2(f0, f1, x0, x1, -n0, -n1);
-    ffma2(p0, p1, f0, f1, kExp2C3, kExp2C3, kExp2C2, kExp2C2);
-    ffma2(p0, p1, p0, p1, f0, f1, kExp2C1, kExp2C1);
-    ffma2(p0, p1, p0, p1, f0, f1, kExp2C0, kExp2C0);
-    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
-
-// Whether exponent pair e (of every 16) uses exp2_fma2 when N of 16 pairs
-// go to the FMA pipe (spread evenly); the rest use the special-function unit.
-template <int N>
-__host__ __device__ constexpr bool poly_pair(int e) {
-    return (e * N) % 16 < N;
 }
 
 // max of three fp32 values in one instruction (sm_100+).

@@ -8,6 +8,19 @@ namespace jfa {
 
 namespace {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Host scratch of the builders, kept per thread across calls: the schedule
+// is rebuilt on every call, and fresh allocations of this size cost more in
+// page faults than the whole build.
+struct Scratch {
+    std::vector<WorkItem> gen;
+    std::vector<int64_t> cost, order, heap, buckets;
+    std::vector<int32_t> owner, fill;
+};
+Scratch& scratch() {
+    static thread_local Scratch s;
+    return s;
+}
 }  // namespace
 
 bool head_partition(int broadcast_q, int H, int P) { return broadcast_q && H > 1 && H <= 255 && P % H == 0; }
@@ -95,14 +108,18 @@ void deal(const WorkItem* gen, const int64_t* order, const int64_t* cost, int64_
         }
         return;
     }
-    int64_t head_pos[256] = {0};
+    // Running (lane, round parity) per group instead of a division per item.
+    int lane_of[256] = {0};
+    bool odd_of[256] = {false};
     for (int64_t i = 0; i < n; ++i) {
-        if (by_head) {
-            const int h = static_cast<int>(gen[order[i]].packed & 0xFFu);
-            owner[i] = zigzag_head_cta(head_pos[h]++, h, G, H);
-        } else {
-            const int64_t r = i / P, p = i % P;
-            owner[i] = static_cast<int32_t>((policy == kSchedLptZigzag && (r & 1)) ? (P - 1 - p) : p);
+        const int g = by_head ? static_cast<int>(gen[order[i]].packed & 0xFFu) : 0;
+        const int lane = lane_of[g];
+        const bool zig = policy == kSchedLptZigzag || by_head;
+        const int slot = (zig && odd_of[g]) ? G - 1 - lane : lane;
+        owner[i] = by_head ? slot * H + g : slot;
+        if (++lane_of[g] == G) {
+            lane_of[g] = 0;
+            odd_of[g] = !odd_of[g];
         }
     }
 }
@@ -191,10 +208,55 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
                        SparseSpec* sparse, SplitSpec* split) {
     if (P <= 0 || P > kMaxCtas) return -1;
     if (sparse && causal) return -1;
+    Scratch& sc = scratch();
+    // Broadcast-Q backward without a selection or causal mask, per-head CTA
+    // groups, the pages' zigzag: every item costs the same (its ceil(Lq/128)
+    // query tiles + 1), so the cost-sorted order is the generation order and
+    // the deal is a running zigzag per head.  One pass then places every item
+    // straight into its CTA's slice of the list -- the schedule the general
+    // path below builds with its separate sort, deal and placement passes.
+    if (is_bwd && broadcast_q && !causal && !sparse && policy == kSchedLptZigzag &&
+        head_partition(broadcast_q, H, P)) {
+        const int G = P / H;
+        int64_t per_head = 0;
+        for (int b = 0; b < B; ++b) per_head += ceil_div(offsets[b + 1] - offsets[b], kTileRows);
+        if (per_head * H > max_items) return -1;
+        // Rounds of G items per head: every lane gets one item per full round;
+        // the last, partial round covers lanes 0 .. rem-1 (even round) or
+        // G-rem .. G-1 (odd round).
+        const int64_t full = per_head / G, rem = per_head % G;
+        cta_start[0] = 0;
+        for (int c = 0; c < P; ++c) {
+            const int lane = c / H;
+            const bool extra = rem > 0 && ((full & 1) ? lane >= G - rem : lane < rem);
+            cta_start[c + 1] = cta_start[c] + static_cast<int32_t>(full + (extra ? 1 : 0));
+        }
+        std::vector<int32_t>& fill = sc.fill;
+        fill.assign(cta_start, cta_start + P);
+        int lane_of[256] = {0};
+        bool odd_of[256] = {false};
+        for (int b = 0; b < B; ++b) {
+            const int32_t Lk = offsets[b + 1] - offsets[b];
+            const int64_t nkv = ceil_div(Lk, kTileRows);
+            for (int h = 0; h < H; ++h)
+                for (int64_t n = 0; n < nkv; ++n) {
+                    const int lane = lane_of[h];
+                    const int cta = (odd_of[h] ? G - 1 - lane : lane) * H + h;
+                    items[fill[cta]++] = WorkItem{b, offsets[b], Lk, pack_item(h, static_cast<int>(n), 0)};
+                    if (++lane_of[h] == G) {
+                        lane_of[h] = 0;
+                        odd_of[h] = !odd_of[h];
+                    }
+                }
+        }
+        if (split) split->n_groups = split->n_slots = 0;
+        return per_head * H;
+    }
     // 1. Generate items in (b, h, tile) order, with their costs.
-    std::vector<WorkItem> gen;
-    std::vector<int64_t> cost;
-    gen.reserve(static_cast<size_t>(std::min<int64_t>(max_items, 1 << 22)));
+    std::vector<WorkItem>& gen = sc.gen;
+    std::vector<int64_t>& cost = sc.cost;
+    gen.clear();
+    cost.clear();
     int64_t bstart = 0;  // global index of the sequence's first key block
     if (sparse) sparse->n_blocks = sparse->n_zero = 0;
     for (int b = 0; b < B; ++b) {
@@ -250,11 +312,13 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     const int64_t n = static_cast<int64_t>(gen.size());
 
     // 2. Order: cost-descending, stable (counting sort on the integer cost).
-    std::vector<int64_t> order(static_cast<size_t>(n));
+    std::vector<int64_t>& order = sc.order;
+    order.resize(static_cast<size_t>(n));
     if (policy != kSchedNaive && n > 0) {
         int64_t cmax = 0;
         for (int64_t i = 0; i < n; ++i) cmax = std::max(cmax, cost[i]);
-        std::vector<int64_t> start(static_cast<size_t>(cmax + 2), 0);
+        std::vector<int64_t>& start = sc.buckets;
+        start.assign(static_cast<size_t>(cmax + 2), 0);
         for (int64_t i = 0; i < n; ++i) ++start[cmax - cost[i] + 1];  // bucket 0 = largest cost
         for (int64_t c = 1; c <= cmax + 1; ++c) start[c] += start[c - 1];
         for (int64_t i = 0; i < n; ++i) order[start[cmax - cost[i]]++] = i;
@@ -263,14 +327,17 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     }
 
     // 3. Deal (see deal()).
-    std::vector<int32_t> owner(static_cast<size_t>(n));
-    std::vector<int64_t> heap(static_cast<size_t>(P));
+    std::vector<int32_t>& owner = sc.owner;
+    owner.resize(static_cast<size_t>(n));
+    std::vector<int64_t>& heap = sc.heap;
+    heap.resize(static_cast<size_t>(P));
     deal(gen.data(), order.data(), cost.data(), n, Lq, H, broadcast_q, causal, is_bwd, P, policy, owner.data(),
          heap.data());
     std::fill(cta_start, cta_start + P + 1, 0);
     for (int64_t i = 0; i < n; ++i) ++cta_start[owner[i] + 1];
     for (int p = 0; p < P; ++p) cta_start[p + 1] += cta_start[p];
-    std::vector<int32_t> fill(cta_start, cta_start + P);
+    std::vector<int32_t>& fill = sc.fill;
+    fill.assign(cta_start, cta_start + P);
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
     // 4. Broadcast Q: group each CTA's items by the Q tiles they read.
     if (broadcast_q && policy != kSchedNaive) group_by_q(items, cta_start, P, is_bwd);

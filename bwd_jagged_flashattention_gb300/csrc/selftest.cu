@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(128, 1)
     __shared__ uint32_t tmem_base_s;
     __shared__ uint32_t abort_flag;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    AbortState ab{&abort_flag, status};
+    AbortState ab{&abort_flag, status, kDefaultWaitLimitNs};
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -131,6 +131,42 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// Abort-path check (no fault, no trap): warp 1 waits on a barrier nothing
+// arrives at, under the given limit; warp 2 waits on another such barrier
+// with a limit 2000 times longer, so it can only return early through the
+// CTA abort flag warp 1 raises; warp 0 holds 32 TMEM columns for the
+// kernel's lifetime and frees them at the end, as the attention kernels do.
+// Every wait is bounded, so the kernel returns; out[w - 1] = 1 if warp w's
+// wait completed, 0 if it gave up.
+__global__ void __launch_bounds__(96, 1) selftest_timeout_kernel(uint32_t* status, uint64_t limit_ns, uint32_t* out) {
+    __shared__ uint64_t bars[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ uint32_t abort_flag;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_s, 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp > 0) {
+        const AbortState ab{&abort_flag, status, warp == 1 ? limit_ns : 2000 * limit_ns};
+        const bool ok = mbar_wait_warp(&bars[warp - 1], 0, ab);
+        if (lane == 0) out[warp - 1] = ok ? 1u : 0u;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem_base_s, 32);
+}
+
 bool map_128x128_bf16(CUtensorMap* m, const void* p) {
     const uint64_t dims[2] = {128, 128};
     const uint64_t strides[1] = {128 * 2};
@@ -155,5 +191,14 @@ extern "C" int jfa_selftest_mma(int mode, const void* a, const void* b, float* c
         return 4;
     selftest_mma_kernel<<<1, 128, smem, s>>>(ma, mb, static_cast<const uint16_t*>(a), c, mode,
                                              reinterpret_cast<uint32_t*>(status));
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+extern "C" int jfa_selftest_timeout(unsigned long long limit_ns, unsigned int* status, unsigned int* out,
+                                    void* stream) {
+    using namespace jfa;
+    if (!status || !out || limit_ns == 0 || limit_ns > 1000000000ull) return 1;
+    selftest_timeout_kernel<<<1, 96, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<uint32_t*>(status), static_cast<uint64_t>(limit_ns), reinterpret_cast<uint32_t*>(out));
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

@@ -104,11 +104,13 @@ jfa_status jfa_fwd(const void *q, const void *k, const void *v, const int32_t *o
 
 /*
  * jfa_bwd -- dQ, dK, dV (the backward pass) given the forward's O and LSE
- * and the upstream gradient dout.  Computes Delta = rowsum(dout * o) in the
- * workspace first.  dq is fp32 and is overwritten (zeroed, then summed over
- * every sequence in broadcast mode); dk and dv are bf16.  Other arguments as
- * for jfa_fwd.  dQ is accumulated with fp32 atomics, so its low-order bits
- * may differ from run to run; dK and dV are deterministic.
+ * and the upstream gradient dout.  A first kernel computes Delta =
+ * rowsum(dout * o) into the workspace, then the main kernel runs.  dq is
+ * fp32 and is overwritten
+ * (zeroed, then summed over every sequence in broadcast mode); dk and dv are
+ * bf16.  Other arguments as for jfa_fwd.  dQ is accumulated with fp32
+ * atomics, so its low-order bits may differ from run to run; dK and dV are
+ * deterministic.
  */
 jfa_status jfa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                    const void *dout, const int32_t *offsets_dev, const int32_t *offsets_host, int B, int Lq, int H,
@@ -204,6 +206,17 @@ int64_t jfa_num_kv_blocks(const int32_t *offsets_host, int B);
  */
 jfa_status jfa_device_status(void *workspace, void *stream);
 
+/*
+ * jfa_set_wait_limit -- how long one barrier wait inside the kernels may
+ * last before the kernel gives up (process-wide, for launches after the
+ * call; 0 restores the default of 4 s).  A wait that runs out sets the
+ * status word (JFA_ERR_DEVICE_TIMEOUT through jfa_device_status), makes the
+ * CTA's other waits give up, lets the CTA's issued copies and products
+ * finish, frees its tensor memory and returns; the outputs are then
+ * incomplete.  Legitimate waits last microseconds.
+ */
+jfa_status jfa_set_wait_limit(unsigned long long ns);
+
 /* Static, human-readable name of a status code. */
 const char *jfa_status_string(jfa_status s);
 
@@ -224,14 +237,27 @@ const char *jfa_status_string(jfa_status s);
  * enqueued.  Every call shares the array and overwrites what the previous
  * call left there; calls whose work overlaps on the GPU (other streams or
  * threads) race on it and must be serialised by the caller.  The first call
- * on each device looks up the array's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture.  A kernel wait that times
- * out is recorded in the array's status word, which this entry point clears
- * at the start of each call and does not report.
+ * on each device looks up the array's device address (cudaGetSymbolAddress)
+ * and keeps it for the rest of the process, so the entry point does not
+ * survive cudaDeviceReset; make that first call before any stream capture.
+ * The schedule is copied into the array from a host buffer that each call
+ * rewrites, so a call on a stream that is capturing returns
+ * JFA_ERR_UNSUPPORTED and enqueues nothing.  A kernel wait that times out is
+ * recorded in the array's status word, which each call clears at its start;
+ * jfa_static_scratch_status() reports it.
  */
 jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, const int32_t *offsets_host, int B,
                                   int Lq, int H, int D, int broadcast_q, int causal, float scale, void *o, float *lse,
                                   void *stream);
+
+/*
+ * jfa_static_scratch_status -- synchronises `stream`, then reads and clears
+ * the status word of jfa_fwd_static_scratch's array on the current device.
+ * Returns JFA_OK, JFA_ERR_DEVICE_TIMEOUT, or JFA_ERR_CUDA if the
+ * synchronisation or the read failed.  Like that entry point, it allocates
+ * nothing.
+ */
+jfa_status jfa_static_scratch_status(void *stream);
 
 /*
  * Measurement aid (computes nothing).  While enabled, every forward and
@@ -240,13 +266,25 @@ jfa_status jfa_fwd_static_scratch(const void *q, const void *k, const void *v, c
  * events and writes, for kernel kind k < count, the summed milliseconds into
  * ms[k] and the launch count into launches[k] (either pointer may be NULL),
  * then clears the totals.  Kinds: 0 forward kernel, 1 backward Delta
- * pre-pass, 2 backward main kernel, 3 broadcast dQ partial sum, 4 block-sparse
- * zeroing of unselected dK/dV tiles, 5 split-KV merge, 6 MXFP8 quantization
- * of V.  The events
+ * pre-pass, 2 backward main kernel, 3 block-sparse zeroing of unselected
+ * dK/dV tiles, 4 split-KV merge, 5 MXFP8 quantization of V.  The events
  * are host-owned CUDA events; no device memory is allocated.
  */
 jfa_status jfa_profile_enable(int on);
 jfa_status jfa_profile_read(double *ms, int *launches, int count);
+
+/*
+ * jfa_set_schedule_policy -- measurement aid: how later calls deal their
+ * sorted work items to the persistent CTAs (process-wide, all devices).
+ * 0 = longest first, zigzag over the CTAs (the pages' deal: Meta's TLX
+ * Jagged Flash Attention Beats FA4 on Blackwell With 3x Less Code, section
+ * "Optimizations layered on top"); 1 = generation order, round-robin (no
+ * balancing); 2 = longest first, each item to the least-loaded CTA.
+ * Defaults: 2 for the forward, 0 for the backward.  Results do not depend on
+ * the policy (up to dQ's summation order); only the time does.  Returns
+ * JFA_ERR_INVALID_ARG for another value.
+ */
+jfa_status jfa_set_schedule_policy(int fwd_policy, int bwd_policy);
 
 /*
  * jfa_num_ctas -- number of persistent CTAs the kernels launch on the current

@@ -32,6 +32,19 @@ extern "C" {
  */
 int jfa_selftest_mma(int mode, const void *a, const void *b, float *c, unsigned int *status, void *stream);
 
+/*
+ * jfa_selftest_timeout -- exercises the kernels' failure path without a
+ * fault: one CTA whose warp 1 waits on a barrier nothing ever completes,
+ * bounded by limit_ns (1 ns .. 1 s), and whose warp 2 waits the same way
+ * with a limit 2000 times longer, so it returns early only if the CTA abort
+ * flag that warp 1's timeout raises reaches it.  The CTA also holds tensor
+ * memory, which it frees before returning.  On return, *status (device
+ * uint32) has the timeout bit set and out[0..1] (device uint32) are 0 for
+ * each warp that gave up.  Asynchronous on `stream`.  Returns 0 on launch,
+ * 1 on a bad argument, 4 on a CUDA error.  Allocates nothing.
+ */
+int jfa_selftest_timeout(unsigned long long limit_ns, unsigned int *status, unsigned int *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

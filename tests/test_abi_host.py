@@ -53,6 +53,15 @@ def test_workspace_bytes(jfa):
     assert lib.jfa_workspace_bytes(-1, 100, 32, 2, 64, 1, 0) == 0
     j = lib.jfa_workspace_bytes(32, 139000, 0, 16, 128, 0, 1)
     assert j >= 16 * 139000 * 4
+    # The boundary's form: (B, total_len, Lq, H, D, broadcast_q, causal), no is_bwd
+    # flag (one workspace serves both passes).  total_len sizes the jagged
+    # Delta [H, N]: 1000 more rows need at least 1000 * H * 4 more bytes.
+    assert len(lib.jfa_workspace_bytes.argtypes) == 7
+    j2 = lib.jfa_workspace_bytes(32, 140000, 0, 16, 128, 0, 1)
+    assert j2 - j >= 1000 * 16 * 4
+    # Broadcast Delta [B, H, Lq]: doubling Lq adds at least B * H * Lq * 4 bytes.
+    a2 = lib.jfa_workspace_bytes(512, 190000, 512, 4, 128, 1, 0)
+    assert a2 - a >= 512 * 4 * 256 * 4
 
 
 # Fake, never-dereferenced device addresses: validation must reject these

@@ -6,7 +6,7 @@ Where the fp64 oracle can afford the whole workload it checks every element
 (tiny; ads forward; ads forward+backward).  Elsewhere it checks sampled
 outputs it can compute on their own: whole sequences x heads (sliced out of
 the same inputs) for O, LSE, dK, dV and the per-sequence dQ, and, for the
-broadcast dQ that sums over every sequence, one head over the whole batch.
+broadcast dQ that sums over every sequence, every head over the whole batch.
 """
 import pytest
 import torch
@@ -114,11 +114,12 @@ def test_dense_llm_sampled():
 def test_extreme_sampled():
     x = jfa_inputs.make("extreme")
     got = gpu_fwd_bwd(x)
-    # broadcast dQ sums over all 2048 sequences: check head 0 over the whole batch
-    y = _slice_heads(x, 0)
-    dq_ref, _, _ = oracle.bwd(y["q"], y["k"], y["v"], y["do"], y["offsets"], y["Lq"], True, False, y["scale"],
-                              want_dkv=False)
-    check_grad(got["dq"][:, 0:1], dq_ref, "extreme dQ head 0")
+    # broadcast dQ sums over all 2048 sequences: check every head over the whole batch
+    for h in range(x["H"]):
+        y = _slice_heads(x, h)
+        dq_ref, _, _ = oracle.bwd(y["q"], y["k"], y["v"], y["do"], y["offsets"], y["Lq"], True, False, y["scale"],
+                                  want_dkv=False)
+        check_grad(got["dq"][:, h:h + 1], dq_ref, f"extreme dQ head {h}")
     L = (x["offsets"][1:] - x["offsets"][:-1])
     order = torch.argsort(L).tolist()
     seqs = order[:3] + order[len(order) // 2: len(order) // 2 + 2] + order[-2:]

@@ -25,7 +25,7 @@ EDGE_LENGTHS = [1, 127, 128, 129, 255, 256, 257]
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("Lq", [1, 32, 129, 256])
+@pytest.mark.parametrize("Lq", [1, 32, 128, 129, 256])
 def test_broadcast_tile_edges(D, Lq):
     x = jfa_inputs.custom(len(EDGE_LENGTHS), Lq, 2, D, EDGE_LENGTHS, True, False, seed=Lq + D)
     _run(x, f"broadcast D={D} Lq={Lq}")
