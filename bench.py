@@ -666,16 +666,19 @@ def main():
     if not args.batch and world == 1:
         ablation = {}
         n_ab = max(20, min(args.steps, 100))
-        for pol_name, pol in (("lpt_greedy", jfa.SCHED_GREEDY), ("lpt_zigzag", jfa.SCHED_ZIGZAG),
-                              ("naive_round_robin", jfa.SCHED_NAIVE)):
-            jfa.set_schedule_policy(pol, pol)
+        for pol_name, fpol, bpol in (("lpt_greedy", jfa.SCHED_GREEDY, jfa.SCHED_GREEDY),
+                                     ("lpt_zigzag", jfa.SCHED_ZIGZAG, jfa.SCHED_ZIGZAG),
+                                     ("naive_round_robin", jfa.SCHED_NAIVE, jfa.SCHED_NAIVE),
+                                     ("cluster_launch_control", jfa.SCHED_GREEDY, jfa.SCHED_CLC)):
+            jfa.set_schedule_policy(fpol, bpol)
             for _ in range(3):
                 step()
             _, f_l, b_l, _ = timed_steps(n_ab)
             ablation[pol_name] = {"fwd_ms": statistics.mean(f_l), "bwd_ms": statistics.mean(b_l) if backward else None}
         jfa.set_schedule_policy()  # the library's defaults: greedy forward, zigzag backward
         ablation["note"] = (f"{n_ab} steps per policy, same inputs; the library deals the forward lpt_greedy and "
-                            f"the backward lpt_zigzag")
+                            f"the backward lpt_zigzag; cluster_launch_control deals the backward at run time "
+                            f"(one CTA per item, resident CTAs taking over those not started), forward lpt_greedy")
 
     # Per-kernel live timing -> rooflines.
     peaks = load_peaks()

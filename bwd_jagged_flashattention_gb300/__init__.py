@@ -344,7 +344,7 @@ def num_ctas() -> int:
     return int(lib().jfa_num_ctas())
 
 
-SCHED_ZIGZAG, SCHED_NAIVE, SCHED_GREEDY = 0, 1, 2  # deal policies (SCHED_GREEDY is the library's)
+SCHED_ZIGZAG, SCHED_NAIVE, SCHED_GREEDY, SCHED_CLC = 0, 1, 2, 3  # deal policies (SCHED_CLC: backward only)
 
 
 def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool, is_bwd: bool, P: int,

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libjfa.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["jfa_api.cu", "fwd.cu", "bwd.cu", "mxfp8.cu", "host_util.cu", "selftest.cu", "scheduler.cpp", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "kernels.h", "scheduler.h", "host_util.h", "trace.cuh"]
+HEADERS = ["ptx.cuh", "kernels.h", "scheduler.h", "host_util.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,19 +44,10 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None, trace: bool = False,
-          defines: list[str] | None = None, tag: str = "") -> str:
-    """Compile (if stale) and link libjfa.so.  Returns its path.
-
-    trace=True builds the separate event-trace variant libjfa_trace.so
-    (-DJFA_TRACE), used only to study the kernels' pipelines.  `defines`
-    with a `tag` builds a separately named variant (tuning experiments)."""
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
+    """Compile (if stale) and link libjfa.so.  Returns its path."""
     nvcc = _nvcc()
-    if trace:
-        tag = "trace" + tag
-    defines = list(defines or []) + (["JFA_TRACE"] if trace else [])
-    build_dir = BUILD_DIR + (f"_{tag}" if tag else "")
-    lib_path = LIB_PATH.replace("libjfa.so", f"libjfa_{tag}.so") if tag else LIB_PATH
+    build_dir, lib_path = BUILD_DIR, LIB_PATH
     os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "jfa.h"),
                                                         os.path.join(ROOT, "include", "jfa_selftest.h")]
@@ -66,7 +57,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
         obj = os.path.join(build_dir, src.replace(".", "_") + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + hdrs):
-            cmds.append([nvcc] + _flags(verbose_ptxas) + [f"-D{d}" for d in defines] + ["-c", path, "-o", obj])
+            cmds.append([nvcc] + _flags(verbose_ptxas) + ["-c", path, "-o", obj])
     if cmds:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(cmds), os.cpu_count() or 4)) as ex:
             results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), cmds))
@@ -86,4 +77,4 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

@@ -31,14 +31,21 @@
 //                   (thread r = key row r = TMEM lane r); dV / dK epilogue
 //   warps 8-11      dQ readout + reduce-add
 //   warp  12        loads: K, V per item; Q_i (+ LSE_i), dO_i, Delta_i per tile
+//                   (with Cluster Launch Control also the run-time deal)
 //   warp  13        tcgen05 MMA issue and TMEM allocation
-//   warps 14-15     Delta producers
+//   warp  14        the MMA warp's barrier waits (see bwd_mma_role)
+//   warp  15        idle (it completes the fourth warpgroup)
 #include <cuda_runtime.h>
+#include <climits>
 
 #include "host_util.h"
 #include "kernels.h"
 #include "ptx.cuh"
-#include "trace.cuh"
+
+#ifndef JFA_BWD_WAITER
+#define JFA_BWD_WAITER 0
+#endif
+
 
 namespace jfa {
 namespace {
@@ -58,6 +65,9 @@ constexpr int kWarpDq = 4 * kCW;        // first warp of the dQ warpgroup
 constexpr int kWarpLoad = 4 * kCW + 4;
 constexpr int kWarpMma = 4 * kCW + 5;
 constexpr float kLog2e = 1.4426950408889634f;
+// Named barrier of the MMA warp and its waiter warp (0 is __syncthreads, 1 the
+// dQ warpgroup's, 2-3 the compute warpgroups').
+constexpr int kMmaSyncBar = 4;
 
 template <int D>
 struct BwdLayout {
@@ -78,7 +88,18 @@ struct BwdLayout {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDK = 256, kColDV = 256 + D;
 };
 
+// Items of a CTA in the Cluster Launch Control mode: the load warp publishes
+// each item index through a small ring, the other roles read it from there.
+constexpr int kItemQ = 4;
+// Readers of a ring slot: the MMA warp (and its waiter warp), the compute
+// warps and the dQ warps (lane 0 of each arrives once it has the index).
+constexpr uint32_t kItemReaders = (JFA_BWD_WAITER ? 2 : 1) + 4 * kCW + 4;
+
 struct BwdBars {
+    alignas(16) uint32_t clc_resp[4];  // Cluster Launch Control response (16 bytes)
+    uint64_t clc_bar;
+    uint64_t iq_full[kItemQ], iq_empty[kItemQ];
+    int32_t item_q[kItemQ];
     uint64_t k_full, k_empty, v_full, v_empty;
     uint64_t q_full[2], q_empty[2];
     uint64_t dl_full[2];  // Delta of the query tile in stats stage [st] is staged
@@ -109,6 +130,23 @@ __device__ __forceinline__ BwdItem decode_bwd(const WorkItem& w, const BwdParams
     it.i1 = (it.q_rows + 127) / 128;
     return it;
 }
+
+// Cluster Launch Control: the item index each role takes next from the
+// ring the load warp fills (-1 at the end, or when the CTA aborts).  The
+// roles keep the static schedule's loop over [ib, ie) -- with ie = INT_MAX in
+// this mode -- and replace its counter by the index read here.
+struct ItemRing {
+    uint32_t n = 0;  // ring slots read so far
+    __device__ __forceinline__ int read(BwdBars& bars, const AbortState& ab) {
+        const int slot = static_cast<int>(n % kItemQ);
+        if (!mbar_wait_warp(&bars.iq_full[slot], (n / kItemQ) & 1, ab)) return -1;
+        ++n;
+        const int v = *reinterpret_cast<volatile int32_t*>(&bars.item_q[slot]);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&bars.iq_empty[slot]);
+        return v;
+    }
+};
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -196,7 +234,7 @@ __device__ __forceinline__ int64_t stat_index(const BwdParams& p, const BwdItem&
 // ---------------------------------------------------------------------------
 // Load warp (all 32 lanes: lane 0 issues TMA, every lane stages statistics).
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kDyn>
 __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* smem, BwdBars& bars, int ib, int ie,
                               const AbortState& ab) {
     using L = BwdLayout<D>;
@@ -212,12 +250,33 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
     // is already resident is not loaded again (the statistics still are).
     // Key = head << 16 | tile (tiles < 2^16 since Lq <= 2^23); -1 = empty.
     int stage_key0 = -1, stage_key1 = -1;
-    for (int idx = ib; idx < ie; ++idx) {
+    // Cluster Launch Control: this CTA's own item first, then every CTA it
+    // cancels before that one starts; each index goes to the other roles
+    // through the ring (-1 last).
+    int cur = static_cast<int>(blockIdx.x);
+    uint32_t published = 0, clc_phase = 0;
+    bool clc_inflight = false;
+    for (int k = ib; k < ie; ++k) {
+        int idx = k;
+        if constexpr (kDyn) {
+            idx = cur;
+            const int slot = static_cast<int>(published % kItemQ);
+            if (!mbar_wait_warp(&bars.iq_empty[slot], ((published / kItemQ) & 1) ^ 1, ab)) goto done;
+            if (lane == 0) {
+                bars.item_q[slot] = idx;
+                mbar_arrive(&bars.iq_full[slot]);
+            }
+            ++published;
+            if (idx < 0) break;
+            if (lane == 0) {  // ask for the next item while this one's tiles load
+                mbar_arrive_expect_tx(&bars.clc_bar, 16);
+                clc_try_cancel(bars.clc_resp, &bars.clc_bar);
+            }
+            clc_inflight = true;
+        }
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int kv_row = it.kv_start + 128 * it.n;
-        if (lane == 0) JFA_TRACE_EVENT(1, 8, idx, 0);
         if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
-        if (lane == 0) JFA_TRACE_EVENT(2, 8, idx, 0);
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars.k_full, L::kTileBytes);
 #pragma unroll
@@ -233,7 +292,6 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                 tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.v_full, it.h * D + 64 * s, kv_row);
         }
         ++v_cnt;
-        if (lane == 0) JFA_TRACE_EVENT(3, 8, idx, 0);
 
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
@@ -273,7 +331,6 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                     stage_key1 = key;
             }
             ++q_cnt;
-            if (lane == 0) JFA_TRACE_EVENT(4, 8, i, 0);
             if (!mbar_wait_warp(&bars.do_empty, (do_cnt & 1) ^ 1, ab)) goto done;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars.do_full, L::kTileBytes);
@@ -283,7 +340,6 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                                 it.o_row0 + 128 * i);
             }
             ++do_cnt;
-            if (lane == 0) JFA_TRACE_EVENT(5, 8, i, 0);
             // Delta_i, from the pre-pass.
             {
                 float dl[4];
@@ -297,9 +353,20 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
                 if (lane == 0) mbar_arrive(&bars.dl_full[st]);
             }
         }
+        if constexpr (kDyn) {  // the next item: a canceled CTA's index, or -1 when none is left
+            if (!mbar_wait_warp(&bars.clc_bar, clc_phase & 1, ab)) goto done;
+            ++clc_phase;
+            clc_inflight = false;
+            cur = clc_response_ctaid_x(bars.clc_resp);
+            if (cur >= p.n_items) {  // not an index of this grid: stop (and report it) rather than read past the list
+                if (lane == 0 && p.status) atomicOr(p.status, 1u << kDevTimeout);
+                cur = -1;
+            }
+        }
     }
 done:
-    // Let every issued copy land before the CTA can exit.
+    // Let every issued copy (and a pending launch-control response) land before the CTA can exit.
+    if (lane == 0 && clc_inflight) mbar_wait_drain(&bars.clc_bar, clc_phase & 1);
     if (lane == 0) {
         if (k_cnt) mbar_wait_drain(&bars.k_full, (k_cnt - 1) & 1);
         if (v_cnt) mbar_wait_drain(&bars.v_full, (v_cnt - 1) & 1);
@@ -316,13 +383,27 @@ done:
 // reuses dQ's columns -- and on the last tile the release of K come one
 // product sooner.
 // ---------------------------------------------------------------------------
-template <int D>
+// kIssuer: the warp that issues the products.  With JFA_BWD_WAITER a second
+// warp runs the same function with kIssuer = false: it takes every barrier
+// wait and hands the outcome to the issuing warp through a named barrier, so
+// the issuing warp performs no memory operation between product groups (one
+// there, a wait even on a completed barrier included, leaves the tensor pipe
+// idle for ~100-175 clocks).  Both warps walk identical loops over identical
+// inputs (with Cluster Launch Control both read every index off the ring), so
+// they meet at every barrier, and an abort reaches both there.
+template <int D, bool kDyn, bool kIssuer>
 __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = BwdLayout<D>;
     // The whole warp runs this role (uniform control flow and operands); only
-    // lane 0 issues the products and commits.
-    const uint32_t lead = (threadIdx.x & 31) == 0 ? 1u : 0u;
+    // lane 0 of the issuing warp issues the products and commits.
+    const uint32_t lead = kIssuer && (threadIdx.x & 31) == 0 ? 1u : 0u;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if constexpr (!JFA_BWD_WAITER) return mbar_wait(bar, parity, ab);
+        bool failed = false;
+        if constexpr (!kIssuer) failed = !mbar_wait_warp(bar, parity, ab);
+        return !bar_red_or(kMmaSyncBar, 64, failed);
+    };
     const uint64_t dK_k = kmajor_desc(smem_u32(smem + L::kK)), dK_mn = mnmajor_desc(smem_u32(smem + L::kK));
     const uint64_t dV_k = kmajor_desc(smem_u32(smem + L::kV));
     const uint64_t dQ_k = kmajor_desc(smem_u32(smem + L::kQ)), dQ_mn = mnmajor_desc(smem_u32(smem + L::kQ));
@@ -330,68 +411,80 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
     const uint64_t dDS_k = kmajor_desc(smem_u32(smem + L::kDS)), dDS_mn = mnmajor_desc(smem_u32(smem + L::kDS));
     constexpr uint64_t kTileUnits = L::kTileBytes / 16;
     uint32_t it_cnt = 0, q_cnt = 0, tile_cnt = 0;
-    for (int idx = ib; idx < ie; ++idx) {
+    ItemRing ring;
+    for (int k = ib; k < ie; ++k) {
+        int idx = k;
+        if constexpr (kDyn) {
+            idx = ring.read(bars, ab);
+            // Both warps read the same slot; they must also leave together
+            // when either read ends the stream or gives up.
+            const bool stop = JFA_BWD_WAITER ? bar_red_or(kMmaSyncBar, 64, idx < 0) : idx < 0;
+            if (stop) break;
+        }
         const BwdItem it = decode_bwd(p.items[idx], p);
-        if (lead) JFA_TRACE_EVENT(10, 9, idx, 0);
-        if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
-        if (lead) JFA_TRACE_EVENT(11, 9, idx, 0);
-        if (!mbar_wait(&bars.v_full, it_cnt & 1, ab)) goto done;
-        if (lead) JFA_TRACE_EVENT(12, 9, idx, 0);
+        if (!wait(&bars.k_full, it_cnt & 1)) goto done;
+        if (!wait(&bars.v_full, it_cnt & 1)) goto done;
         {  // S^T of the item's first query tile
             const int st = q_cnt % 2;
-            if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
-            if (lead) JFA_TRACE_EVENT(13, 9, it.i0, 0);
-            tc_fence_after();
-            issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
-            mma_commit_p(lead, &bars.s_full);
+            if (!wait(&bars.q_full[st], (q_cnt / 2) & 1)) goto done;
+            if constexpr (kIssuer) {
+                tc_fence_after();
+                issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
+                mma_commit_p(lead, &bars.s_full);
+            }
         }
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
-            if (!mbar_wait(&bars.do_full, tile_cnt & 1, ab)) goto done;
-            if (lead) JFA_TRACE_EVENT(15, 9, i, 0);
-            if (!mbar_wait(&bars.dq_empty, (tile_cnt & 1) ^ 1, ab)) goto done;  // previous dQ read out
-            if (lead) JFA_TRACE_EVENT(16, 9, i, 0);
-            tc_fence_after();
-            issue_kmajor<D>(lead, tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
-            mma_commit_p(lead, &bars.dp_full);
-            if (i == it.i1 - 1) mma_commit_p(lead, &bars.v_empty);
-            if (i == it.i0) {  // the previous item's dV has been read out of TMEM
-                if (!mbar_wait(&bars.dv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
-                if (lead) JFA_TRACE_EVENT(18, 9, i, 0);
+            if (!wait(&bars.do_full, tile_cnt & 1)) goto done;
+            if (!wait(&bars.dq_empty, (tile_cnt & 1) ^ 1)) goto done;  // previous dQ read out
+            if constexpr (kIssuer) {
+                tc_fence_after();
+                issue_kmajor<D>(lead, tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
+                mma_commit_p(lead, &bars.dp_full);
+                if (i == it.i1 - 1) mma_commit_p(lead, &bars.v_empty);
             }
-            if (!mbar_wait(&bars.p_full, tile_cnt & 1, ab)) goto done;
-            if (lead) JFA_TRACE_EVENT(19, 9, i, 0);
-            tc_fence_after();
-            issue_dv<D>(lead, tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
-            mma_commit_p(lead, &bars.do_empty);
+            if (i == it.i0) {  // the previous item's dV has been read out of TMEM
+                if (!wait(&bars.dv_empty, (it_cnt & 1) ^ 1)) goto done;
+            }
+            if (!wait(&bars.p_full, tile_cnt & 1)) goto done;
+            if constexpr (kIssuer) {
+                tc_fence_after();
+                issue_dv<D>(lead, tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
+                mma_commit_p(lead, &bars.do_empty);
+            }
             if (i + 1 < it.i1) {  // next tile's S^T (the compute warps keep P in registers)
                 const int st2 = (q_cnt + 1) % 2;
-                if (!mbar_wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1, ab)) goto done;
-                tc_fence_after();
-                issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
-                mma_commit_p(lead, &bars.s_full);
+                if (!wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1)) goto done;
+                if constexpr (kIssuer) {
+                    tc_fence_after();
+                    issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
+                    mma_commit_p(lead, &bars.s_full);
+                }
             }
-            if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
-            if (lead) JFA_TRACE_EVENT(20, 9, i, 0);
+            if (!wait(&bars.ds_full, tile_cnt & 1)) goto done;
             if (i == it.i0) {  // ... and its dK
-                if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+                if (!wait(&bars.dk_empty, (it_cnt & 1) ^ 1)) goto done;
             }
-            tc_fence_after();
-            issue_dq<D>(lead, tmem + L::kColDP, dDS_mn, dK_mn);
-            mma_commit_p(lead, &bars.dq_full);
-            if (i == it.i1 - 1) mma_commit_p(lead, &bars.k_empty);
-            issue_dk<D>(lead, tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
-            mma_commit_p(lead, &bars.q_empty[st]);
-            mma_commit_p(lead, &bars.ds_empty);
+            if constexpr (kIssuer) {
+                tc_fence_after();
+                issue_dq<D>(lead, tmem + L::kColDP, dDS_mn, dK_mn);
+                mma_commit_p(lead, &bars.dq_full);
+                if (i == it.i1 - 1) mma_commit_p(lead, &bars.k_empty);
+                issue_dk<D>(lead, tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
+                mma_commit_p(lead, &bars.q_empty[st]);
+                mma_commit_p(lead, &bars.ds_empty);
+            }
             ++q_cnt;
             ++tile_cnt;
         }
-        mma_commit_p(lead, &bars.dkv_full);
+        if constexpr (kIssuer) mma_commit_p(lead, &bars.dkv_full);
         ++it_cnt;
     }
 done:
-    mma_commit_p(lead, &bars.mma_done);
-    mbar_wait_drain(&bars.mma_done, 0);
+    if constexpr (kIssuer) {
+        mma_commit_p(lead, &bars.mma_done);
+        mbar_wait_drain(&bars.mma_done, 0);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -457,8 +550,13 @@ __device__ __forceinline__ void bwd_compute_ds_cols(const float* delta, uint32_t
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int e = 2 * e2 + h;
-                const float d0 = bf16lo_to_f32(pkeep[cc * 16 + e]) * (__uint_as_float(dp[2 * e]) - (h ? f.z : f.x));
-                const float d1 = bf16hi_to_f32(pkeep[cc * 16 + e]) * (__uint_as_float(dp[2 * e + 1]) - (h ? f.w : f.y));
+                const float p0 = bf16lo_to_f32(pkeep[cc * 16 + e]), p1 = bf16hi_to_f32(pkeep[cc * 16 + e]);
+                // dS = P (dP - Delta) as P dP - P Delta: one paired multiply
+                // and one paired FMA per two columns (ads step: 8 us less
+                // than two scalar subtract-multiply pairs).
+                float d0, d1, n0, n1;
+                fmul2(n0, n1, p0, p1, -(h ? f.z : f.x), -(h ? f.w : f.y));
+                ffma2(d0, d1, p0, p1, __uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1]), n0, n1);
                 pk[e] = pack_bf16x2(d0, d1);
             }
         }
@@ -481,7 +579,7 @@ __device__ __forceinline__ void handoff_arrive(uint64_t* bar) {
     mbar_arrive(bar);
 }
 
-template <int D>
+template <int D, bool kDyn>
 __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_t* smem, BwdBars& bars,
                                  uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = BwdLayout<D>;
@@ -492,19 +590,22 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
     const uint32_t dp_addr = tmem + lane_off + L::kColDP;
     uint8_t* ds_tile = smem + L::kDS;
     uint32_t q_cnt = 0, tile_cnt = 0, item_cnt = 0;
-    for (int idx = ib; idx < ie; ++idx, ++item_cnt) {
+    ItemRing ring;
+    for (int k = ib; k < ie; ++k, ++item_cnt) {
+        int idx = k;
+        if constexpr (kDyn) {
+            if ((idx = ring.read(bars, ab)) < 0) break;
+        }
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int key = 128 * it.n + row;
         const bool row_valid = key < it.Lk;
         const bool kv_full_tile = 128 * (it.n + 1) <= it.Lk;
-        if (threadIdx.x == 0) JFA_TRACE_EVENT(30, 0, idx, 0);
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             const float* lse2 = reinterpret_cast<const float*>(smem + L::kStats + st * 1024);
             const float* delta = lse2 + 128;
             if (!mbar_wait_warp(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
             if (!mbar_wait_warp(&bars.s_full, tile_cnt & 1, ab)) goto done;
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(31, 0, i, 0);
             tc_fence_after();
             const bool unmasked = kv_full_tile && 128 * (i + 1) <= it.q_rows && !(p.causal && i == it.n);
             uint32_t pkeep[32];
@@ -512,13 +613,10 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                 bwd_compute_p_cols<D, false>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, 2 * wg, pkeep);
             else
                 bwd_compute_p_cols<D, true>(p, lse2, s_addr, key, 128 * i, it.q_rows, row_valid, 2 * wg, pkeep);
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(32, 0, i, 0);
             handoff_arrive(&bars.p_full);
             if (!mbar_wait_warp(&bars.dp_full, tile_cnt & 1, ab)) goto done;
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(33, 0, i, 0);
             if (!mbar_wait_warp(&bars.ds_empty, (tile_cnt & 1) ^ 1, ab)) goto done;
             if (!mbar_wait_warp(&bars.dl_full[st], (q_cnt / 2) & 1, ab)) goto done;
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(34, 0, i, 0);
             tc_fence_after();
             if (i == it.i0) {  // the last item's dK/dV stores have read the tile
                 if (row == 0) bulk_wait_group_read<0>();
@@ -526,7 +624,6 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
             }
             bwd_compute_ds_cols<D>(delta, dp_addr, ds_tile, row, 2 * wg, pkeep);
             fence_proxy_async_smem();
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(35, 0, i, 0);
             handoff_arrive(&bars.ds_full);
             ++q_cnt;
             ++tile_cnt;
@@ -541,7 +638,6 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
         // after its last half is read.
         {
             if (!mbar_wait_warp(&bars.dkv_full, item_cnt & 1, ab)) goto done;
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(36, 0, idx, 0);
             tc_fence_after();
             const int rows_valid = min(128, it.Lk - 128 * it.n);
             const int64_t row0 = static_cast<int64_t>(it.kv_start) + 128 * it.n;
@@ -597,7 +693,6 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                 }
                 compute_sync(wg);
             }
-            if (threadIdx.x == 0) JFA_TRACE_EVENT(37, 0, idx, 0);
         }
     }
 done:
@@ -608,7 +703,7 @@ done:
 // dQ warpgroup: TMEM dQ -> registers (release TMEM) -> two 128x16 fp32 smem
 // stages -> TMA bulk reduce-add into global dQ.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool kDyn>
 __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8_t* smem, BwdBars& bars,
                             uint32_t tmem, int ib, int ie, const AbortState& ab) {
     using L = BwdLayout<D>;
@@ -619,19 +714,22 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
     uint8_t* stage_base = smem + L::kDQ;
     uint32_t tile_cnt = 0, stage_uses = 0;
     if (issuer) prefetch_tensormap(map_dq);
-    for (int idx = ib; idx < ie; ++idx) {
+    ItemRing ring;
+    for (int k = ib; k < ie; ++k) {
+        int idx = k;
+        if constexpr (kDyn) {
+            if ((idx = ring.read(bars, ab)) < 0) break;
+        }
         const BwdItem it = decode_bwd(p.items[idx], p);
         for (int i = it.i0; i < it.i1; ++i) {
             bool ok = mbar_wait_warp(&bars.dq_full, tile_cnt & 1, ab);
             if (!group_all(1, ok)) goto done;
-            if (issuer) JFA_TRACE_EVENT(41, 4, i, 0);
             tc_fence_after();
             uint32_t v[D / 32][32];
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_ld32(dq_addr + c * 32, v[c]);
             tmem_ld_wait();
             handoff_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
-            if (issuer) JFA_TRACE_EVENT(42, 4, i, 0);
 #pragma unroll
             for (int sl = 0; sl < D / 16; ++sl) {
                 const int st = stage_uses % 2;
@@ -655,7 +753,6 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
                 }
                 ++stage_uses;
             }
-            if (issuer) JFA_TRACE_EVENT(43, 4, i, 0);
             ++tile_cnt;
         }
     }
@@ -663,20 +760,25 @@ done:
     if (issuer) bulk_wait_group<0>();
 }
 
-template <int D>
+template <int D, bool kDyn>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     jfa_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps maps) {
     using L = BwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ BwdBars bars;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
+    const int warp = threadIdx.x / 32;
+    const int ib = kDyn ? 0 : p.cta_start[blockIdx.x];
+    const int ie = kDyn ? INT_MAX : p.cta_start[blockIdx.x + 1];  // dynamic: the roles stop at a -1 index
     const AbortState ab{&bars.abort_flag, p.status, p.wait_ns};
 
-    JFA_TRACE_INIT();
     if (threadIdx.x == 0) {
         bars.abort_flag = 0;
+        mbar_init(&bars.clc_bar, 1);
+        for (int s = 0; s < kItemQ; ++s) {
+            mbar_init(&bars.iq_full[s], 1);
+            mbar_init(&bars.iq_empty[s], kItemReaders);
+        }
         mbar_init(&bars.k_full, 1);
         mbar_init(&bars.k_empty, 1);
         mbar_init(&bars.v_full, 1);
@@ -712,16 +814,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (warp < kWarpDq) {
         regs_dec<kComputeRegs>();
-        bwd_compute_role<D>(p, &maps, smem, bars, tmem, ib, ie, ab);
+        bwd_compute_role<D, kDyn>(p, &maps, smem, bars, tmem, ib, ie, ab);
     } else if (warp < kWarpDq + 4) {
         regs_inc<kDqRegs>();
-        bwd_dq_role<D>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);
+        bwd_dq_role<D, kDyn>(p, &maps.dq, smem, bars, tmem, ib, ie, ab);
     } else {
         regs_dec<kAuxRegs>();
         if (warp == kWarpLoad) {
-            bwd_load_role<D>(p, &maps, smem, bars, ib, ie, ab);
+            bwd_load_role<D, kDyn>(p, &maps, smem, bars, ib, ie, ab);
         } else if (warp == kWarpMma) {
-            bwd_mma_role<D>(p, smem, bars, tmem, ib, ie, ab);
+            bwd_mma_role<D, kDyn, true>(p, smem, bars, tmem, ib, ie, ab);
+            __syncwarp();
+        } else if (JFA_BWD_WAITER && warp == kWarpMma + 1) {
+            bwd_mma_role<D, kDyn, false>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }
@@ -732,22 +837,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (warp == kWarpMma) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-template <int D>
-cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
+template <int D, bool kDyn>
+cudaError_t launch_bwd_dk(const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
     using L = BwdLayout<D>;
     static bool configured = false;
     if (!configured) {
         // The register split is only safe at exactly kLaunchRegs per thread.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_bwd_kernel<D>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, jfa_bwd_kernel<D, kDyn>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
-        e = cudaFuncSetAttribute(jfa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+        e = cudaFuncSetAttribute(jfa_bwd_kernel<D, kDyn>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    jfa_bwd_kernel<D><<<grid, kBwdThreads, L::kDynSmem, s>>>(p, m);
+    jfa_bwd_kernel<D, kDyn><<<grid, kBwdThreads, L::kDynSmem, s>>>(p, m);
     return cudaGetLastError();
+}
+
+// The static schedule and the Cluster Launch Control mode are separate
+// instantiations, so the static kernel carries none of the run-time deal.
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s) {
+    return p.clc ? launch_bwd_dk<D, true>(p, m, grid, s) : launch_bwd_dk<D, false>(p, m, grid, s);
 }
 
 // Delta[row] = sum_d dO[row, d] * O[row, d] (fp32) for every (O row, head)
@@ -756,6 +868,10 @@ cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStr
 // 51.3 us).
 template <int D>
 __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
+    // dQ starts at zero (the main kernel adds every tile's dQ into it).
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < p.dq_vec4;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        reinterpret_cast<float4*>(p.dq)[e] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     constexpr int kVec = 2;
     constexpr int kLanes = D / (8 * kVec);
     const int64_t total = p.rows;
@@ -850,4 +966,3 @@ cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cu
 
 }  // namespace jfa
 
-JFA_TRACE_DEFINE_READER(jfa_trace_read_bwd)

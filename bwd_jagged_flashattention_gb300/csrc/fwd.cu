@@ -36,7 +36,6 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
-#include "trace.cuh"
 
 namespace jfa {
 namespace {
@@ -44,6 +43,12 @@ namespace {
 // K/V ring depth in 128-row tiles at D = 128 (twice as many at D = 64):
 // three slots cost 23 us on the ads step, a fifth gained nothing.
 constexpr int kRingSlots = 4;
+#ifndef JFA_FWD_WAITER
+#define JFA_FWD_WAITER 0
+#endif
+// Named barrier of the MMA warp and its waiter warp (0 is __syncthreads, 1-2
+// the softmax warpgroups').
+constexpr int kMmaSyncBar = 3;
 
 // 384 threads = three warpgroups: two softmax warpgroups and one holding the
 // TMA warp, the MMA warp and two idle warps.  Registers are moved from the
@@ -248,7 +253,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
         const WorkItem wc = wn;
         wn = load_item(p.items, i + 1, ie);
         const FwdItem it = decode_fwd<kSparse>(wc, p);
-        JFA_TRACE_EVENT(1, 8, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {  // else: the resident Q tiles serve this item too
             if (!mbar_wait(&bars.q_empty, (q_loads & 1) ^ 1, ab)) goto done;
@@ -261,7 +265,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
             ++q_loads;
             qk.set(it);
         }
-        JFA_TRACE_EVENT(2, 8, i, 0);
         for (int j = 0; j < it.nb; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = ring % L::kSlots;
@@ -270,7 +273,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                     mbar_arrive_expect_tx(&bars.kv_full[slot], 128 * D);
                     tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes, mv, &bars.kv_full[slot], it.h * D,
                                 it.kv_start + 128 * j);
-                    JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
                     ++ring;
                     continue;
                 }
@@ -279,7 +281,6 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                 for (int s = 0; s < L::kSlabs; ++s)
                     tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
                                 &bars.kv_full[slot], it.h * D + 64 * s, it.kv_start + 128 * kv_block<kSparse>(p, it, j));
-                JFA_TRACE_EVENT(3, 8, static_cast<int>(ring), j * 2 + kv);
                 ++ring;
             }
         }
@@ -297,13 +298,26 @@ done:
 //   S0=Q0K0, S1=Q1K0, then for each block j: O0+=P0Vj, S0=Q0K(j+1),
 //   O1+=P1Vj, S1=Q1K(j+1).
 // ---------------------------------------------------------------------------
-template <int D, bool kSparse, bool kMx>
+// kIssuer: the warp that issues the products.  With JFA_FWD_WAITER a second
+// warp runs the same function with kIssuer = false: it takes every barrier
+// wait and hands the outcome to the issuing warp through a named barrier, so
+// the issuing warp performs no memory operation between product groups (one
+// there, a wait even on a completed barrier included, leaves the tensor pipe
+// idle for ~100-175 clocks).  Both warps walk identical loops over identical
+// inputs, so they meet at every barrier, and an abort reaches both there.
+template <int D, bool kSparse, bool kMx, bool kIssuer>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
     // The whole warp runs this role (uniform control flow and operands); only
-    // lane 0 issues the products and commits.
-    const uint32_t lead = (threadIdx.x & 31) == 0 ? 1u : 0u;
+    // lane 0 of the issuing warp issues the products and commits.
+    const uint32_t lead = kIssuer && (threadIdx.x & 31) == 0 ? 1u : 0u;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if constexpr (!JFA_FWD_WAITER) return mbar_wait(bar, parity, ab);
+        bool failed = false;
+        if constexpr (!kIssuer) failed = !mbar_wait_warp(bar, parity, ab);
+        return !bar_red_or(kMmaSyncBar, 64, failed);
+    };
     const uint64_t q_desc = kmajor_desc(smem_u32(smem + L::kQOff));
     const uint64_t k_desc = kmajor_desc(smem_u32(smem + L::kRingOff));
     const uint64_t v_desc = kMx ? smem_desc_swz(smem_u32(smem + L::kRingOff), 16384, 8 * D, D == 128 ? 2u : 4u)
@@ -318,76 +332,74 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         wn = wn2;  // item i + 1, loaded an iteration ago
         wn2 = load_item(p.items, i + 2, ie);
         const FwdItem it = decode_fwd<kSparse>(wc, p);
-        if (lead) JFA_TRACE_EVENT(10, 9, i, it.nb);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {
-            if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
+            if (!wait(&bars.q_full, q_ph)) goto done;
             q_ph ^= 1;
             qk.set(it);
         }
         const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
-        if (lead) JFA_TRACE_EVENT(11, 9, i, 0);
         uint32_t kslot = ring % L::kSlots;
-        if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
+        if (!wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1)) goto done;
         ++ring;
-        if (lead) JFA_TRACE_EVENT(12, 9, 0, 0);
-        tc_fence_after();
+        if constexpr (kIssuer) {
+            tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
-            if (it.nblk[t] > 0) {
-                issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
-                mma_commit_p(lead, &bars.s_full[t]);
-            }
-        mma_commit_p(lead, &bars.kv_empty[kslot]);
-        if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
+            for (int t = 0; t < 2; ++t)
+                if (it.nblk[t] > 0) {
+                    issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                    mma_commit_p(lead, &bars.s_full[t]);
+                }
+            mma_commit_p(lead, &bars.kv_empty[kslot]);
+            if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
+        }
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
-            if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
+            if (!wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1)) goto done;
             ++ring;
-            if (lead) JFA_TRACE_EVENT(13, 9, j, 0);
             const bool has_next = j + 1 < it.nb;
             if (has_next) {
                 kslot = ring % L::kSlots;
-                if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
+                if (!wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1)) goto done;
                 ++ring;
-                if (lead) JFA_TRACE_EVENT(12, 9, j + 1, 0);
             }
-            tc_fence_after();
+            if constexpr (kIssuer) tc_fence_after();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j >= it.nblk[t]) continue;
                 if (j == 0) {
-                    if (!mbar_wait(&bars.o_empty[t], oe_ph[t], ab)) goto done;
+                    if (!wait(&bars.o_empty[t], oe_ph[t])) goto done;
                     oe_ph[t] ^= 1;
-                    if (lead) JFA_TRACE_EVENT(17, 9, t, j);
                 }
-                if (!mbar_wait(&bars.p_full[t], p_ph[t], ab)) goto done;
+                if (!wait(&bars.p_full[t], p_ph[t])) goto done;
                 p_ph[t] ^= 1;
-                if (lead) JFA_TRACE_EVENT(15, 9, t, j);
-                tc_fence_after();
-                if (kMx)
-                    issue_pv_mx<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
-                else
-                    issue_pv<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
-                if (lead) JFA_TRACE_EVENT(16, 9, t, j);
-                if (j == it.nblk[t] - 1) mma_commit_p(lead, &bars.o_full[t]);
-                if (j + 1 < it.nblk[t]) {
-                    issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
-                    if (lead) JFA_TRACE_EVENT(18, 9, t, j + 1);
-                    mma_commit_p(lead, &bars.s_full[t]);
+                if constexpr (kIssuer) {
+                    tc_fence_after();
+                    if (kMx)
+                        issue_pv_mx<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits,
+                                       j > 0);
+                    else
+                        issue_pv<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                    if (j == it.nblk[t] - 1) mma_commit_p(lead, &bars.o_full[t]);
+                    if (j + 1 < it.nblk[t]) {
+                        issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                        mma_commit_p(lead, &bars.s_full[t]);
+                    }
                 }
             }
-            mma_commit_p(lead, &bars.kv_empty[vslot]);
-            if (has_next) {
-                mma_commit_p(lead, &bars.kv_empty[kslot]);
-                if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
+            if constexpr (kIssuer) {
+                mma_commit_p(lead, &bars.kv_empty[vslot]);
+                if (has_next) {
+                    mma_commit_p(lead, &bars.kv_empty[kslot]);
+                    if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
+                }
             }
         }
     }
 done:
     // All issued MMAs must finish before TMEM is released.  A CTA that never
     // took a K/V tile (no items, or only empty ones) issued none.
-    if (ring > 0) {
+    if (kIssuer && ring > 0) {
         mma_commit_p(lead, &bars.mma_done);
         mbar_wait_drain(&bars.mma_done, 0);
     }
@@ -615,7 +627,6 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
         if (t >= it.nq) continue;
         const int nblk = t == 0 ? it.nblk[0] : it.nblk[1];   // scalar copies: no
         const int nfull = t == 0 ? it.nfull[0] : it.nfull[1];  // dynamic array indexing
-        if (row == 0) JFA_TRACE_EVENT(20, t, i, nblk);
         const int qpos = 128 * (it.m0 + t) + row;
         const bool valid = qpos < it.q_rows;
         const int64_t orow = p.broadcast_q ? static_cast<int64_t>(it.b) * p.Lq + qpos
@@ -645,13 +656,11 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             }
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
-            if (row == 0) JFA_TRACE_EVENT(21, t, j, 0);
             tc_fence_after();
             if constexpr (kMx)
                 softmax_block_mx<D, false>(p, it, j, qpos, wq, s_addr, o_addr, vsc, m_use, l);
             else
                 softmax_block<D, kSparse, false>(p, it, j, qpos, s_addr, o_addr, m_use, l);
-            if (row == 0) JFA_TRACE_EVENT(22, t, j, 0);
             handoff_arrive(&bars.p_full[t]);
         }
         for (; j < nblk; ++j) {  // tail: ragged end and/or causal diagonal
@@ -662,13 +671,11 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
             }
             if (!mbar_wait_warp(&bars.s_full[t], s_ph, ab)) goto done;
             s_ph ^= 1;
-            if (row == 0) JFA_TRACE_EVENT(21, t, j, 1);
             tc_fence_after();
             if constexpr (kMx)
                 softmax_block_mx<D, true>(p, it, j, qpos, wq, s_addr, o_addr, vsc, m_use, l);
             else
                 softmax_block<D, kSparse, true>(p, it, j, qpos, s_addr, o_addr, m_use, l);
-            if (row == 0) JFA_TRACE_EVENT(22, t, j, 1);
             handoff_arrive(&bars.p_full[t]);
         }
         // Epilogue: O / l to bf16, LSE = ln(sum exp) of the scaled scores.
@@ -677,7 +684,6 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
         // each warp store covers four whole 128-byte segments.
         if (!mbar_wait_warp(&bars.o_full[t], o_ph, ab)) goto done;
         o_ph ^= 1;
-        if (row == 0) JFA_TRACE_EVENT(23, t, i, 0);
         tc_fence_after();
         {
             uint32_t orr[D / 32][32];
@@ -730,7 +736,6 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
                 group_sync(1 + t);
             }
         }
-        if (row == 0) JFA_TRACE_EVENT(24, t, i, 0);
     }
 done:
     return;
@@ -749,7 +754,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int ib = p.cta_start[blockIdx.x], ie = p.cta_start[blockIdx.x + 1];
     const AbortState ab{&bars.abort_flag, p.status, p.wait_ns};
 
-    JFA_TRACE_INIT();
     if (threadIdx.x == 0) {
         bars.abort_flag = 0;
         mbar_init(&bars.q_full, 1);
@@ -776,8 +780,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (threadIdx.x == 0 || threadIdx.x == 128 || threadIdx.x == 256 || threadIdx.x == 288)
-        JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     if (warp < 8) {
         regs_inc<kSoftmaxRegs>();
         fwd_softmax_role<D, kSparse, kMx>(p, &map_o, smem, bars, tmem, ib, ie, ab);
@@ -787,13 +789,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) fwd_tma_role<D, kSparse, kMx>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            fwd_mma_role<D, kSparse, kMx>(p, smem, bars, tmem, ib, ie, ab);
+            fwd_mma_role<D, kSparse, kMx, true>(p, smem, bars, tmem, ib, ie, ab);
+            __syncwarp();
+        } else if (JFA_FWD_WAITER && warp == kWarpMma + 1) {
+            fwd_mma_role<D, kSparse, kMx, false>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }
 
-    if (threadIdx.x == 0 || threadIdx.x == 128 || threadIdx.x == 256 || threadIdx.x == 288)
-        JFA_TRACE_CLOCK(threadIdx.x < 256 ? threadIdx.x / 128 : warp);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -919,5 +922,3 @@ cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cu
 }
 
 }  // namespace jfa
-
-JFA_TRACE_DEFINE_READER(jfa_trace_read_fwd)

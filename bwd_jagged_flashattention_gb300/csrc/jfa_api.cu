@@ -118,7 +118,7 @@ jfa_status with_stage(size_t need, cudaStream_t stream, F&& fill) {
 // (block-sparse) the selection tables follow; *n_zero receives the number of
 // unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
 int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
-                       const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
+                       int policy, const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
                        int64_t* n_zero, int64_t* n_split_groups, jfa_status* st) {
     const int64_t max_items = w.max_items;
     const bool may_split = JFA_FWD_SPLIT_KV && !is_bwd && !mask && broadcast_q && n_split_groups;
@@ -138,7 +138,7 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
             sp.cap = w.sel_cap;
         }
         split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
-        n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, is_bwd ? g_bwd_policy.load() : g_fwd_policy.load(),
+        n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, policy,
                            items, cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
         if (n < 0) return JFA_ERR_WORKSPACE;
         char* dst = static_cast<char*>(ws_region);
@@ -363,7 +363,7 @@ extern "C" jfa_status jfa_set_wait_limit(unsigned long long ns) {
 
 extern "C" jfa_status jfa_set_schedule_policy(int fwd_policy, int bwd_policy) {
     auto ok = [](int v) { return v == kSchedLptZigzag || v == kSchedNaive || v == kSchedLptGreedy; };
-    if (!ok(fwd_policy) || !ok(bwd_policy)) return JFA_ERR_INVALID_ARG;
+    if (!ok(fwd_policy) || !(ok(bwd_policy) || bwd_policy == kSchedClc)) return JFA_ERR_INVALID_ARG;
     g_fwd_policy.store(fwd_policy);
     g_bwd_policy.store(bwd_policy);
     return JFA_OK;
@@ -400,8 +400,8 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     const int64_t n_items = may_split ? (int64_t{1} << 30) : count_items(pr, 0);
     const int P = ctas_for(n_items);
     int64_t n_groups = 0;
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, w, mask,
-                                     ws + w.fwd_off, s, nullptr, may_split ? &n_groups : nullptr, &st);
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, g_fwd_policy.load(),
+                                     w, mask, ws + w.fwd_off, s, nullptr, may_split ? &n_groups : nullptr, &st);
     if (n < 0) return st;
     if (n == 0) return JFA_OK;
     int64_t n_blocks = 0;
@@ -528,28 +528,35 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
         return JFA_OK;
     }
 
-    // Stream order: schedule copy, dQ zeroing, zeroed dK/dV of unselected
-    // tiles (block-sparse), the Delta pre-pass, then the main kernel.
+    // Stream order: schedule copy, zeroed dK/dV of unselected tiles
+    // (block-sparse), the Delta pre-pass (which also zeroes dQ), then the
+    // main kernel.
+    // Cluster Launch Control: the cost-sorted list (built as a one-CTA
+    // schedule), one CTA per item; otherwise a static deal to one CTA per SM.
+    const int policy = g_bwd_policy.load();
+    const bool clc = policy == kSchedClc;
     const int64_t n_items = count_items(pr, 1);
-    const int P = ctas_for(n_items);
+    const int P = clc ? 1 : ctas_for(n_items);
     int64_t n_zero = 0;
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P, w, mask,
-                                     ws + w.bwd_off, s, &n_zero, nullptr, &st);
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P,
+                                     policy, w, mask, ws + w.bwd_off, s, &n_zero, nullptr, &st);
     if (n < 0) return st;
-    if (q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess) return JFA_ERR_CUDA;
     if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
                           return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
                                                    n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
                                                    D, s);
                       }) != cudaSuccess)
         return JFA_ERR_CUDA;
-    if (n == 0) return JFA_OK;
+    if (n == 0) return q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess ? JFA_ERR_CUDA
+                                                                                                 : JFA_OK;
 
     float* delta = reinterpret_cast<float*>(ws + w.delta_off);
     PreParams pp;
     pp.o = static_cast<const uint16_t*>(o);
     pp.dout = static_cast<const uint16_t*>(dout);
     pp.delta = delta;
+    pp.dq = dq;
+    pp.dq_vec4 = static_cast<int64_t>(elems_q / 4);  // H * D is a multiple of 4
     pp.rows = o_rows * H;
     pp.B = pr.B;
     pp.Lq = pr.Lq;
@@ -577,11 +584,14 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     p.N = static_cast<int>(pr.N);
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
+    p.clc = clc ? 1 : 0;
+    p.n_items = static_cast<int>(n);
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.wait_ns = wait_limit_ns();
+    const int grid = clc ? static_cast<int>(n) : P;
     if (timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess) return JFA_ERR_CUDA;
-    if (timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
+    if (timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, grid, s); }) != cudaSuccess) return JFA_ERR_CUDA;
     return JFA_OK;
 }
 

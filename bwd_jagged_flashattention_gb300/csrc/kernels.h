@@ -40,6 +40,11 @@ struct BwdParams {
     uint32_t* status;
     int Lq, H, N;
     int broadcast_q, causal;
+    // 1: Cluster Launch Control -- one CTA per item of the (cost-sorted) list,
+    // each resident CTA taking over CTAs that have not started; 0: the static
+    // schedule, CTA p owning items [cta_start[p], cta_start[p + 1]).
+    int clc;
+    int n_items;               // items in the list (the grid size with clc)
     float scale, scale_log2;
     uint64_t wait_ns;          // limit of one barrier wait (jfa_set_wait_limit)
     const float* delta;        // same layout as lse (the pre-pass writes it)
@@ -49,6 +54,8 @@ struct PreParams {
     const uint16_t* o;         // bf16, O layout
     const uint16_t* dout;      // bf16, O layout
     float* delta;              // fp32, LSE layout
+    float* dq;                 // fp32 dQ, zeroed by the same kernel (dq_vec4 float4 vectors)
+    int64_t dq_vec4;
     int64_t rows;              // number of (row, head) pairs = O rows * H
     int B, Lq, H, N, D;
     int broadcast_q;
@@ -80,7 +87,7 @@ cudaError_t launch_fwd(int D, const FwdParams& p, const FwdMaps& m, int grid, cu
 // Split-KV merge of n_groups split query tiles into the broadcast O / LSE.
 cudaError_t launch_fwd_merge(int D, const SplitGroup* groups, int64_t n_groups, const float* o_part,
                              const float* lse_part, uint16_t* o, float* lse, int Lq, int H, cudaStream_t s);
-// Delta = rowsum(dO * O) in fp32 (LSE layout), before launch_bwd on the same stream.
+// Delta = rowsum(dO * O) in fp32 (LSE layout), and dQ zeroed, before launch_bwd on the same stream.
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t s);
 cudaError_t launch_bwd(int D, const BwdParams& p, const BwdMaps& m, int grid, cudaStream_t s);
 // MXFP8 quantization of bf16 V [N,H,D] into E4M3 codes (same layout) and

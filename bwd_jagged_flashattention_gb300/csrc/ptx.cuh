@@ -109,6 +109,22 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     }
 }
 
+// Named barrier `id` over `count` threads (whole, converged warps) that also
+// ORs a predicate across them: every participant gets "some participant
+// passed true".  A barrier, not a memory operation.
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(out)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
 // Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
 // all lanes saw the phase complete (so warp-collective tcgen05 ops that
 // follow are executed by all lanes or by none).
@@ -167,6 +183,41 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Cluster Launch Control (dynamic scheduling of a grid larger than what is
+// resident): try_cancel asks the hardware to cancel one CTA (a cluster of
+// one) that has not started yet; the 16-byte response lands in shared memory
+// and completes 16 transaction bytes on `bar`.  If the cancel succeeded, the
+// caller takes over that CTA's work, identified by its first ctaid.  After a
+// failed request no further one may be issued.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void clc_try_cancel(void* resp16, uint64_t* bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            smem_u32(resp16)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Decodes a response: the canceled CTA's x index, or -1 if nothing was canceled.
+__device__ __forceinline__ int clc_response_ctaid_x(const void* resp16) {
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(resp16)) : "memory");
+    uint32_t ok, x = 0;
+    asm volatile(
+        "{\n\t.reg .b128 resp;\n\t.reg .pred p;\n\t"
+        "mov.b128 resp, {%2, %3};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, resp;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, resp;\n\t}\n"
+        : "=r"(ok), "=r"(x)
+        : "l"(static_cast<uint64_t>(r0) | (static_cast<uint64_t>(r1) << 32)),
+          "l"(static_cast<uint64_t>(r2) | (static_cast<uint64_t>(r3) << 32))
+        : "memory");
+    return ok ? static_cast<int>(x) : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -355,6 +406,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -427,6 +487,17 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
         "mov.b64 {%0, %1}, rd;\n\t}\n"
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// d = a * b on two fp32 lanes at once.
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}\n"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // d = a + b on two fp32 lanes at once.

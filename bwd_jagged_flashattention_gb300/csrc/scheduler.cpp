@@ -208,6 +208,9 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
                        SparseSpec* sparse, SplitSpec* split) {
     if (P <= 0 || P > kMaxCtas) return -1;
     if (sparse && causal) return -1;
+    // Cluster Launch Control: the backward's cost-sorted list as one CTA's
+    // slice (the kernel launches one CTA per entry).
+    if (policy == kSchedClc && (!is_bwd || P != 1)) return -1;
     Scratch& sc = scratch();
     // Broadcast-Q backward without a selection or causal mask, per-head CTA
     // groups, the pages' zigzag: every item costs the same (its ceil(Lq/128)
@@ -339,8 +342,11 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     std::vector<int32_t>& fill = sc.fill;
     fill.assign(cta_start, cta_start + P);
     for (int64_t i = 0; i < n; ++i) items[fill[owner[i]]++] = gen[order[i]];
-    // 4. Broadcast Q: group each CTA's items by the Q tiles they read.
-    if (broadcast_q && policy != kSchedNaive) group_by_q(items, cta_start, P, is_bwd);
+    // 4. Broadcast Q: group each CTA's items by the Q tiles they read.  Not
+    // for Cluster Launch Control: a resident CTA's successive items lie about
+    // one SM count apart in the list, so grouping shares no Q tile; it would
+    // only make the CTAs that run together all add into one head's dQ.
+    if (broadcast_q && policy != kSchedNaive && policy != kSchedClc) group_by_q(items, cta_start, P, is_bwd);
     return n;
 }
 

@@ -54,6 +54,8 @@ enum SchedPolicy {
     kSchedLptZigzag = 0,  // cost-descending stable sort, then zigzag deal (the pages' deal)
     kSchedNaive = 1,      // generation order, round-robin deal (ablation)
     kSchedLptGreedy = 2,  // cost-descending stable sort, each item to the least-loaded CTA (the library's)
+    kSchedClc = 3,        // backward only: the cost-sorted list, one CTA per item, dealt at run time by
+                          // Cluster Launch Control (each resident CTA takes over CTAs not yet started)
 };
 
 // Whether broadcast-Q items are dealt per head group (H divides P).

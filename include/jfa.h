@@ -280,6 +280,12 @@ jfa_status jfa_profile_read(double *ms, int *launches, int count);
  * Jagged Flash Attention Beats FA4 on Blackwell With 3x Less Code, section
  * "Optimizations layered on top"); 1 = generation order, round-robin (no
  * balancing); 2 = longest first, each item to the least-loaded CTA.
+ * Backward only: 3 = Cluster Launch Control (the pages list it among the
+ * primitives that keep SMs busy under length skew: same page, sections "What
+ * TLX changes" and "Optimizations layered on top"): the longest-first list,
+ * one CTA per item, and every resident CTA, when it starts an item, asks the
+ * hardware to cancel a CTA that has not started yet and takes over its item
+ * -- a deal made at run time by whichever SM is free.
  * Defaults: 2 for the forward, 0 for the backward.  Results do not depend on
  * the policy (up to dQ's summation order); only the time does.  Returns
  * JFA_ERR_INVALID_ARG for another value.

@@ -181,3 +181,24 @@ def test_mxfp8_argument_errors(jfa):
     assert quant(v=None) == jfa.JFA_ERR_INVALID_ARG
     assert quant(vs=ctypes.c_void_p(P16 + 8)) == jfa.JFA_ERR_UNSUPPORTED
     assert quant(ws_bytes=256) == jfa.JFA_ERR_WORKSPACE                  # needs 256 + 4 (B + 1) bytes
+
+
+def test_schedule_policy_values(jfa):
+    """Deal policies: 0 zigzag, 1 round-robin, 2 greedy for either pass; 3 (Cluster
+    Launch Control) for the backward only; anything else is rejected."""
+    lib = jfa.lib()
+    try:
+        for f in (0, 1, 2):
+            for b in (0, 1, 2, 3):
+                assert lib.jfa_set_schedule_policy(f, b) == jfa.JFA_OK
+        assert lib.jfa_set_schedule_policy(3, 0) == jfa.JFA_ERR_INVALID_ARG
+        assert lib.jfa_set_schedule_policy(0, 4) == jfa.JFA_ERR_INVALID_ARG
+        assert lib.jfa_set_schedule_policy(-1, 0) == jfa.JFA_ERR_INVALID_ARG
+    finally:
+        jfa.set_schedule_policy()
+
+
+def test_wait_limit_setter(jfa):
+    lib = jfa.lib()
+    assert lib.jfa_set_wait_limit(1_000_000) == jfa.JFA_OK
+    assert lib.jfa_set_wait_limit(0) == jfa.JFA_OK  # back to the 4 s default

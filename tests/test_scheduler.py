@@ -232,3 +232,38 @@ def test_greedy_balances_the_ads_forward(jfa):
 
     assert ratio(jfa.SCHED_GREEDY) < 1.05
     assert ratio(jfa.SCHED_ZIGZAG) > 1.2
+
+
+@pytest.mark.parametrize("name,causal", [("ads_bwd", False), ("extreme", False), ("tiny", True)])
+def test_clc_list_is_cost_sorted_generation_order(jfa, name, causal):
+    """Cluster Launch Control backward: one slice holding every item, largest
+    cost first, equal costs in generation order (sequence, head, key tile) --
+    not grouped by head, since the CTAs that run together take consecutive
+    entries -- built in linear time (the extreme workload's tens of thousands
+    of items well inside a second)."""
+    import time
+    w = jfa_inputs.WORKLOADS[name]
+    L = jfa_inputs.draw_lengths(w.lengths, w.B, torch.Generator().manual_seed(6))
+    off = jfa_inputs.offsets_from_lengths(L)
+    t0 = time.perf_counter()
+    items, starts = jfa.host_schedule(off, w.Lq, w.H, w.broadcast_q, causal, True, 1, policy=jfa.SCHED_CLC)
+    took = time.perf_counter() - t0
+    b, start, length, h, tile, two = _decode(items)
+    n = items.shape[0]
+    assert starts.tolist() == [0, n]
+    gen = [(bb, hh, t) for bb in range(w.B) for hh in range(w.H)
+           for t in range((int(off[bb + 1] - off[bb]) + 127) // 128)]
+    assert n == len(gen)
+    cost = {g: _cost(int(off[g[0] + 1] - off[g[0]]), g[2], 0, w.Lq, w.broadcast_q, causal, True) for g in gen}
+    expect = sorted(gen, key=lambda g: -cost[g])  # stable: ties keep generation order
+    got = list(zip(b.tolist(), h.tolist(), tile.tolist()))
+    assert got == expect
+    assert took < 1.0, f"CLC list build took {took:.2f} s for {n} items"
+
+
+def test_clc_policy_is_backward_single_slice_only(jfa):
+    off = jfa_inputs.offsets_from_lengths(torch.tensor([300, 5, 129], dtype=torch.int32))
+    with pytest.raises(jfa.JFAError):
+        jfa.host_schedule(off, 256, 2, True, False, True, 152, policy=jfa.SCHED_CLC)
+    with pytest.raises(jfa.JFAError):
+        jfa.host_schedule(off, 256, 2, True, False, False, 1, policy=jfa.SCHED_CLC)
