@@ -33,8 +33,8 @@
 //   warp  12        loads: K, V per item; Q_i (+ LSE_i), dO_i, Delta_i per tile
 //                   (with Cluster Launch Control also the run-time deal)
 //   warp  13        tcgen05 MMA issue and TMEM allocation
-//   warp  14        the MMA warp's barrier waits (see bwd_mma_role)
-//   warp  15        idle (it completes the fourth warpgroup)
+//   warps 14-15     idle (they complete the fourth warpgroup, whose register
+//                   share the load and MMA warps take)
 #include <cuda_runtime.h>
 #include <climits>
 
@@ -42,9 +42,6 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
-#ifndef JFA_BWD_WAITER
-#define JFA_BWD_WAITER 0
-#endif
 
 
 namespace jfa {
@@ -65,9 +62,6 @@ constexpr int kWarpDq = 4 * kCW;        // first warp of the dQ warpgroup
 constexpr int kWarpLoad = 4 * kCW + 4;
 constexpr int kWarpMma = 4 * kCW + 5;
 constexpr float kLog2e = 1.4426950408889634f;
-// Named barrier of the MMA warp and its waiter warp (0 is __syncthreads, 1 the
-// dQ warpgroup's, 2-3 the compute warpgroups').
-constexpr int kMmaSyncBar = 4;
 
 template <int D>
 struct BwdLayout {
@@ -91,9 +85,9 @@ struct BwdLayout {
 // Items of a CTA in the Cluster Launch Control mode: the load warp publishes
 // each item index through a small ring, the other roles read it from there.
 constexpr int kItemQ = 4;
-// Readers of a ring slot: the MMA warp (and its waiter warp), the compute
-// warps and the dQ warps (lane 0 of each arrives once it has the index).
-constexpr uint32_t kItemReaders = (JFA_BWD_WAITER ? 2 : 1) + 4 * kCW + 4;
+// Readers of a ring slot: the MMA warp, the compute warps and the dQ warps
+// (lane 0 of each arrives once it has the index).
+constexpr uint32_t kItemReaders = 1 + 4 * kCW + 4;
 
 struct BwdBars {
     alignas(16) uint32_t clc_resp[4];  // Cluster Launch Control response (16 bytes)
@@ -383,27 +377,13 @@ done:
 // reuses dQ's columns -- and on the last tile the release of K come one
 // product sooner.
 // ---------------------------------------------------------------------------
-// kIssuer: the warp that issues the products.  With JFA_BWD_WAITER a second
-// warp runs the same function with kIssuer = false: it takes every barrier
-// wait and hands the outcome to the issuing warp through a named barrier, so
-// the issuing warp performs no memory operation between product groups (one
-// there, a wait even on a completed barrier included, leaves the tensor pipe
-// idle for ~100-175 clocks).  Both warps walk identical loops over identical
-// inputs (with Cluster Launch Control both read every index off the ring), so
-// they meet at every barrier, and an abort reaches both there.
-template <int D, bool kDyn, bool kIssuer>
+template <int D, bool kDyn>
 __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = BwdLayout<D>;
     // The whole warp runs this role (uniform control flow and operands); only
-    // lane 0 of the issuing warp issues the products and commits.
-    const uint32_t lead = kIssuer && (threadIdx.x & 31) == 0 ? 1u : 0u;
-    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        if constexpr (!JFA_BWD_WAITER) return mbar_wait(bar, parity, ab);
-        bool failed = false;
-        if constexpr (!kIssuer) failed = !mbar_wait_warp(bar, parity, ab);
-        return !bar_red_or(kMmaSyncBar, 64, failed);
-    };
+    // lane 0 issues the products and commits.
+    const uint32_t lead = (threadIdx.x & 31) == 0 ? 1u : 0u;
     const uint64_t dK_k = kmajor_desc(smem_u32(smem + L::kK)), dK_mn = mnmajor_desc(smem_u32(smem + L::kK));
     const uint64_t dV_k = kmajor_desc(smem_u32(smem + L::kV));
     const uint64_t dQ_k = kmajor_desc(smem_u32(smem + L::kQ)), dQ_mn = mnmajor_desc(smem_u32(smem + L::kQ));
@@ -415,76 +395,60 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
     for (int k = ib; k < ie; ++k) {
         int idx = k;
         if constexpr (kDyn) {
-            idx = ring.read(bars, ab);
-            // Both warps read the same slot; they must also leave together
-            // when either read ends the stream or gives up.
-            const bool stop = JFA_BWD_WAITER ? bar_red_or(kMmaSyncBar, 64, idx < 0) : idx < 0;
-            if (stop) break;
+            if ((idx = ring.read(bars, ab)) < 0) break;
         }
         const BwdItem it = decode_bwd(p.items[idx], p);
-        if (!wait(&bars.k_full, it_cnt & 1)) goto done;
-        if (!wait(&bars.v_full, it_cnt & 1)) goto done;
+        if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
+        if (!mbar_wait(&bars.v_full, it_cnt & 1, ab)) goto done;
         {  // S^T of the item's first query tile
             const int st = q_cnt % 2;
-            if (!wait(&bars.q_full[st], (q_cnt / 2) & 1)) goto done;
-            if constexpr (kIssuer) {
-                tc_fence_after();
-                issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
-                mma_commit_p(lead, &bars.s_full);
-            }
+            if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
+            tc_fence_after();
+            issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
+            mma_commit_p(lead, &bars.s_full);
         }
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
-            if (!wait(&bars.do_full, tile_cnt & 1)) goto done;
-            if (!wait(&bars.dq_empty, (tile_cnt & 1) ^ 1)) goto done;  // previous dQ read out
-            if constexpr (kIssuer) {
-                tc_fence_after();
-                issue_kmajor<D>(lead, tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
-                mma_commit_p(lead, &bars.dp_full);
-                if (i == it.i1 - 1) mma_commit_p(lead, &bars.v_empty);
-            }
+            if (!mbar_wait(&bars.do_full, tile_cnt & 1, ab)) goto done;
+            if (!mbar_wait(&bars.dq_empty, (tile_cnt & 1) ^ 1, ab)) goto done;  // previous dQ read out
+            tc_fence_after();
+            issue_kmajor<D>(lead, tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
+            mma_commit_p(lead, &bars.dp_full);
+            if (i == it.i1 - 1) mma_commit_p(lead, &bars.v_empty);
             if (i == it.i0) {  // the previous item's dV has been read out of TMEM
-                if (!wait(&bars.dv_empty, (it_cnt & 1) ^ 1)) goto done;
+                if (!mbar_wait(&bars.dv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
             }
-            if (!wait(&bars.p_full, tile_cnt & 1)) goto done;
-            if constexpr (kIssuer) {
-                tc_fence_after();
-                issue_dv<D>(lead, tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
-                mma_commit_p(lead, &bars.do_empty);
-            }
+            if (!mbar_wait(&bars.p_full, tile_cnt & 1, ab)) goto done;
+            tc_fence_after();
+            issue_dv<D>(lead, tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
+            mma_commit_p(lead, &bars.do_empty);
             if (i + 1 < it.i1) {  // next tile's S^T (the compute warps keep P in registers)
                 const int st2 = (q_cnt + 1) % 2;
-                if (!wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1)) goto done;
-                if constexpr (kIssuer) {
-                    tc_fence_after();
-                    issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
-                    mma_commit_p(lead, &bars.s_full);
-                }
-            }
-            if (!wait(&bars.ds_full, tile_cnt & 1)) goto done;
-            if (i == it.i0) {  // ... and its dK
-                if (!wait(&bars.dk_empty, (it_cnt & 1) ^ 1)) goto done;
-            }
-            if constexpr (kIssuer) {
+                if (!mbar_wait(&bars.q_full[st2], ((q_cnt + 1) / 2) & 1, ab)) goto done;
                 tc_fence_after();
-                issue_dq<D>(lead, tmem + L::kColDP, dDS_mn, dK_mn);
-                mma_commit_p(lead, &bars.dq_full);
-                if (i == it.i1 - 1) mma_commit_p(lead, &bars.k_empty);
-                issue_dk<D>(lead, tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
-                mma_commit_p(lead, &bars.q_empty[st]);
-                mma_commit_p(lead, &bars.ds_empty);
+                issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st2 * kTileUnits);
+                mma_commit_p(lead, &bars.s_full);
             }
+            if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
+            if (i == it.i0) {  // ... and its dK
+                if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
+            }
+            tc_fence_after();
+            issue_dq<D>(lead, tmem + L::kColDP, dDS_mn, dK_mn);
+            mma_commit_p(lead, &bars.dq_full);
+            if (i == it.i1 - 1) mma_commit_p(lead, &bars.k_empty);
+            issue_dk<D>(lead, tmem + L::kColDK, dDS_k, dQ_mn + st * kTileUnits, i > it.i0);
+            mma_commit_p(lead, &bars.q_empty[st]);
+            mma_commit_p(lead, &bars.ds_empty);
             ++q_cnt;
             ++tile_cnt;
         }
-        if constexpr (kIssuer) mma_commit_p(lead, &bars.dkv_full);
+        mma_commit_p(lead, &bars.dkv_full);
         ++it_cnt;
     }
 done:
-    if constexpr (kIssuer) {
-        mma_commit_p(lead, &bars.mma_done);
-        mbar_wait_drain(&bars.mma_done, 0);
-    }
+    mma_commit_p(lead, &bars.mma_done);
+    mbar_wait_drain(&bars.mma_done, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -823,10 +787,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (warp == kWarpLoad) {
             bwd_load_role<D, kDyn>(p, &maps, smem, bars, ib, ie, ab);
         } else if (warp == kWarpMma) {
-            bwd_mma_role<D, kDyn, true>(p, smem, bars, tmem, ib, ie, ab);
-            __syncwarp();
-        } else if (JFA_BWD_WAITER && warp == kWarpMma + 1) {
-            bwd_mma_role<D, kDyn, false>(p, smem, bars, tmem, ib, ie, ab);
+            bwd_mma_role<D, kDyn>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }

@@ -43,12 +43,6 @@ namespace {
 // K/V ring depth in 128-row tiles at D = 128 (twice as many at D = 64):
 // three slots cost 23 us on the ads step, a fifth gained nothing.
 constexpr int kRingSlots = 4;
-#ifndef JFA_FWD_WAITER
-#define JFA_FWD_WAITER 0
-#endif
-// Named barrier of the MMA warp and its waiter warp (0 is __syncthreads, 1-2
-// the softmax warpgroups').
-constexpr int kMmaSyncBar = 3;
 
 // 384 threads = three warpgroups: two softmax warpgroups and one holding the
 // TMA warp, the MMA warp and two idle warps.  Registers are moved from the
@@ -298,26 +292,13 @@ done:
 //   S0=Q0K0, S1=Q1K0, then for each block j: O0+=P0Vj, S0=Q0K(j+1),
 //   O1+=P1Vj, S1=Q1K(j+1).
 // ---------------------------------------------------------------------------
-// kIssuer: the warp that issues the products.  With JFA_FWD_WAITER a second
-// warp runs the same function with kIssuer = false: it takes every barrier
-// wait and hands the outcome to the issuing warp through a named barrier, so
-// the issuing warp performs no memory operation between product groups (one
-// there, a wait even on a completed barrier included, leaves the tensor pipe
-// idle for ~100-175 clocks).  Both warps walk identical loops over identical
-// inputs, so they meet at every barrier, and an abort reaches both there.
-template <int D, bool kSparse, bool kMx, bool kIssuer>
+template <int D, bool kSparse, bool kMx>
 __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, uint32_t tmem, int ib, int ie,
                              const AbortState& ab) {
     using L = FwdLayout<D>;
     // The whole warp runs this role (uniform control flow and operands); only
-    // lane 0 of the issuing warp issues the products and commits.
-    const uint32_t lead = kIssuer && (threadIdx.x & 31) == 0 ? 1u : 0u;
-    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        if constexpr (!JFA_FWD_WAITER) return mbar_wait(bar, parity, ab);
-        bool failed = false;
-        if constexpr (!kIssuer) failed = !mbar_wait_warp(bar, parity, ab);
-        return !bar_red_or(kMmaSyncBar, 64, failed);
-    };
+    // lane 0 issues the products and commits.
+    const uint32_t lead = (threadIdx.x & 31) == 0 ? 1u : 0u;
     const uint64_t q_desc = kmajor_desc(smem_u32(smem + L::kQOff));
     const uint64_t k_desc = kmajor_desc(smem_u32(smem + L::kRingOff));
     const uint64_t v_desc = kMx ? smem_desc_swz(smem_u32(smem + L::kRingOff), 16384, 8 * D, D == 128 ? 2u : 4u)
@@ -334,72 +315,65 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         const FwdItem it = decode_fwd<kSparse>(wc, p);
         if (it.nb == 0) continue;
         if (!(p.broadcast_q && qk.same(it))) {
-            if (!wait(&bars.q_full, q_ph)) goto done;
+            if (!mbar_wait(&bars.q_full, q_ph, ab)) goto done;
             q_ph ^= 1;
             qk.set(it);
         }
         const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
         uint32_t kslot = ring % L::kSlots;
-        if (!wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1)) goto done;
+        if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
         ++ring;
-        if constexpr (kIssuer) {
-            tc_fence_after();
+        tc_fence_after();
 #pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if (it.nblk[t] > 0) {
-                    issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
-                    mma_commit_p(lead, &bars.s_full[t]);
-                }
-            mma_commit_p(lead, &bars.kv_empty[kslot]);
-            if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
-        }
+        for (int t = 0; t < 2; ++t)
+            if (it.nblk[t] > 0) {
+                issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                mma_commit_p(lead, &bars.s_full[t]);
+            }
+        mma_commit_p(lead, &bars.kv_empty[kslot]);
+        if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
-            if (!wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1)) goto done;
+            if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
             ++ring;
             const bool has_next = j + 1 < it.nb;
             if (has_next) {
                 kslot = ring % L::kSlots;
-                if (!wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1)) goto done;
+                if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
                 ++ring;
             }
-            if constexpr (kIssuer) tc_fence_after();
+            tc_fence_after();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j >= it.nblk[t]) continue;
                 if (j == 0) {
-                    if (!wait(&bars.o_empty[t], oe_ph[t])) goto done;
+                    if (!mbar_wait(&bars.o_empty[t], oe_ph[t], ab)) goto done;
                     oe_ph[t] ^= 1;
                 }
-                if (!wait(&bars.p_full[t], p_ph[t])) goto done;
+                if (!mbar_wait(&bars.p_full[t], p_ph[t], ab)) goto done;
                 p_ph[t] ^= 1;
-                if constexpr (kIssuer) {
-                    tc_fence_after();
-                    if (kMx)
-                        issue_pv_mx<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits,
-                                       j > 0);
-                    else
-                        issue_pv<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
-                    if (j == it.nblk[t] - 1) mma_commit_p(lead, &bars.o_full[t]);
-                    if (j + 1 < it.nblk[t]) {
-                        issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
-                        mma_commit_p(lead, &bars.s_full[t]);
-                    }
+                tc_fence_after();
+                if (kMx)
+                    issue_pv_mx<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                else
+                    issue_pv<D>(lead, tmem + L::kOCol + t * D, tmem + t * 128, v_desc + vslot * kTileUnits, j > 0);
+                if (j == it.nblk[t] - 1) mma_commit_p(lead, &bars.o_full[t]);
+                if (j + 1 < it.nblk[t]) {
+                    issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
+                    mma_commit_p(lead, &bars.s_full[t]);
                 }
             }
-            if constexpr (kIssuer) {
-                mma_commit_p(lead, &bars.kv_empty[vslot]);
-                if (has_next) {
-                    mma_commit_p(lead, &bars.kv_empty[kslot]);
-                    if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
-                }
+            mma_commit_p(lead, &bars.kv_empty[vslot]);
+            if (has_next) {
+                mma_commit_p(lead, &bars.kv_empty[kslot]);
+                if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
             }
         }
     }
 done:
     // All issued MMAs must finish before TMEM is released.  A CTA that never
     // took a K/V tile (no items, or only empty ones) issued none.
-    if (kIssuer && ring > 0) {
+    if (ring > 0) {
         mma_commit_p(lead, &bars.mma_done);
         mbar_wait_drain(&bars.mma_done, 0);
     }
@@ -789,10 +763,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             if (lane == 0) fwd_tma_role<D, kSparse, kMx>(p, &map_q, &map_k, &map_v, smem, bars, ib, ie, ab);
             __syncwarp();
         } else if (warp == kWarpMma) {
-            fwd_mma_role<D, kSparse, kMx, true>(p, smem, bars, tmem, ib, ie, ab);
-            __syncwarp();
-        } else if (JFA_FWD_WAITER && warp == kWarpMma + 1) {
-            fwd_mma_role<D, kSparse, kMx, false>(p, smem, bars, tmem, ib, ie, ab);
+            fwd_mma_role<D, kSparse, kMx>(p, smem, bars, tmem, ib, ie, ab);
             __syncwarp();
         }
     }

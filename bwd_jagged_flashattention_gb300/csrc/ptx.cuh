@@ -109,22 +109,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
     }
 }
 
-// Named barrier `id` over `count` threads (whole, converged warps) that also
-// ORs a predicate across them: every participant gets "some participant
-// passed true".  A barrier, not a memory operation.
-__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}\n"
-        : "=r"(out)
-        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
-        : "memory");
-    return out != 0;
-}
-
 // Warp-uniform bounded wait: every lane waits, and the warp proceeds only if
 // all lanes saw the phase complete (so warp-collective tcgen05 ops that
 // follow are executed by all lanes or by none).
