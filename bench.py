@@ -669,7 +669,8 @@ def main():
         for pol_name, fpol, bpol in (("lpt_greedy", jfa.SCHED_GREEDY, jfa.SCHED_GREEDY),
                                      ("lpt_zigzag", jfa.SCHED_ZIGZAG, jfa.SCHED_ZIGZAG),
                                      ("naive_round_robin", jfa.SCHED_NAIVE, jfa.SCHED_NAIVE),
-                                     ("cluster_launch_control", jfa.SCHED_GREEDY, jfa.SCHED_CLC)):
+                                     ("cluster_launch_control", jfa.SCHED_GREEDY, jfa.SCHED_CLC),
+                                     ("per_head_queue", jfa.SCHED_GREEDY, jfa.SCHED_QUEUE)):
             jfa.set_schedule_policy(fpol, bpol)
             for _ in range(3):
                 step()
@@ -678,7 +679,9 @@ def main():
         jfa.set_schedule_policy()  # the library's defaults: greedy forward, zigzag backward
         ablation["note"] = (f"{n_ab} steps per policy, same inputs; the library deals the forward lpt_greedy and "
                             f"the backward lpt_zigzag; cluster_launch_control deals the backward at run time "
-                            f"(one CTA per item, resident CTAs taking over those not started), forward lpt_greedy")
+                            f"(one CTA per item, resident CTAs taking over those not started), per_head_queue "
+                            f"too (one CTA per SM, each taking its head group's next longest item), forward "
+                            f"lpt_greedy")
 
     # Per-kernel live timing -> rooflines.
     peaks = load_peaks()

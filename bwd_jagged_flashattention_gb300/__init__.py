@@ -344,7 +344,8 @@ def num_ctas() -> int:
     return int(lib().jfa_num_ctas())
 
 
-SCHED_ZIGZAG, SCHED_NAIVE, SCHED_GREEDY, SCHED_CLC = 0, 1, 2, 3  # deal policies (SCHED_CLC: backward only)
+# deal policies (SCHED_CLC, SCHED_QUEUE: backward only)
+SCHED_ZIGZAG, SCHED_NAIVE, SCHED_GREEDY, SCHED_CLC, SCHED_QUEUE = 0, 1, 2, 3, 4
 
 
 def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool, is_bwd: bool, P: int,
@@ -356,7 +357,8 @@ def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool
     N = int(off[-1]) if B > 0 else 0
     cap = H * (N // 128 + B) + H * B * ((max(Lq, 0) + 255) // 256) + 1
     items = torch.zeros((cap, 4), dtype=torch.int32)
-    starts = torch.zeros(P + 1, dtype=torch.int32)
+    # P + 1 CTA bounds; a queue schedule writes 2G + 1 <= 2H + 1 entries
+    starts = torch.zeros(max(P + 1, 2 * H + 1), dtype=torch.int32)
     if noalloc:
         n = lib().jfa_host_build_schedule_noalloc(ctypes.c_void_p(off.data_ptr()), B, Lq, H, int(broadcast_q),
                                                   int(causal), int(is_bwd), P, ctypes.c_void_p(items.data_ptr()),
@@ -367,7 +369,7 @@ def host_schedule(offsets_host, Lq: int, H: int, broadcast_q: bool, causal: bool
                                           ctypes.c_void_p(starts.data_ptr()), cap)
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule")
-    return items[:n].clone(), starts
+    return items[:n].clone(), (starts if policy == SCHED_QUEUE else starts[:P + 1].clone())
 
 
 def set_wait_limit(ns: int = 0) -> None:

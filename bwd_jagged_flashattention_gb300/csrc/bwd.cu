@@ -42,8 +42,6 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
-
-
 namespace jfa {
 namespace {
 
@@ -247,7 +245,21 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
     // Cluster Launch Control: this CTA's own item first, then every CTA it
     // cancels before that one starts; each index goes to the other roles
     // through the ring (-1 last).
+    // Queues instead: the next item of this CTA's queue, taken (atomically)
+    // one item ahead; lane 0 holds the position until it is needed.
+    const bool from_queue = kDyn && p.queue != nullptr;
+    const int qg = from_queue ? static_cast<int>(blockIdx.x) % p.n_queues : 0;
+    auto queue_item = [&](int taken) {
+        const int v = __shfl_sync(0xffffffffu, taken, 0);
+        const int q0 = p.cta_start[qg], q1 = p.cta_start[qg + 1];
+        return v < q1 - q0 ? q0 + v : -1;
+    };
+    int taken = 0;
     int cur = static_cast<int>(blockIdx.x);
+    if (from_queue) {
+        if (lane == 0) taken = atomicAdd(p.queue + qg, 1);
+        cur = queue_item(taken);
+    }
     uint32_t published = 0, clc_phase = 0;
     bool clc_inflight = false;
     for (int k = ib; k < ie; ++k) {
@@ -262,11 +274,15 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             }
             ++published;
             if (idx < 0) break;
-            if (lane == 0) {  // ask for the next item while this one's tiles load
-                mbar_arrive_expect_tx(&bars.clc_bar, 16);
-                clc_try_cancel(bars.clc_resp, &bars.clc_bar);
+            if (from_queue) {  // take the next item while this one's tiles load
+                if (lane == 0) taken = atomicAdd(p.queue + qg, 1);
+            } else {
+                if (lane == 0) {  // ask for the next item while this one's tiles load
+                    mbar_arrive_expect_tx(&bars.clc_bar, 16);
+                    clc_try_cancel(bars.clc_resp, &bars.clc_bar);
+                }
+                clc_inflight = true;
             }
-            clc_inflight = true;
         }
         const BwdItem it = decode_bwd(p.items[idx], p);
         const int kv_row = it.kv_start + 128 * it.n;
@@ -348,6 +364,10 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             }
         }
         if constexpr (kDyn) {  // the next item: a canceled CTA's index, or -1 when none is left
+            if (from_queue) {
+                cur = queue_item(taken);
+                continue;
+            }
             if (!mbar_wait_warp(&bars.clc_bar, clc_phase & 1, ab)) goto done;
             ++clc_phase;
             clc_inflight = false;
@@ -848,8 +868,10 @@ __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
             uint4 a[kVec], b[kVec];
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
-                a[u] = reinterpret_cast<const uint4*>(p.o + pair * D)[sub * kVec + u];
-                b[u] = reinterpret_cast<const uint4*>(p.dout + pair * D)[sub * kVec + u];
+                // Streaming (evict-first) loads: O and dO are read once here;
+                // cached loads measured 53 vs 45 us on the ads step.
+                a[u] = __ldcs(reinterpret_cast<const uint4*>(p.o + pair * D) + sub * kVec + u);
+                b[u] = __ldcs(reinterpret_cast<const uint4*>(p.dout + pair * D) + sub * kVec + u);
             }
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {

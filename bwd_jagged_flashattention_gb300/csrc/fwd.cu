@@ -241,6 +241,11 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
     prefetch_tensormap(mk);
     prefetch_tensormap(mv);
     uint32_t ring = 0, q_loads = 0;
+    // K and V blocks are read once per forward: evict them from L2 first, so
+    // more of the O rows the kernel writes (which the backward's Delta pass
+    // reads next) stay there (ads step: forward 137 vs 141 us, Delta pass 43
+    // vs 45 us).
+    const uint64_t kv_policy = l2_policy_evict_first();
     QKey qk;
     WorkItem wn = load_item(p.items, ib, ie);
     for (int i = ib; i < ie; ++i) {
@@ -265,16 +270,17 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
                 if (!mbar_wait(&bars.kv_empty[slot], ((ring / L::kSlots) & 1) ^ 1, ab)) goto done;
                 if (kMx && kv) {  // E4M3 V: one box of 128 rows x D bytes
                     mbar_arrive_expect_tx(&bars.kv_full[slot], 128 * D);
-                    tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes, mv, &bars.kv_full[slot], it.h * D,
-                                it.kv_start + 128 * j);
+                    tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes, mv, &bars.kv_full[slot], it.h * D,
+                                     it.kv_start + 128 * j, kv_policy);
                     ++ring;
                     continue;
                 }
                 mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
 #pragma unroll
                 for (int s = 0; s < L::kSlabs; ++s)
-                    tma_load_2d(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
-                                &bars.kv_full[slot], it.h * D + 64 * s, it.kv_start + 128 * kv_block<kSparse>(p, it, j));
+                    tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
+                                     &bars.kv_full[slot], it.h * D + 64 * s,
+                                     it.kv_start + 128 * kv_block<kSparse>(p, it, j), kv_policy);
                 ++ring;
             }
         }

@@ -363,7 +363,8 @@ extern "C" jfa_status jfa_set_wait_limit(unsigned long long ns) {
 
 extern "C" jfa_status jfa_set_schedule_policy(int fwd_policy, int bwd_policy) {
     auto ok = [](int v) { return v == kSchedLptZigzag || v == kSchedNaive || v == kSchedLptGreedy; };
-    if (!ok(fwd_policy) || !(ok(bwd_policy) || bwd_policy == kSchedClc)) return JFA_ERR_INVALID_ARG;
+    if (!ok(fwd_policy) || !(ok(bwd_policy) || bwd_policy == kSchedClc || bwd_policy == kSchedQueue))
+        return JFA_ERR_INVALID_ARG;
     g_fwd_policy.store(fwd_policy);
     g_bwd_policy.store(bwd_policy);
     return JFA_OK;
@@ -532,9 +533,12 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     // (block-sparse), the Delta pre-pass (which also zeroes dQ), then the
     // main kernel.
     // Cluster Launch Control: the cost-sorted list (built as a one-CTA
-    // schedule), one CTA per item; otherwise a static deal to one CTA per SM.
+    // schedule), one CTA per item; queues: one CTA per SM taking items from
+    // its head group's queue at run time; otherwise a static deal to one CTA
+    // per SM.
     const int policy = g_bwd_policy.load();
     const bool clc = policy == kSchedClc;
+    const bool queue = policy == kSchedQueue;
     const int64_t n_items = count_items(pr, 1);
     const int P = clc ? 1 : ctas_for(n_items);
     int64_t n_zero = 0;
@@ -584,8 +588,10 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     p.N = static_cast<int>(pr.N);
     p.broadcast_q = pr.broadcast_q;
     p.causal = pr.causal;
-    p.clc = clc ? 1 : 0;
+    p.clc = (clc || queue) ? 1 : 0;
     p.n_items = static_cast<int>(n);
+    p.n_queues = queue ? queue_groups(pr.broadcast_q, H, P) : 0;
+    p.queue = queue ? reinterpret_cast<int32_t*>(ws + w.bwd_off) + p.n_queues + 1 : nullptr;
     p.scale = pr.scale;
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.wait_ns = wait_limit_ns();

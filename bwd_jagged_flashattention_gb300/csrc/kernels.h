@@ -40,11 +40,16 @@ struct BwdParams {
     uint32_t* status;
     int Lq, H, N;
     int broadcast_q, causal;
-    // 1: Cluster Launch Control -- one CTA per item of the (cost-sorted) list,
-    // each resident CTA taking over CTAs that have not started; 0: the static
-    // schedule, CTA p owning items [cta_start[p], cta_start[p + 1]).
+    // 1: items dealt at run time -- by Cluster Launch Control (queue null: one
+    // CTA per item of the cost-sorted list, each resident CTA taking over CTAs
+    // that have not started) or from queues (queue set: CTA c takes the next
+    // item of queue c % n_queues, items [cta_start[g], cta_start[g + 1]), by
+    // atomically incrementing queue[g]); 0: the static schedule, CTA p owning
+    // items [cta_start[p], cta_start[p + 1]).
     int clc;
-    int n_items;               // items in the list (the grid size with clc)
+    int n_items;               // items in the list (the grid size with Cluster Launch Control)
+    int n_queues;
+    int32_t* queue;            // take counters (zero at launch), or null
     float scale, scale_log2;
     uint64_t wait_ns;          // limit of one barrier wait (jfa_set_wait_limit)
     const float* delta;        // same layout as lse (the pre-pass writes it)

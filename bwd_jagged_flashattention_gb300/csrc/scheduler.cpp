@@ -211,6 +211,7 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     // Cluster Launch Control: the backward's cost-sorted list as one CTA's
     // slice (the kernel launches one CTA per entry).
     if (policy == kSchedClc && (!is_bwd || P != 1)) return -1;
+    if (policy == kSchedQueue && !is_bwd) return -1;
     Scratch& sc = scratch();
     // Broadcast-Q backward without a selection or causal mask, per-head CTA
     // groups, the pages' zigzag: every item costs the same (its ceil(Lq/128)
@@ -327,6 +328,22 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         for (int64_t i = 0; i < n; ++i) order[start[cmax - cost[i]]++] = i;
     } else {
         for (int64_t i = 0; i < n; ++i) order[i] = i;
+    }
+
+    // 3q. Queues: each item to its head group's queue, in the sorted order
+    // (longest first); the CTAs of the group take them at run time.
+    if (policy == kSchedQueue) {
+        const int G = queue_groups(broadcast_q, H, P);
+        std::fill(cta_start, cta_start + 2 * G + 1, 0);
+        for (int64_t i = 0; i < n; ++i) ++cta_start[(G > 1 ? static_cast<int>(gen[order[i]].packed & 0xFFu) : 0) + 1];
+        for (int g = 0; g < G; ++g) cta_start[g + 1] += cta_start[g];
+        std::vector<int32_t>& fill = sc.fill;
+        fill.assign(cta_start, cta_start + G);
+        for (int64_t i = 0; i < n; ++i) {
+            const WorkItem& w = gen[order[i]];
+            items[fill[G > 1 ? static_cast<int>(w.packed & 0xFFu) : 0]++] = w;
+        }
+        return n;
     }
 
     // 3. Deal (see deal()).

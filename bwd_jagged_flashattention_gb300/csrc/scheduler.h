@@ -56,10 +56,18 @@ enum SchedPolicy {
     kSchedLptGreedy = 2,  // cost-descending stable sort, each item to the least-loaded CTA (the library's)
     kSchedClc = 3,        // backward only: the cost-sorted list, one CTA per item, dealt at run time by
                           // Cluster Launch Control (each resident CTA takes over CTAs not yet started)
+    kSchedQueue = 4,      // backward only: one cost-sorted queue per head group (broadcast Q, H | P; else one
+                          // queue), taken from at run time by the persistent CTAs of that group
 };
+
+// kSchedQueue layout of cta_start: entries 0..G are the queues' bounds (queue
+// g = items [cta_start[g], cta_start[g + 1])), entries G+1 .. 2G are the
+// queues' take counters, zero in the uploaded schedule.
 
 // Whether broadcast-Q items are dealt per head group (H divides P).
 bool head_partition(int broadcast_q, int H, int P);
+// Number of queues of a kSchedQueue schedule.
+inline int queue_groups(int broadcast_q, int H, int P) { return head_partition(broadcast_q, H, P) ? H : 1; }
 
 // Upper bound on the number of items either pass produces.
 int64_t max_work_items(int B, int64_t total_len, int Lq, int H, int broadcast_q);

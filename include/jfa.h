@@ -285,7 +285,11 @@ jfa_status jfa_profile_read(double *ms, int *launches, int count);
  * TLX changes" and "Optimizations layered on top"): the longest-first list,
  * one CTA per item, and every resident CTA, when it starts an item, asks the
  * hardware to cancel a CTA that has not started yet and takes over its item
- * -- a deal made at run time by whichever SM is free.
+ * -- a deal made at run time by whichever SM is free; 4 = queues: one CTA
+ * per SM as in the static deals, the items of each head group (broadcast Q
+ * with H dividing the CTA count; otherwise all items) in one longest-first
+ * queue, and each CTA, as it starts an item, atomically takes the next item
+ * of its group's queue -- a run-time deal that keeps each CTA on one head.
  * Defaults: 2 for the forward, 0 for the backward.  Results do not depend on
  * the policy (up to dQ's summation order); only the time does.  Returns
  * JFA_ERR_INVALID_ARG for another value.

@@ -185,14 +185,16 @@ def test_mxfp8_argument_errors(jfa):
 
 def test_schedule_policy_values(jfa):
     """Deal policies: 0 zigzag, 1 round-robin, 2 greedy for either pass; 3 (Cluster
-    Launch Control) for the backward only; anything else is rejected."""
+    Launch Control) and 4 (per-head-group queues) for the backward only;
+    anything else is rejected."""
     lib = jfa.lib()
     try:
         for f in (0, 1, 2):
-            for b in (0, 1, 2, 3):
+            for b in (0, 1, 2, 3, 4):
                 assert lib.jfa_set_schedule_policy(f, b) == jfa.JFA_OK
         assert lib.jfa_set_schedule_policy(3, 0) == jfa.JFA_ERR_INVALID_ARG
-        assert lib.jfa_set_schedule_policy(0, 4) == jfa.JFA_ERR_INVALID_ARG
+        assert lib.jfa_set_schedule_policy(4, 0) == jfa.JFA_ERR_INVALID_ARG
+        assert lib.jfa_set_schedule_policy(0, 5) == jfa.JFA_ERR_INVALID_ARG
         assert lib.jfa_set_schedule_policy(-1, 0) == jfa.JFA_ERR_INVALID_ARG
     finally:
         jfa.set_schedule_policy()

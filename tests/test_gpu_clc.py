@@ -1,4 +1,5 @@
-"""The backward with its items dealt at run time by Cluster Launch Control.
+"""The backward with its items dealt at run time: by Cluster Launch Control,
+or from per-head-group queues.
 
 With jfa_set_schedule_policy(bwd=3) the backward launches one CTA per item of
 the longest-first list; every resident CTA, as it starts an item, asks the
@@ -18,10 +19,12 @@ from tests.gpu_util import check_all, gpu_fwd_bwd, oracle_fwd_bwd
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture
-def clc_backward():
+@pytest.fixture(params=["clc", "queue"])
+def clc_backward(request):
+    """The backward dealt at run time: by Cluster Launch Control, or by the
+    persistent CTAs taking items from their head group's queue."""
     import bwd_jagged_flashattention_gb300 as jfa
-    jfa.set_schedule_policy(bwd_policy=jfa.SCHED_CLC)
+    jfa.set_schedule_policy(bwd_policy=jfa.SCHED_CLC if request.param == "clc" else jfa.SCHED_QUEUE)
     yield jfa
     jfa.set_schedule_policy()
 

@@ -267,3 +267,35 @@ def test_clc_policy_is_backward_single_slice_only(jfa):
         jfa.host_schedule(off, 256, 2, True, False, True, 152, policy=jfa.SCHED_CLC)
     with pytest.raises(jfa.JFAError):
         jfa.host_schedule(off, 256, 2, True, False, False, 1, policy=jfa.SCHED_CLC)
+
+
+@pytest.mark.parametrize("name,P", [("ads_bwd", 152), ("extreme", 152), ("tiny", 8), ("ads_bwd", 150)])
+def test_queue_schedule_layout(jfa, name, P):
+    """Backward queues: with broadcast Q and H | P one queue per head (else
+    one), each longest-first and stable, every item once, bounds in
+    cta_start[0..G], the G take counters after them zero."""
+    w = jfa_inputs.WORKLOADS[name]
+    L = jfa_inputs.draw_lengths(w.lengths, w.B, torch.Generator().manual_seed(7))
+    off = jfa_inputs.offsets_from_lengths(L)
+    items, starts = jfa.host_schedule(off, w.Lq, w.H, w.broadcast_q, w.causal, True, P, policy=jfa.SCHED_QUEUE)
+    G = w.H if (w.broadcast_q and 1 < w.H <= 255 and P % w.H == 0) else 1
+    st = starts.tolist()
+    assert st[0] == 0 and st[G] == items.shape[0] and st[G + 1:2 * G + 1] == [0] * G
+    b, start, length, h, tile, two = _decode(items)
+    gen = [(bb, hh, t) for bb in range(w.B) for hh in range(w.H)
+           for t in range((int(off[bb + 1] - off[bb]) + 127) // 128)]
+    assert sorted(zip(b.tolist(), h.tolist(), tile.tolist())) == sorted(gen)
+    for g in range(G):
+        lo, hi = st[g], st[g + 1]
+        part = list(zip(b[lo:hi].tolist(), h[lo:hi].tolist(), tile[lo:hi].tolist()))
+        if G > 1:
+            assert all(hh == g for _, hh, _ in part)
+        mine = [x for x in gen if G == 1 or x[1] == g]
+        cost = {x: _cost(int(off[x[0] + 1] - off[x[0]]), x[2], 0, w.Lq, w.broadcast_q, w.causal, True) for x in mine}
+        assert part == sorted(mine, key=lambda x: -cost[x])
+
+
+def test_queue_policy_is_backward_only(jfa):
+    off = jfa_inputs.offsets_from_lengths(torch.tensor([300, 5, 129], dtype=torch.int32))
+    with pytest.raises(jfa.JFAError):
+        jfa.host_schedule(off, 256, 2, True, False, False, 8, policy=jfa.SCHED_QUEUE)
