@@ -140,6 +140,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def make_inputs(args, backward=None):
+    """The workload's synthetic inputs; with --lengths, its shapes with those KV lengths
+    (e.g. "131072,512x31": one 131072-key sequence and 31 of 512 keys)."""
+    if not args.lengths:
+        return jfa_inputs.make(args.workload) if backward is None else jfa_inputs.make(args.workload, backward=backward)
+    w = jfa_inputs.WORKLOADS[args.workload]
+    lens = []
+    for part in args.lengths.split(","):
+        n, _, rep_ = part.partition("x")
+        lens += [int(n)] * (int(rep_) if rep_ else 1)
+    x = jfa_inputs.custom(len(lens), w.Lq, w.H, w.D, lens, w.broadcast_q, w.causal, seed=1,
+                          backward=w.backward if backward is None else backward)
+    x["workload"] = f"{args.workload} with lengths {args.lengths}"
+    return x
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("fwd.cu", "bwd.cu", "ptx.cuh", "kernels.h"):
@@ -362,7 +378,7 @@ def run_mxfp8(args, world, rank):
     jfa.lib()
     dev = torch.device("cuda", 0 if world == 1 else int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    x = jfa_inputs.make(args.workload, backward=False)
+    x = make_inputs(args, backward=False)
     if args.batch:
         x = first_sequences(x, args.batch)
     acc = accounting(x)
@@ -469,7 +485,8 @@ def run_mxfp8(args, world, rank):
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (P V, E8M0 scales) + bf16 (Q K^T)", "data": "synthetic",
-        "config": {"workload": workload_desc(args.workload) + "; forward only, V in MXFP8",
+        "config": {"workload": workload_desc(args.workload) + "; forward only, V in MXFP8"
+                   + (f"; sequence lengths replaced by {args.lengths}" if args.lengths else ""),
                    "B": B, "Lq": Lq, "H": H, "D": D, "N": N, "pairs": acc["pairs"],
                    "l2": "no flush: Q, K, V inputs exceed the 129 MB L2" if 3 * N * H * D > 129e6 else "no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -522,16 +539,7 @@ def main():
     jfa.lib()  # raises if the CUDA library is missing: no fallback
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = jfa_inputs.make(args.workload)
-    if args.lengths:
-        w = jfa_inputs.WORKLOADS[args.workload]
-        lens = []
-        for part in args.lengths.split(","):
-            n, _, rep_ = part.partition("x")
-            lens += [int(n)] * (int(rep_) if rep_ else 1)
-        x = jfa_inputs.custom(len(lens), w.Lq, w.H, w.D, lens, w.broadcast_q, w.causal, seed=1,
-                              backward=w.backward)
-        x["workload"] = f"{args.workload} with lengths {args.lengths}"
+    x = make_inputs(args)
     backward = "do" in x
     if args.batch:
         x = first_sequences(x, args.batch)

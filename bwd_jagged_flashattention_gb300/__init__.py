@@ -100,7 +100,7 @@ def lib() -> ctypes.CDLL:
             L.jfa_host_build_schedule.argtypes = [vp, ci, ci, ci, ci, ci, ci, ci, ci, vp, vp, ctypes.c_longlong]
             ll = ctypes.c_longlong
             if hasattr(L, "jfa_host_build_schedule_split"):
-                L.jfa_host_build_schedule_split.argtypes = [vp, ci, ci, ci, ci, vp, vp, ll, vp, ctypes.POINTER(ll)]
+                L.jfa_host_build_schedule_split.argtypes = [vp, ci, ci, ci, ci, vp, vp, ll, vp, ctypes.POINTER(ll), vp]
                 L.jfa_host_build_schedule_split.restype = ll
             if hasattr(L, "jfa_host_build_schedule_sparse"):
                 L.jfa_host_build_schedule_sparse.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, ll, vp, vp, vp,
@@ -384,9 +384,10 @@ def set_schedule_policy(fwd_policy: int = None, bwd_policy: int = None) -> None:
            "jfa_set_schedule_policy")
 
 
-def host_schedule_split(offsets_host, Lq: int, H: int, P: int):
+def host_schedule_split(offsets_host, Lq: int, H: int, P: int, with_slot_blocks: bool = False):
     """The broadcast-Q forward schedule with split-KV (no GPU): (items [n,4], cta_start [P+1],
-    groups [n_groups,4] = (b, first slot, chunks, h | tile << 8), slot count)."""
+    groups [n_groups,4] = (b, first slot, chunks, h | tile << 8), slot count); with_slot_blocks
+    adds each slot's first key block over all sequences (int32 [slots])."""
     off = offsets_host.to(torch.int32).contiguous()
     B = off.numel() - 1
     N = int(off[-1]) if B > 0 else 0
@@ -396,10 +397,13 @@ def host_schedule_split(offsets_host, Lq: int, H: int, P: int):
     groups = torch.zeros((SPLIT_MAX_SLOTS, 4), dtype=torch.int32)
     counts = (ctypes.c_longlong * 2)()
     vp = lambda t: ctypes.c_void_p(t.data_ptr())
-    n = lib().jfa_host_build_schedule_split(vp(off), B, Lq, H, P, vp(items), vp(starts), cap, vp(groups), counts)
+    slot_blocks = torch.zeros(SPLIT_MAX_SLOTS, dtype=torch.int32)
+    n = lib().jfa_host_build_schedule_split(vp(off), B, Lq, H, P, vp(items), vp(starts), cap, vp(groups), counts,
+                                            vp(slot_blocks) if with_slot_blocks else None)
     if n < 0:
         raise JFAError(JFA_ERR_WORKSPACE, "jfa_host_build_schedule_split")
-    return items[:n].clone(), starts, groups[:counts[0]].clone(), int(counts[1])
+    out = (items[:n].clone(), starts, groups[:counts[0]].clone(), int(counts[1]))
+    return out + (slot_blocks[:counts[1]].clone(),) if with_slot_blocks else out
 
 
 SPLIT_MAX_SLOTS = 512  # split-KV partial slots per call (the library's workspace bound)

@@ -626,7 +626,9 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
         int j = 0;
         // MXFP8: this lane's V-scale words, fetched one block ahead
         uint32_t vsc[D / 32], vsn[D / 32];
-        const int64_t blk0 = kMx ? static_cast<int64_t>(__ldg(p.block_start + it.b)) : 0;
+        const int64_t blk0 = !kMx ? 0
+                             : it.slot >= 0 ? static_cast<int64_t>(__ldg(p.split_block0 + it.slot))
+                                            : static_cast<int64_t>(__ldg(p.block_start + it.b));
         if (kMx) load_vscale<D>(p, blk0, it.h, vsn);
         for (; j < nfull; ++j) {  // bulk: every key visible, no mask
             if (kMx) {

@@ -40,6 +40,7 @@ struct WsLayout {
     size_t fwd_off, bwd_off, fwd_region, bwd_region, delta_off, delta_bytes, total;
     size_t sel_off, blocks_off, zero_off;  // offsets inside a region
     size_t split_off;                      // forward region: split-KV groups (broadcast Q)
+    size_t split_blk_off;                  // forward region: each split slot's first key block (MXFP8 V scales)
     size_t opart_off, lpart_off;           // split-KV partial O / LSE (broadcast Q; 0 bytes otherwise)
     int64_t max_items, sel_cap;            // sel_cap >= NB * H (NB = key blocks over all sequences)
 };
@@ -52,7 +53,8 @@ bool ws_layout(int B, int64_t N, int Lq, int H, int D, int broadcast_q, WsLayout
     w->blocks_off = w->sel_off + align_up(static_cast<size_t>(B) * H * sizeof(SparseSel), 256);
     w->zero_off = w->sel_off;
     w->split_off = w->blocks_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(int32_t), 256);
-    w->fwd_region = w->split_off + (broadcast_q ? align_up(kMaxSplitSlots * sizeof(SplitGroup), 256) : 0);
+    w->split_blk_off = w->split_off + (broadcast_q ? align_up(kMaxSplitSlots * sizeof(SplitGroup), 256) : 0);
+    w->fwd_region = w->split_blk_off + (broadcast_q ? align_up(kMaxSplitSlots * sizeof(int32_t), 256) : 0);
     w->bwd_region = w->zero_off + align_up(static_cast<size_t>(w->sel_cap) * sizeof(ZeroTile), 256);
     w->fwd_off = kStatusBytes;
     w->bwd_off = w->fwd_off + w->fwd_region;
@@ -138,6 +140,7 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
             sp.cap = w.sel_cap;
         }
         split.groups = reinterpret_cast<SplitGroup*>(buf + w.split_off);
+        split.slot_block0 = reinterpret_cast<int32_t*>(buf + w.split_blk_off);
         n = build_schedule(offsets, B, Lq, H, broadcast_q, causal, is_bwd, P, policy,
                            items, cta_start, max_items, mask ? &sp : nullptr, may_split ? &split : nullptr);
         if (n < 0) return JFA_ERR_WORKSPACE;
@@ -155,10 +158,14 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
             ok = ok && (sp.n_zero == 0 ||
                         cudaMemcpyAsync(dst + w.zero_off, buf + w.zero_off, sp.n_zero * sizeof(ZeroTile),
                                         cudaMemcpyHostToDevice, stream) == cudaSuccess);
-        if (may_split)
+        if (may_split) {
             ok = ok && (split.n_groups == 0 ||
                         cudaMemcpyAsync(dst + w.split_off, buf + w.split_off, split.n_groups * sizeof(SplitGroup),
                                         cudaMemcpyHostToDevice, stream) == cudaSuccess);
+            ok = ok && (split.n_slots == 0 ||
+                        cudaMemcpyAsync(dst + w.split_blk_off, buf + w.split_blk_off, split.n_slots * sizeof(int32_t),
+                                        cudaMemcpyHostToDevice, stream) == cudaSuccess);
+        }
         return ok ? JFA_OK : JFA_ERR_CUDA;
     });
     if (*st != JFA_OK) return -1;
@@ -395,9 +402,8 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     char* ws = static_cast<char*>(workspace);
     // Broadcast Q (split-KV possible): every SM, since splitting can make
     // more items than the batch has; CTAs left without items exit at once.
-    // The MXFP8 forward does not split (its items look up their sequence's
-    // V scales by sequence index, which a split chunk does not carry).
-    const bool may_split = pr.broadcast_q && !mask && !v_scale;
+    // (An MXFP8 chunk finds its V scales through its slot's first block.)
+    const bool may_split = pr.broadcast_q && !mask;
     const int64_t n_items = may_split ? (int64_t{1} << 30) : count_items(pr, 0);
     const int P = ctas_for(n_items);
     int64_t n_groups = 0;
@@ -437,6 +443,7 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     if (n_groups > 0) {  // split-KV chunks write partials; the merge pass writes their O / LSE
         p.o_part = reinterpret_cast<float*>(ws + w.opart_off);
         p.lse_part = reinterpret_cast<float*>(ws + w.lpart_off);
+        p.split_block0 = reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.split_blk_off);
     }
     if (timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
     if (n_groups > 0 && timed_launch(kProfMerge, s, [&] {

@@ -29,6 +29,9 @@ struct FwdParams {
     // (block_start[b] + n) * H * D + h * D + d; block_start[b] = first block of sequence b.
     const uint32_t* v_scale = nullptr;
     const int32_t* block_start = nullptr;
+    // MXFP8 split-KV chunks: per slot, the first key block of the chunk (in the
+    // numbering of block_start); a chunk's work item carries its slot, not b.
+    const int32_t* split_block0 = nullptr;
 };
 
 struct BwdParams {

@@ -159,7 +159,14 @@ void group_by_q(WorkItem* items, const int32_t* cta_start, int P, int is_bwd) {
 // the longest-first deal: splitting them cost more in chunk overhead and the
 // merge than it gained, e.g. 75.6 vs 67.4 us on the first 256 ads sequences.)
 void split_long_items(std::vector<WorkItem>& gen, std::vector<int64_t>& cost, int P, int64_t max_items,
-                      SplitSpec* split) {
+                      const int32_t* offsets, int B, SplitSpec* split) {
+    // First 128-key block of every sequence (only for slot_block0).
+    std::vector<int64_t> bs;
+    if (split->slot_block0) {
+        bs.resize(static_cast<size_t>(B) + 1);
+        bs[0] = 0;
+        for (int b = 0; b < B; ++b) bs[b + 1] = bs[b] + ceil_div(offsets[b + 1] - offsets[b], kTileRows);
+    }
     int64_t total = 0;
     for (int64_t c : cost) total += c;
     const int64_t avg = total / P;
@@ -191,6 +198,7 @@ void split_long_items(std::vector<WorkItem>& gen, std::vector<int64_t>& cost, in
                 const int64_t j0 = c * chunk, j1 = std::min(nkv, j0 + chunk);
                 const int64_t k0 = j0 * kTileRows, k1 = std::min<int64_t>(w.kv_len, j1 * kTileRows);
                 const int32_t slot = static_cast<int32_t>(split->n_slots++);
+                if (split->slot_block0) split->slot_block0[slot] = static_cast<int32_t>(bs[w.b] + j0);
                 out_items.push_back({-(slot + 1), static_cast<int32_t>(w.kv_start + k0), static_cast<int32_t>(k1 - k0),
                                      pack_item(h, tile + t, 0)});
                 out_cost.push_back((j1 - j0) + 1);
@@ -312,7 +320,7 @@ int64_t build_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
     }
     if (split) split->n_groups = split->n_slots = 0;
     if (split && !is_bwd && broadcast_q && !sparse && policy != kSchedNaive && !gen.empty())
-        split_long_items(gen, cost, P, max_items, split);
+        split_long_items(gen, cost, P, max_items, offsets, B, split);
     const int64_t n = static_cast<int64_t>(gen.size());
 
     // 2. Order: cost-descending, stable (counting sort on the integer cost).
@@ -455,9 +463,10 @@ extern "C" long long jfa_host_build_schedule_sparse(const int32_t* offsets, int 
 // count or -1.
 extern "C" long long jfa_host_build_schedule_split(const int32_t* offsets, int B, int Lq, int H, int P, void* items,
                                                    int32_t* cta_start, long long max_items, void* groups,
-                                                   long long* counts) {
+                                                   long long* counts, int32_t* slot_block0) {
     jfa::SplitSpec sp;
     sp.groups = static_cast<jfa::SplitGroup*>(groups);
+    sp.slot_block0 = slot_block0;  // may be null
     const long long n = jfa::build_schedule(offsets, B, Lq, H, 1, 0, 0, P, jfa::kSchedLptGreedy,
                                             static_cast<jfa::WorkItem*>(items), cta_start, max_items, nullptr, &sp);
     counts[0] = sp.n_groups;

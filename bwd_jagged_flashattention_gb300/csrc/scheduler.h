@@ -124,6 +124,10 @@ static_assert(sizeof(SplitGroup) == 16, "16-byte record");
 struct SplitSpec {
     SplitGroup* groups;               // out: capacity kMaxSplitSlots
     int64_t n_groups = 0, n_slots = 0;
+    // out (if set; capacity kMaxSplitSlots): per slot, the index of its
+    // chunk's first 128-key block over all sequences' blocks in order -- what
+    // the MXFP8 forward needs to find the chunk's V scales.
+    int32_t* slot_block0 = nullptr;
 };
 
 // Build a schedule.  Writes `n` items into `items` (capacity max_items) and

@@ -192,3 +192,20 @@ def test_mxfp8_dense_llm_sampled():
         o_ref, lse_ref, slack = oracle._default().fwd_mxfp8(sub["q"], sub["k"], r8, rs, sub["offsets"], 0, False,
                                                             True, x["scale"], want_slack=True)
         check_mx(o[rows, h0:h1], lse[h0:h1, rows], o_ref, lse_ref, slack, f"dense-LLM sequence {b} heads {h0}:{h1}")
+
+
+@pytest.mark.parametrize("D,Lq", [(128, 256), (64, 300), (128, 128)])
+def test_mxfp8_split_kv(D, Lq):
+    """Split-KV in the MXFP8 forward: a skewed broadcast batch whose long
+    sequence's query tiles the host cuts into key chunks; each chunk finds
+    its V scales through its slot's first key block, writes fp32 partials,
+    and the merge pass combines them.  Checked against the oracle's MXFP8
+    forward like the unsplit cases (a chunk quantizes P exactly as the
+    whole tile would: the shared exponents do not depend on the running
+    max)."""
+    import bwd_jagged_flashattention_gb300 as jfa
+    lengths = [20000, 5, 300, 0, 129, 1000, 1]
+    x = jfa_inputs.custom(len(lengths), Lq, 2, D, lengths, True, False, seed=D + Lq + 7, backward=False)
+    _, _, groups, slots = jfa.host_schedule_split(x["offsets"], x["Lq"], x["H"], jfa.num_ctas())
+    assert len(groups) > 0, "the batch must exercise split-KV"
+    run_case(x, f"MXFP8 split-KV D={D} Lq={Lq} ({len(groups)} tiles, {slots} chunks)")

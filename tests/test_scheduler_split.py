@@ -111,3 +111,29 @@ def test_profiling_case_does_not_split(jfa):
     off = x["offsets"][:257].clone()
     _, _, groups, slots = jfa.host_schedule_split(off, 256, 4, 152)
     assert len(groups) == 0
+
+
+def test_slot_first_blocks(jfa):
+    """Each split slot's first key block, numbered over all sequences' 128-key
+    blocks in order (what the MXFP8 forward looks its V scales up by): the
+    chunk's start row minus its sequence's start, in blocks, plus the blocks
+    of all earlier sequences."""
+    lengths = [20000, 5, 300, 0, 129, 1000, 1, 9000]
+    off = torch.tensor([0] + list(torch.tensor(lengths).cumsum(0)), dtype=torch.int32)
+    items, _, groups, slots, slot_blocks = jfa.host_schedule_split(off, 256, 2, 152, with_slot_blocks=True)
+    assert slots > 0
+    first_block = [0]
+    for L in lengths:
+        first_block.append(first_block[-1] + (L + 127) // 128)
+    seen = 0
+    for g in groups.tolist():
+        b, slot0, n = g[0], g[1], g[2]
+        for c in range(n):
+            slot = slot0 + c
+            it = [r for r in items.tolist() if r[0] == -(slot + 1)]
+            assert len(it) == 1
+            kv_start = it[0][1]
+            assert (kv_start - int(off[b])) % 128 == 0
+            assert int(slot_blocks[slot]) == first_block[b] + (kv_start - int(off[b])) // 128
+            seen += 1
+    assert seen == slots
