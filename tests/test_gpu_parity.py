@@ -88,3 +88,16 @@ def test_repeat_determinism():
     for n in ("o", "lse", "dk", "dv"):
         assert torch.equal(a[n], b[n]), n
     assert (a["dq"] - b["dq"]).abs().max().item() <= 1e-4 * max(1.0, a["dq"].abs().max().item())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Lq", [64, 128])
+def test_broadcast_one_query_tile_many_items(D, Lq):
+    """Broadcast Q of a single query tile (Lq <= 128) with many key-tile
+    items per CTA (60 sequences of up to 3000 keys over the SMs): every item
+    reuses the CTA's resident Q tile, and every CTA walks several items
+    through the single-buffered K/V; dK / dV / dQ against the oracle."""
+    g = torch.Generator().manual_seed(Lq + D)
+    lengths = torch.randint(1, 3000, (60,), generator=g).tolist()
+    x = jfa_inputs.custom(len(lengths), Lq, 2, D, lengths, True, False, seed=Lq * D)
+    _run(x, f"broadcast one query tile D={D} Lq={Lq}")
