@@ -138,3 +138,19 @@ def test_mask_shape_is_checked():
     x = jfa_inputs.custom(2, 32, 2, 64, [130, 5], True, False, seed=1)
     with pytest.raises(ValueError):
         _gpu(x, torch.ones(2, 2, dtype=torch.uint8), backward=False)
+
+
+@pytest.mark.parametrize("policy", ["clc", "queue"])
+@pytest.mark.parametrize("bq", [True, False])
+def test_block_sparse_backward_dealt_at_run_time(policy, bq):
+    """The block-sparse backward with its selected key tiles dealt at run
+    time (Cluster Launch Control, or the per-head-group queues), the
+    unselected ones zeroed as in the static deal."""
+    import bwd_jagged_flashattention_gb300 as jfa
+    x = jfa_inputs.custom(len(LENGTHS), 256 if bq else 0, 2, 128, LENGTHS, bq, False, seed=11 + bq)
+    jfa.set_schedule_policy(bwd_policy=jfa.SCHED_CLC if policy == "clc" else jfa.SCHED_QUEUE)
+    try:
+        for name, mask in _masks(x["offsets"], 2, seed=5).items():
+            _check(x, mask, f"{policy} broadcast={bq} {name}")
+    finally:
+        jfa.set_schedule_policy()
