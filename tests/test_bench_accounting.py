@@ -59,3 +59,20 @@ def test_sparse_accounting_matches_dense_at_the_extremes():
     none = bench.accounting_sparse(x, torch.zeros(nb, 2, dtype=torch.uint8))
     assert none["flops_fwd"] == 0 and none["selected_fraction"] == 0.0
     assert none["bytes_zero"] == 2 * 2 * x["N"] * 2 * 64      # every dK and dV row written as zeros
+
+
+def test_make_inputs_lengths_override():
+    """bench.py --lengths SPEC: the workload's shapes with the given KV
+    lengths ("N" or "NxR" entries), for the fwd+bwd step and the MXFP8
+    forward alike."""
+    import argparse
+    args = argparse.Namespace(workload="extreme", lengths="300,5x3,0,129")
+    x = bench.make_inputs(args)
+    w = jfa_inputs.WORKLOADS["extreme"]
+    assert x["B"] == 6 and x["offsets"].tolist() == [0, 300, 305, 310, 315, 315, 444]
+    assert (x["Lq"], x["H"], x["D"]) == (w.Lq, w.H, w.D) and x["broadcast_q"] == w.broadcast_q
+    assert "do" in x and x["workload"].endswith("300,5x3,0,129")
+    fwd_only = bench.make_inputs(args, backward=False)
+    assert "do" not in fwd_only and fwd_only["offsets"].tolist() == x["offsets"].tolist()
+    plain = bench.make_inputs(argparse.Namespace(workload="tiny", lengths=None))
+    assert plain["B"] == jfa_inputs.WORKLOADS["tiny"].B
