@@ -5,7 +5,7 @@ One step = one pass of the whole hot path over one batch: the host tile
 schedules, the forward kernel (O, LSE), the backward pre-pass (Delta) and the
 backward kernel (dQ summed over the batch, dK, dV), all through the C ABI.
 
-Workload (BASELINE metric's configuration): jagged broadcast-Q attention in
+Workload (the headline metric's configuration): jagged broadcast-Q attention in
 the ads shape, B=512 sequences with lognormal KV lengths (median 256,
 sigma 1, clipped to [8, 4096]), one dense Q [256, 4, 128] shared by every
 sequence, bf16 N(0,1) inputs and upstream gradient, non-causal.  Inputs are
