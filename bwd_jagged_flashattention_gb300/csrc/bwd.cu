@@ -92,13 +92,20 @@ struct BwdBars {
     uint64_t clc_bar;
     uint64_t iq_full[kItemQ], iq_empty[kItemQ];
     int32_t item_q[kItemQ];
-    uint64_t k_full, k_empty, v_full, v_empty;
+    // k_full: the item's K and V tiles landed (one barrier for both loads).
+    // k_empty: every product of the item that reads K or V has completed.
+    uint64_t k_full, k_empty;
     uint64_t q_full[2], q_empty[2];
     uint64_t dl_full[2];  // Delta of the query tile in stats stage [st] is staged
+    // do_full: the tile's dO landed and the dQ warps have read the previous
+    // tile's dQ out of TMEM (the dP^T of this tile overwrites those columns).
     uint64_t do_full, do_empty;
     uint64_t s_full, dp_full, p_full, ds_full, ds_empty;
-    uint64_t dq_full, dq_empty;
-    uint64_t dkv_full, dv_empty, dk_empty;
+    uint64_t dq_full;
+    // There is no barrier for the dK/dV read-out: each compute thread reads
+    // its accumulator rows before it arrives on the next item's first p_full,
+    // and the MMA warp waits on that p_full before the item's first dV and dK.
+    uint64_t dkv_full;
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -237,7 +244,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         prefetch_tensormap(&m->v);
         prefetch_tensormap(&m->dout);
     }
-    uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, do_cnt = 0;
+    uint32_t k_cnt = 0, q_cnt = 0, do_cnt = 0;
     // Broadcast Q: the (head, query tile) each Q stage holds, so a tile that
     // is already resident is not loaded again (the statistics still are).
     // Key = head << 16 | tile (tiles < 2^16 since Lq <= 2^23); -1 = empty.
@@ -288,20 +295,18 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         const int kv_row = it.kv_start + 128 * it.n;
         if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars.k_full, L::kTileBytes);
+            mbar_arrive_expect_tx(&bars.k_full, 2 * L::kTileBytes);  // K and V
 #pragma unroll
             for (int s = 0; s < L::kSlabs; ++s)
                 tma_load_2d(smem + L::kK + s * L::kSlabBytes, &m->k, &bars.k_full, it.h * D + 64 * s, kv_row);
         }
         ++k_cnt;
-        if (!mbar_wait_warp(&bars.v_empty, (v_cnt & 1) ^ 1, ab)) goto done;
+        // V's buffer is free too: k_empty is committed after every product that reads V.
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars.v_full, L::kTileBytes);
 #pragma unroll
             for (int s = 0; s < L::kSlabs; ++s)
-                tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.v_full, it.h * D + 64 * s, kv_row);
+                tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.k_full, it.h * D + 64 * s, kv_row);
         }
-        ++v_cnt;
 
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
@@ -383,7 +388,6 @@ done:
     if (lane == 0 && clc_inflight) mbar_wait_drain(&bars.clc_bar, clc_phase & 1);
     if (lane == 0) {
         if (k_cnt) mbar_wait_drain(&bars.k_full, (k_cnt - 1) & 1);
-        if (v_cnt) mbar_wait_drain(&bars.v_full, (v_cnt - 1) & 1);
         for (uint32_t c = q_cnt > 2 ? q_cnt - 2 : 0; c < q_cnt; ++c) mbar_wait_drain(&bars.q_full[c % 2], (c / 2) & 1);
         if (do_cnt) mbar_wait_drain(&bars.do_full, (do_cnt - 1) & 1);
     }
@@ -419,7 +423,6 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
         }
         const BwdItem it = decode_bwd(p.items[idx], p);
         if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
-        if (!mbar_wait(&bars.v_full, it_cnt & 1, ab)) goto done;
         {  // S^T of the item's first query tile
             const int st = q_cnt % 2;
             if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
@@ -430,14 +433,9 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
             if (!mbar_wait(&bars.do_full, tile_cnt & 1, ab)) goto done;
-            if (!mbar_wait(&bars.dq_empty, (tile_cnt & 1) ^ 1, ab)) goto done;  // previous dQ read out
             tc_fence_after();
             issue_kmajor<D>(lead, tmem + L::kColDP, dV_k, dDO_k);  // dP^T = V dO^T
             mma_commit_p(lead, &bars.dp_full);
-            if (i == it.i1 - 1) mma_commit_p(lead, &bars.v_empty);
-            if (i == it.i0) {  // the previous item's dV has been read out of TMEM
-                if (!mbar_wait(&bars.dv_empty, (it_cnt & 1) ^ 1, ab)) goto done;
-            }
             if (!mbar_wait(&bars.p_full, tile_cnt & 1, ab)) goto done;
             tc_fence_after();
             issue_dv<D>(lead, tmem + L::kColDV, tmem + L::kColS, dDO_mn, i > it.i0);
@@ -450,9 +448,6 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
                 mma_commit_p(lead, &bars.s_full);
             }
             if (!mbar_wait(&bars.ds_full, tile_cnt & 1, ab)) goto done;
-            if (i == it.i0) {  // ... and its dK
-                if (!mbar_wait(&bars.dk_empty, (it_cnt & 1) ^ 1, ab)) goto done;
-            }
             tc_fence_after();
             issue_dq<D>(lead, tmem + L::kColDP, dDS_mn, dK_mn);
             mma_commit_p(lead, &bars.dq_full);
@@ -618,8 +613,9 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
         // halves go TMEM -> registers -> 128-byte-swizzled stage in the
         // warpgroup's slab of the dS tile -> a TMA store of the whole tile, or
         // for a ragged tail tile (which must not touch the next sequence's
-        // rows) coalesced row copies.  The accumulator's columns are released
-        // after its last half is read.
+        // rows) coalesced row copies.  The accumulator's columns are free for
+        // the next item once this thread arrives on that item's first p_full
+        // (the MMA warp waits on it before the item's first dV and dK).
         {
             if (!mbar_wait_warp(&bars.dkv_full, item_cnt & 1, ab)) goto done;
             tc_fence_after();
@@ -640,10 +636,6 @@ __device__ void bwd_compute_role(const BwdParams& p, const BwdMaps* maps, uint8_
                 tmem_ld32(tmem + lane_off + col + half * 64, v[0]);
                 tmem_ld32(tmem + lane_off + col + half * 64 + 32, v[1]);
                 tmem_ld_wait();
-                if (half == D / 64 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(wg ? &bars.dk_empty : &bars.dv_empty);
-                }
                 if (tma_ok && half > 0) {  // the store that used this stage has read it
                     if (row == 0) bulk_wait_group_read<0>();
                     compute_sync(wg);
@@ -698,6 +690,9 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
     uint8_t* stage_base = smem + L::kDQ;
     uint32_t tile_cnt = 0, stage_uses = 0;
     if (issuer) prefetch_tensormap(map_dq);
+    // do_full's phase t also counts the read-out of dQ t-1; for the first
+    // tile there is none, so arrive for it now.
+    mbar_arrive(&bars.do_full);
     ItemRing ring;
     for (int k = ib; k < ie; ++k) {
         int idx = k;
@@ -713,7 +708,8 @@ __device__ void bwd_dq_role(const BwdParams& p, const CUtensorMap* map_dq, uint8
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tmem_ld32(dq_addr + c * 32, v[c]);
             tmem_ld_wait();
-            handoff_arrive(&bars.dq_empty);  // early release: the next dP^T/dQ may overwrite these columns
+            // early release: the next dP^T/dQ may overwrite these columns
+            handoff_arrive(&bars.do_full);
 #pragma unroll
             for (int sl = 0; sl < D / 16; ++sl) {
                 const int st = stage_uses % 2;
@@ -765,14 +761,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(&bars.k_full, 1);
         mbar_init(&bars.k_empty, 1);
-        mbar_init(&bars.v_full, 1);
-        mbar_init(&bars.v_empty, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.q_full[s], 1);
             mbar_init(&bars.q_empty[s], 1);
             mbar_init(&bars.dl_full[s], 1);
         }
-        mbar_init(&bars.do_full, 1);
+        // dO landed (one arrival and the bytes) and, merged in, the dQ warps'
+        // read-out of the previous tile's dQ (128 arrivals).
+        mbar_init(&bars.do_full, 1 + 4 * 32);
         mbar_init(&bars.do_empty, 1);
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.dp_full, 1);
@@ -780,10 +776,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&bars.ds_full, 4 * kCW * 32);
         mbar_init(&bars.ds_empty, 1);
         mbar_init(&bars.dq_full, 1);
-        mbar_init(&bars.dq_empty, 4 * 32);
         mbar_init(&bars.dkv_full, 1);
-        mbar_init(&bars.dv_empty, 128);
-        mbar_init(&bars.dk_empty, 128);
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
     }

@@ -79,7 +79,10 @@ struct FwdLayout {
 struct FwdBars {
     uint64_t q_full, q_empty;
     uint64_t kv_full[2 * kRingSlots], kv_empty[2 * kRingSlots];
-    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    // No barrier for the O read-out: a softmax thread reads its O row out of
+    // TMEM before it arrives on the next item's first p_full of that tile,
+    // and the MMA warp waits on that p_full before the item's first P V.
+    uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -311,7 +314,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                                 : mnmajor_desc(smem_u32(smem + L::kRingOff));
     constexpr uint64_t kTileUnits = L::kTileBytes / 16;  // descriptor step between tiles
     uint32_t ring = 0, q_ph = 0;
-    uint32_t p_ph[2] = {0, 0}, oe_ph[2] = {1, 1};
+    uint32_t p_ph[2] = {0, 0};
     QKey qk;
     WorkItem wn = load_item(p.items, ib, ie), wn2 = load_item(p.items, ib + 1, ie);
     for (int i = ib; i < ie; ++i) {
@@ -352,10 +355,6 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (j >= it.nblk[t]) continue;
-                if (j == 0) {
-                    if (!mbar_wait(&bars.o_empty[t], oe_ph[t], ab)) goto done;
-                    oe_ph[t] ^= 1;
-                }
                 if (!mbar_wait(&bars.p_full[t], p_ph[t], ab)) goto done;
                 p_ph[t] ^= 1;
                 tc_fence_after();
@@ -672,7 +671,6 @@ __device__ void fwd_softmax_role(const FwdParams& p, const CUtensorMap* map_o, u
 #pragma unroll
             for (int oc = 0; oc < D / 32; ++oc) tmem_ld32(o_addr + oc * 32, orr[oc]);
             tmem_ld_wait();
-            handoff_arrive(&bars.o_empty[t]);  // TMEM O is free: the next item's PV may start
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
             if (!kSparse && it.slot >= 0) {  // split-KV chunk: fp32 O and LSE of its keys for the merge pass
                 if (valid) {
@@ -748,7 +746,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mbar_init(&bars.s_full[t], 1);
             mbar_init(&bars.p_full[t], kHandoffCount);
             mbar_init(&bars.o_full[t], 1);
-            mbar_init(&bars.o_empty[t], kHandoffCount);
         }
         mbar_init(&bars.mma_done, 1);
         fence_mbar_init();
