@@ -271,27 +271,38 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = ring % L::kSlots;
                 if (!mbar_wait(&bars.kv_empty[slot], ((ring / L::kSlots) & 1) ^ 1, ab)) goto done;
-                if (kMx && kv) {  // E4M3 V: one box of 128 rows x D bytes
-                    mbar_arrive_expect_tx(&bars.kv_full[slot], 128 * D);
-                    tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes, mv, &bars.kv_full[slot], it.h * D,
+                // V tiles sit at odd ring positions, K tiles at even ones.  A K
+                // tile after the first completes on the barrier of the V tile
+                // before it (V(j) with K(j+1), or an item's last V with the next
+                // item's first K): V's bytes are announced without an arrival,
+                // and K's arrival closes the pair, so the MMA warp waits once per
+                // block.  Both tiles of a pair are released together anyway.
+                uint64_t* full = &bars.kv_full[!kv && ring > 0 ? (ring - 1) % L::kSlots : slot];
+                mbar_expect_tx(full, kMx && kv ? 128 * D : L::kTileBytes);  // E4M3 V: 128 rows x D bytes
+                if (kMx && kv) {
+                    tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes, mv, full, it.h * D,
                                      it.kv_start + 128 * j, kv_policy);
-                    ++ring;
-                    continue;
-                }
-                mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
+                } else {
 #pragma unroll
-                for (int s = 0; s < L::kSlabs; ++s)
-                    tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
-                                     &bars.kv_full[slot], it.h * D + 64 * s,
-                                     it.kv_start + 128 * kv_block<kSparse>(p, it, j), kv_policy);
+                    for (int s = 0; s < L::kSlabs; ++s)
+                        tma_load_2d_hint(smem + L::kRingOff + slot * L::kTileBytes + s * L::kSlabBytes, kv ? mv : mk,
+                                         full, it.h * D + 64 * s, it.kv_start + 128 * kv_block<kSparse>(p, it, j),
+                                         kv_policy);
+                }
+                if (!kv) mbar_arrive(full);
                 ++ring;
             }
         }
     }
 done:
-    // Let every issued copy land before the CTA can exit.
+    // The last V tile has no K after it to close its barrier's phase; with no
+    // tile at all, close the first K's phase, which the MMA warp waits on.
+    if (ring % 2 == 0) mbar_arrive(&bars.kv_full[ring > 0 ? (ring - 1) % L::kSlots : 0]);
+    // Let every issued copy land before the CTA can exit (a K tile completes
+    // with the V tile before it; any older pair has completed, since a later
+    // tile reused its slot).
     for (uint32_t r = ring > L::kSlots ? ring - L::kSlots : 0; r < ring; ++r)
-        mbar_wait_drain(&bars.kv_full[r % L::kSlots], (r / L::kSlots) & 1);
+        if (r == 0 || r % 2 == 1) mbar_wait_drain(&bars.kv_full[r % L::kSlots], (r / L::kSlots) & 1);
     if (q_loads) mbar_wait_drain(&bars.q_full, (q_loads - 1) & 1);
 }
 
@@ -317,6 +328,10 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
     uint32_t p_ph[2] = {0, 0};
     QKey qk;
     WorkItem wn = load_item(p.items, ib, ie), wn2 = load_item(p.items, ib + 1, ie);
+    // Paired ring: only the stream's first K tile has a barrier phase of its
+    // own (the load warp closes it even when it loads nothing); every later K
+    // lands with the V tile before it.
+    if (!mbar_wait(&bars.kv_full[0], 0, ab)) goto done;
     for (int i = ib; i < ie; ++i) {
         const WorkItem wc = wn;
         wn = wn2;  // item i + 1, loaded an iteration ago
@@ -329,8 +344,7 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             qk.set(it);
         }
         const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
-        uint32_t kslot = ring % L::kSlots;
-        if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
+        uint32_t kslot = ring % L::kSlots;  // landed with the V tile before it (or the stream's first K)
         ++ring;
         tc_fence_after();
 #pragma unroll
@@ -343,12 +357,11 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
         if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
-            if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;
+            if (!mbar_wait(&bars.kv_full[vslot], (ring / L::kSlots) & 1, ab)) goto done;  // V(j) and K(j+1)
             ++ring;
             const bool has_next = j + 1 < it.nb;
             if (has_next) {
                 kslot = ring % L::kSlots;
-                if (!mbar_wait(&bars.kv_full[kslot], (ring / L::kSlots) & 1, ab)) goto done;
                 ++ring;
             }
             tc_fence_after();

@@ -55,6 +55,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Raise the transaction bytes the current phase waits for, without an
+// arrival: a later arrive (with or without bytes) closes the phase.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 // One test of a barrier phase (without a suspend-time hint: a hinted wait,
 // which sleeps in hardware until the phase completes, measured 1% slower on
 // the ads backward, 367.5 vs 371.5 us).
