@@ -42,6 +42,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+
 namespace jfa {
 namespace {
 
@@ -92,7 +93,8 @@ struct BwdBars {
     uint64_t clc_bar;
     uint64_t iq_full[kItemQ], iq_empty[kItemQ];
     int32_t item_q[kItemQ];
-    // k_full: the item's K and V tiles landed (one barrier for both loads).
+    // k_full: the item's K and V tiles and its first Q tile landed (one
+    // barrier for the three loads; q_full of that tile covers the statistics).
     // k_empty: every product of the item that reads K or V has completed.
     uint64_t k_full, k_empty;
     uint64_t q_full[2], q_empty[2];
@@ -245,6 +247,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         prefetch_tensormap(&m->dout);
     }
     uint32_t k_cnt = 0, q_cnt = 0, do_cnt = 0;
+    bool k_open = false;  // k_full's phase still waits for its closing arrival
     // Broadcast Q: the (head, query tile) each Q stage holds, so a tile that
     // is already resident is not loaded again (the statistics still are).
     // Key = head << 16 | tile (tiles < 2^16 since Lq <= 2^23); -1 = empty.
@@ -295,7 +298,9 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
         const int kv_row = it.kv_start + 128 * it.n;
         if (!mbar_wait_warp(&bars.k_empty, (k_cnt & 1) ^ 1, ab)) goto done;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars.k_full, 2 * L::kTileBytes);  // K and V
+            // K and V; the item's first Q tile lands on the same barrier, and
+            // its arrival closes the phase.
+            mbar_expect_tx(&bars.k_full, 2 * L::kTileBytes);
 #pragma unroll
             for (int s = 0; s < L::kSlabs; ++s)
                 tma_load_2d(smem + L::kK + s * L::kSlabBytes, &m->k, &bars.k_full, it.h * D + 64 * s, kv_row);
@@ -307,6 +312,7 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             for (int s = 0; s < L::kSlabs; ++s)
                 tma_load_2d(smem + L::kV + s * L::kSlabBytes, &m->v, &bars.k_full, it.h * D + 64 * s, kv_row);
         }
+        k_open = true;
 
         for (int i = it.i0; i < it.i1; ++i) {
             const int st = q_cnt % 2;
@@ -330,21 +336,30 @@ __device__ void bwd_load_role(const BwdParams& p, const BwdMaps* m, uint8_t* sme
             }
             __syncwarp();
             const int key = (it.h << 16) | i;
+            // The item's first Q tile completes on k_full (q_full then only
+            // says that the statistics are staged).
+            const bool first = i == it.i0;
             if (p.broadcast_q && (st == 0 ? stage_key0 : stage_key1) == key) {
-                if (lane == 0) mbar_arrive(&bars.q_full[st]);  // Q_i already resident: statistics only
+                if (lane == 0) {
+                    mbar_arrive(&bars.q_full[st]);  // Q_i already resident: statistics only
+                    if (first) mbar_arrive(&bars.k_full);
+                }
             } else {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&bars.q_full[st], L::kTileBytes);
+                    uint64_t* qbar = first ? &bars.k_full : &bars.q_full[st];
+                    mbar_arrive_expect_tx(qbar, L::kTileBytes);
 #pragma unroll
                     for (int s = 0; s < L::kSlabs; ++s)
-                        tma_load_2d(smem + L::kQ + st * L::kTileBytes + s * L::kSlabBytes, &m->q, &bars.q_full[st],
+                        tma_load_2d(smem + L::kQ + st * L::kTileBytes + s * L::kSlabBytes, &m->q, qbar,
                                     it.h * D + 64 * s, it.q_row0 + 128 * i);
+                    if (first) mbar_arrive(&bars.q_full[st]);
                 }
                 if (st == 0)
                     stage_key0 = key;
                 else
                     stage_key1 = key;
             }
+            if (first) k_open = false;
             ++q_cnt;
             if (!mbar_wait_warp(&bars.do_empty, (do_cnt & 1) ^ 1, ab)) goto done;
             if (lane == 0) {
@@ -387,6 +402,7 @@ done:
     // Let every issued copy (and a pending launch-control response) land before the CTA can exit.
     if (lane == 0 && clc_inflight) mbar_wait_drain(&bars.clc_bar, clc_phase & 1);
     if (lane == 0) {
+        if (k_open) mbar_arrive(&bars.k_full);  // left before the item's first Q tile
         if (k_cnt) mbar_wait_drain(&bars.k_full, (k_cnt - 1) & 1);
         for (uint32_t c = q_cnt > 2 ? q_cnt - 2 : 0; c < q_cnt; ++c) mbar_wait_drain(&bars.q_full[c % 2], (c / 2) & 1);
         if (do_cnt) mbar_wait_drain(&bars.do_full, (do_cnt - 1) & 1);
@@ -422,10 +438,9 @@ __device__ void bwd_mma_role(const BwdParams& p, uint8_t* smem, BwdBars& bars, u
             if ((idx = ring.read(bars, ab)) < 0) break;
         }
         const BwdItem it = decode_bwd(p.items[idx], p);
-        if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;
+        if (!mbar_wait(&bars.k_full, it_cnt & 1, ab)) goto done;  // K, V (and the first Q tile)
         {  // S^T of the item's first query tile
             const int st = q_cnt % 2;
-            if (!mbar_wait(&bars.q_full[st], (q_cnt / 2) & 1, ab)) goto done;
             tc_fence_after();
             issue_kmajor<D>(lead, tmem + L::kColS, dK_k, dQ_k + st * kTileUnits);  // S^T = K Q^T
             mma_commit_p(lead, &bars.s_full);
