@@ -270,7 +270,12 @@ __device__ void fwd_tma_role(const FwdParams& p, const CUtensorMap* mq, const CU
         for (int j = 0; j < it.nb; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = ring % L::kSlots;
-                if (!mbar_wait(&bars.kv_empty[slot], ((ring / L::kSlots) & 1) ^ 1, ab)) goto done;
+                // Releases come in the same pairs (one commit frees V(j) and K(j+1)),
+                // so a K tile's slot is free once the V slot before it was; only
+                // the stream's first K, alone, has a release of its own.
+                if ((kv || ring == L::kSlots) &&
+                    !mbar_wait(&bars.kv_empty[slot], ((ring / L::kSlots) & 1) ^ 1, ab))
+                    goto done;
                 // V tiles sit at odd ring positions, K tiles at even ones.  A K
                 // tile after the first completes on the barrier of the V tile
                 // before it (V(j) with K(j+1), or an item's last V with the next
@@ -344,7 +349,8 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
             qk.set(it);
         }
         const bool release_q = !next_item_reuses_q<kSparse>(p, it, wn, i, ie);  // this item is the run's last Q user
-        uint32_t kslot = ring % L::kSlots;  // landed with the V tile before it (or the stream's first K)
+        const uint32_t kpos = ring;
+        uint32_t kslot = kpos % L::kSlots;  // landed with the V tile before it (or the stream's first K)
         ++ring;
         tc_fence_after();
 #pragma unroll
@@ -353,7 +359,8 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                 issue_qk<D>(lead, tmem + t * 128, q_desc + t * kTileUnits, k_desc + kslot * kTileUnits);
                 mma_commit_p(lead, &bars.s_full[t]);
             }
-        mma_commit_p(lead, &bars.kv_empty[kslot]);
+        // (paired: this K frees its slot together with the previous item's last V)
+        mma_commit_p(lead, &bars.kv_empty[kpos > 0 ? (kpos - 1) % L::kSlots : kslot]);
         if (it.nb == 1 && release_q) mma_commit_p(lead, &bars.q_empty);
         for (int j = 0; j < it.nb; ++j) {
             const uint32_t vslot = ring % L::kSlots;
@@ -381,9 +388,10 @@ __device__ void fwd_mma_role(const FwdParams& p, uint8_t* smem, FwdBars& bars, u
                     mma_commit_p(lead, &bars.s_full[t]);
                 }
             }
-            mma_commit_p(lead, &bars.kv_empty[vslot]);
+            // V(j) and K(j+1) are free: one commit for the pair (an item's last V
+            // goes with the next item's first K)
             if (has_next) {
-                mma_commit_p(lead, &bars.kv_empty[kslot]);
+                mma_commit_p(lead, &bars.kv_empty[vslot]);
                 if (j + 2 == it.nb && release_q) mma_commit_p(lead, &bars.q_empty);
             }
         }
