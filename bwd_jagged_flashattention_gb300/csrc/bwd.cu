@@ -42,7 +42,6 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
-
 namespace jfa {
 namespace {
 
