@@ -101,3 +101,18 @@ def test_broadcast_one_query_tile_many_items(D, Lq):
     lengths = torch.randint(1, 3000, (60,), generator=g).tolist()
     x = jfa_inputs.custom(len(lengths), Lq, 2, D, lengths, True, False, seed=Lq * D)
     _run(x, f"broadcast one query tile D={D} Lq={Lq}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bq", [True, False])
+def test_many_items_per_cta_with_empty_sequences(D, bq):
+    """Several items per CTA (700 short sequences over the SMs), with empty
+    sequences between them: each CTA's K/V ring (4 slots at D = 128, 8 at
+    D = 64) wraps across items, so a V tile and the next item's first K share
+    a barrier phase and a release, with empty items skipped in between; the
+    backward walks several key tiles per CTA the same way."""
+    g = torch.Generator().manual_seed(31 + D + bq)
+    pool = torch.tensor([0, 0, 1, 5, 64, 127, 128, 129, 200, 256, 300])
+    lengths = pool[torch.randint(0, len(pool), (700,), generator=g)].tolist()
+    x = jfa_inputs.custom(len(lengths), 64 if bq else 0, 1, D, lengths, bq, False, seed=41 + D)
+    _run(x, f"many items per CTA D={D} broadcast={bq}")
