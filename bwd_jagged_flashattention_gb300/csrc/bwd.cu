@@ -856,6 +856,12 @@ cudaError_t launch_bwd_d(const BwdParams& p, const BwdMaps& m, int grid, cudaStr
 // 51.3 us).
 template <int D>
 __global__ void __launch_bounds__(256) jfa_bwd_pre_kernel(const PreParams p) {
+    // The main kernel's tile schedule, from the pinned host buffer the host
+    // built it in (instead of a host-to-device copy in the stream before this
+    // kernel).
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < p.sched_vec16;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        p.sched_dst[e] = p.sched_src[e];
     // dQ starts at zero (the main kernel adds every tile's dQ into it).
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < p.dq_vec4;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x)

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <vector>
 
@@ -115,13 +116,20 @@ jfa_status with_stage(size_t need, cudaStream_t stream, F&& fill) {
     return JFA_OK;
 }
 
+// Moves a staged schedule (device-mapped pinned source, byte count) into the
+// workspace region by a kernel the caller launches anyway.
+using ScheduleUpload = std::function<cudaError_t(const void* src_dev, size_t bytes)>;
+
 // Builds the schedule into a pinned slot laid out like the workspace region
-// (WsLayout) and enqueues its copy into ws_region.  With a block mask
-// (block-sparse) the selection tables follow; *n_zero receives the number of
-// unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
+// (WsLayout) and enqueues its copy into ws_region -- or, given `upload` and a
+// non-empty schedule, has upload move the CTA bounds and items (the slot is
+// then read by upload's kernel, which its reuse event follows).  With a block
+// mask (block-sparse) the selection tables follow; *n_zero receives the number
+// of unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
 int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
                        int policy, const WsLayout& w, const uint8_t* mask, void* ws_region, cudaStream_t stream,
-                       int64_t* n_zero, int64_t* n_split_groups, jfa_status* st) {
+                       int64_t* n_zero, int64_t* n_split_groups, jfa_status* st,
+                       const ScheduleUpload* upload = nullptr) {
     const int64_t max_items = w.max_items;
     const bool may_split = JFA_FWD_SPLIT_KV && !is_bwd && !mask && broadcast_q && n_split_groups;
     const size_t need = (mask || may_split) ? (is_bwd ? w.bwd_region : w.fwd_region)
@@ -146,7 +154,13 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         if (n < 0) return JFA_ERR_WORKSPACE;
         char* dst = static_cast<char*>(ws_region);
         const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
-        bool ok = cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+        void* src_dev = nullptr;
+        if (upload && n > 0 && cudaHostGetDevicePointer(&src_dev, buf, 0) != cudaSuccess) {
+            cudaGetLastError();  // not mapped: clear the error and copy instead
+            src_dev = nullptr;
+        }
+        bool ok = src_dev ? (*upload)(src_dev, bytes) == cudaSuccess
+                          : cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, stream) == cudaSuccess;
         if (mask && !is_bwd) {
             ok = ok && cudaMemcpyAsync(dst + w.sel_off, buf + w.sel_off, static_cast<size_t>(B) * H * sizeof(SparseSel),
                                        cudaMemcpyHostToDevice, stream) == cudaSuccess;
@@ -536,8 +550,9 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
         return JFA_OK;
     }
 
-    // Stream order: schedule copy, zeroed dK/dV of unselected tiles
-    // (block-sparse), the Delta pre-pass (which also zeroes dQ), then the
+    // Stream order: schedule copy (dense: done by the Delta pass itself),
+    // zeroed dK/dV of unselected tiles (block-sparse), the Delta pre-pass
+    // (which also zeroes dQ), then the
     // main kernel.
     // Cluster Launch Control: the cost-sorted list (built as a one-CTA
     // schedule), one CTA per item; queues: one CTA per SM taking items from
@@ -548,18 +563,6 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     const bool queue = policy == kSchedQueue;
     const int64_t n_items = count_items(pr, 1);
     const int P = clc ? 1 : ctas_for(n_items);
-    int64_t n_zero = 0;
-    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P,
-                                     policy, w, mask, ws + w.bwd_off, s, &n_zero, nullptr, &st);
-    if (n < 0) return st;
-    if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
-                          return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
-                                                   n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
-                                                   D, s);
-                      }) != cudaSuccess)
-        return JFA_ERR_CUDA;
-    if (n == 0) return q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess ? JFA_ERR_CUDA
-                                                                                                 : JFA_OK;
 
     float* delta = reinterpret_cast<float*>(ws + w.delta_off);
     PreParams pp;
@@ -575,6 +578,33 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     pp.N = static_cast<int>(pr.N);
     pp.D = D;
     pp.broadcast_q = pr.broadcast_q;
+
+    // Dense: the Delta pass, which runs right before the main kernel anyway,
+    // moves the schedule from the pinned staging slot into the workspace, so
+    // the stream holds no separate host-to-device copy.  (Block-sparse: the
+    // zero-tile kernel reads the schedule region before the Delta pass, so
+    // the schedule is copied as before.)
+    bool pre_launched = false;
+    const ScheduleUpload upload = [&](const void* src_dev, size_t bytes) {
+        pp.sched_src = static_cast<const uint4*>(src_dev);
+        pp.sched_dst = reinterpret_cast<uint4*>(ws + w.bwd_off);
+        pp.sched_vec16 = static_cast<int64_t>(bytes / 16);
+        pre_launched = true;
+        return timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); });
+    };
+    int64_t n_zero = 0;
+    const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 1, P,
+                                     policy, w, mask, ws + w.bwd_off, s, &n_zero, nullptr, &st,
+                                     mask ? nullptr : &upload);
+    if (n < 0) return st;
+    if (n_zero > 0 && timed_launch(kProfZero, s, [&] {
+                          return launch_zero_tiles(reinterpret_cast<const ZeroTile*>(ws + w.bwd_off + w.zero_off),
+                                                   n_zero, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), H,
+                                                   D, s);
+                      }) != cudaSuccess)
+        return JFA_ERR_CUDA;
+    if (n == 0) return q_rows > 0 && cudaMemsetAsync(dq, 0, elems_q * sizeof(float), s) != cudaSuccess ? JFA_ERR_CUDA
+                                                                                                 : JFA_OK;
 
     BwdMaps maps;
     if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
@@ -603,7 +633,8 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
     p.scale_log2 = pr.scale * 1.4426950408889634f;
     p.wait_ns = wait_limit_ns();
     const int grid = clc ? static_cast<int>(n) : P;
-    if (timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess) return JFA_ERR_CUDA;
+    if (!pre_launched && timed_launch(kProfPre, s, [&] { return launch_bwd_pre(pp, s); }) != cudaSuccess)
+        return JFA_ERR_CUDA;
     if (timed_launch(kProfBwd, s, [&] { return launch_bwd(D, p, maps, grid, s); }) != cudaSuccess) return JFA_ERR_CUDA;
     return JFA_OK;
 }

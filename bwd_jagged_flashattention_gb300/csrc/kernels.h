@@ -67,6 +67,11 @@ struct PreParams {
     int64_t rows;              // number of (row, head) pairs = O rows * H
     int B, Lq, H, N, D;
     int broadcast_q;
+    // Optional: the backward's tile schedule, copied by this kernel from the
+    // host's pinned staging buffer (its device mapping) into the workspace.
+    const uint4* sched_src = nullptr;
+    uint4* sched_dst = nullptr;
+    int64_t sched_vec16 = 0;
 };
 
 #ifdef __CUDACC__
