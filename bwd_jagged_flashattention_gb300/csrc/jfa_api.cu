@@ -155,7 +155,10 @@ int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadca
         char* dst = static_cast<char*>(ws_region);
         const size_t bytes = kCtaStartBytes + static_cast<size_t>(n) * sizeof(WorkItem);
         void* src_dev = nullptr;
-        if (upload && n > 0 && cudaHostGetDevicePointer(&src_dev, buf, 0) != cudaSuccess) {
+        // (only for the CTA bounds and items alone: with selection or split
+        // tables after them, everything is copied)
+        const bool extras = mask || (may_split && split.n_groups > 0);
+        if (upload && n > 0 && !extras && cudaHostGetDevicePointer(&src_dev, buf, 0) != cudaSuccess) {
             cudaGetLastError();  // not mapped: clear the error and copy instead
             src_dev = nullptr;
         }
@@ -420,46 +423,66 @@ static jfa_status fwd_impl(const void* q, const void* k, const void* v, const in
     const bool may_split = pr.broadcast_q && !mask;
     const int64_t n_items = may_split ? (int64_t{1} << 30) : count_items(pr, 0);
     const int P = ctas_for(n_items);
+    FwdMaps maps;
+    FwdParams p;
+    auto build = [&]() -> bool {
+        const bool v_ok = v_scale ? map_rows_e4m3(&maps.v, v, pr.N, H, D, workspace)
+                                  : map_rows_bf16(&maps.v, v, pr.N, H, D, workspace);
+        if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
+            !v_ok || !map_rows_bf16(&maps.o, o, o_rows, H, D, workspace))
+            return false;
+        p.cta_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off);
+        p.items = reinterpret_cast<const WorkItem*>(ws + w.fwd_off + kCtaStartBytes);
+        p.o = static_cast<uint16_t*>(o);
+        p.lse = lse;
+        p.status = reinterpret_cast<uint32_t*>(ws);
+        p.Lq = pr.Lq;
+        p.H = H;
+        p.N = static_cast<int>(pr.N);
+        p.broadcast_q = pr.broadcast_q;
+        p.causal = pr.causal;
+        p.scale_log2 = pr.scale * 1.4426950408889634f;
+        p.wait_ns = wait_limit_ns();
+        p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
+        p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
+        if (v_scale) {
+            p.v_scale = static_cast<const uint32_t*>(v_scale);
+            p.block_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off);
+        }
+        return true;
+    };
+    // Plain forward (no block-sparse lists, no MXFP8 block table): the kernel
+    // reads its CTA bounds and work items straight from the pinned staging
+    // slot (through the slot's device mapping; every role reads items one
+    // iteration ahead) and is launched from inside the staging call, so the
+    // slot's reuse event follows it: no host-to-device copy in the stream.
+    // With split-KV tables after the items, they are all copied as before.
+    const bool direct = !mask && !v_scale && pr.N > 0;
+    if (direct && !build()) return JFA_ERR_CUDA;
+    bool launched = false;
+    const ScheduleUpload upload = [&](const void* src_dev, size_t) {
+        p.cta_start = static_cast<const int32_t*>(src_dev);
+        p.items = reinterpret_cast<const WorkItem*>(static_cast<const char*>(src_dev) + kCtaStartBytes);
+        launched = true;
+        return timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); });
+    };
     int64_t n_groups = 0;
     const int64_t n = stage_schedule(pr.off, pr.B, pr.Lq, pr.H, pr.broadcast_q, pr.causal, 0, P, g_fwd_policy.load(),
-                                     w, mask, ws + w.fwd_off, s, nullptr, may_split ? &n_groups : nullptr, &st);
+                                     w, mask, ws + w.fwd_off, s, nullptr, may_split ? &n_groups : nullptr, &st,
+                                     direct ? &upload : nullptr);
     if (n < 0) return st;
     if (n == 0) return JFA_OK;
     int64_t n_blocks = 0;
     if (v_scale && (st = stage_block_starts(pr.off, pr.B, ws + w.fwd_off + w.blocks_off, s, &n_blocks)) != JFA_OK)
         return st;
-
-    FwdMaps maps;
-    const bool v_ok = v_scale ? map_rows_e4m3(&maps.v, v, pr.N, H, D, workspace)
-                              : map_rows_bf16(&maps.v, v, pr.N, H, D, workspace);
-    if (!map_rows_bf16(&maps.q, q, q_rows, H, D, workspace) || !map_rows_bf16(&maps.k, k, pr.N, H, D, workspace) ||
-        !v_ok || !map_rows_bf16(&maps.o, o, o_rows, H, D, workspace))
-        return JFA_ERR_CUDA;
-    FwdParams p;
-    p.cta_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off);
-    p.items = reinterpret_cast<const WorkItem*>(ws + w.fwd_off + kCtaStartBytes);
-    p.o = static_cast<uint16_t*>(o);
-    p.lse = lse;
-    p.status = reinterpret_cast<uint32_t*>(ws);
-    p.Lq = pr.Lq;
-    p.H = H;
-    p.N = static_cast<int>(pr.N);
-    p.broadcast_q = pr.broadcast_q;
-    p.causal = pr.causal;
-    p.scale_log2 = pr.scale * 1.4426950408889634f;
-    p.wait_ns = wait_limit_ns();
-    p.sel = mask ? reinterpret_cast<const SparseSel*>(ws + w.fwd_off + w.sel_off) : nullptr;
-    p.sel_blocks = mask ? reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off) : nullptr;
-    if (v_scale) {
-        p.v_scale = static_cast<const uint32_t*>(v_scale);
-        p.block_start = reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.blocks_off);
-    }
+    if (!direct && !build()) return JFA_ERR_CUDA;
     if (n_groups > 0) {  // split-KV chunks write partials; the merge pass writes their O / LSE
         p.o_part = reinterpret_cast<float*>(ws + w.opart_off);
         p.lse_part = reinterpret_cast<float*>(ws + w.lpart_off);
         p.split_block0 = reinterpret_cast<const int32_t*>(ws + w.fwd_off + w.split_blk_off);
     }
-    if (timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) != cudaSuccess) return JFA_ERR_CUDA;
+    if (!launched && timed_launch(kProfFwd, s, [&] { return launch_fwd(D, p, maps, P, s); }) != cudaSuccess)
+        return JFA_ERR_CUDA;
     if (n_groups > 0 && timed_launch(kProfMerge, s, [&] {
                             return launch_fwd_merge(D, reinterpret_cast<const SplitGroup*>(ws + w.fwd_off + w.split_off),
                                                     n_groups, p.o_part, p.lse_part, static_cast<uint16_t*>(o), lse,

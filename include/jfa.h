@@ -40,10 +40,11 @@
  *
  * Ownership and concurrency.  The caller owns every device buffer and the
  * stream.  The library allocates no device memory; it keeps a small pinned
- * host staging ring per device for the tile schedule (the forward copies it
- * into the workspace; the dense backward's Delta pass reads it through its
- * device mapping and writes it there, falling back to a copy where the ring
- * is not mapped).  Scratch memory (the
+ * host staging ring per device for the tile schedule: the plain forward's
+ * kernel reads its work list there through the ring's device mapping, the
+ * dense backward's Delta pass moves it into the workspace the same way, and
+ * the other paths (block-sparse, MXFP8, split-KV tables) copy it into the
+ * workspace; where the ring is not mapped, it is copied.  Scratch memory (the
  * tile schedule, the backward row statistics and a status word) lives in the
  * caller's `workspace`, which must hold jfa_workspace_bytes(...) bytes and
  * must not be shared by calls that may run concurrently.  Calls are
