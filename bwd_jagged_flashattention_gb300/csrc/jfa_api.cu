@@ -116,14 +116,16 @@ jfa_status with_stage(size_t need, cudaStream_t stream, F&& fill) {
     return JFA_OK;
 }
 
-// Moves a staged schedule (device-mapped pinned source, byte count) into the
-// workspace region by a kernel the caller launches anyway.
+// Hands a staged schedule (its device-mapped pinned source and byte count) to
+// a kernel launched from inside the staging call, which either moves it into
+// the workspace region (the backward's Delta pass) or reads it where it is
+// (the forward kernel).
 using ScheduleUpload = std::function<cudaError_t(const void* src_dev, size_t bytes)>;
 
 // Builds the schedule into a pinned slot laid out like the workspace region
 // (WsLayout) and enqueues its copy into ws_region -- or, given `upload` and a
-// non-empty schedule, has upload move the CTA bounds and items (the slot is
-// then read by upload's kernel, which its reuse event follows).  With a block
+// non-empty schedule of CTA bounds and items alone, calls upload instead (the
+// slot is then read by upload's kernel, which its reuse event follows).  With a block
 // mask (block-sparse) the selection tables follow; *n_zero receives the number
 // of unselected backward tiles.  Returns the item count (>= 0) or -1 on error.
 int64_t stage_schedule(const int32_t* offsets, int B, int Lq, int H, int broadcast_q, int causal, int is_bwd, int P,
@@ -575,8 +577,7 @@ static jfa_status bwd_impl(const void* q, const void* k, const void* v, const vo
 
     // Stream order: schedule copy (dense: done by the Delta pass itself),
     // zeroed dK/dV of unselected tiles (block-sparse), the Delta pre-pass
-    // (which also zeroes dQ), then the
-    // main kernel.
+    // (which also zeroes dQ), then the main kernel.
     // Cluster Launch Control: the cost-sorted list (built as a one-CTA
     // schedule), one CTA per item; queues: one CTA per SM taking items from
     // its head group's queue at run time; otherwise a static deal to one CTA
